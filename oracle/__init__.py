@@ -1,0 +1,222 @@
+"""CPU oracle for the W8A8_DYNAMIC linear layer and MoE-expert chain.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only users.  The product path (the CUDA
+library under ``w8a8_dynamic_quant_gb300``) never imports this package, and
+this package never imports the product.
+
+Every function is a thin numpy <-> C marshalling layer over
+``w8a8_oracle.c``; the arithmetic and its page citations live in that file.
+BF16 tensors travel as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+_c_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _load(_build.build())
+    return _lib
+
+
+def use_library(path: str):
+    """Point this wrapper at another build of the oracle source (the mutation
+    tests load deliberately broken copies this way); returns the previous one."""
+    global _lib
+    with _lock:
+        prev = _lib
+        _lib = _load(path)
+    return prev
+
+
+def restore_library(prev):
+    global _lib
+    with _lock:
+        _lib = prev
+
+
+def _load(path: str) -> ctypes.CDLL:
+    L = ctypes.CDLL(path)
+    L.oracle_num_threads.restype = ctypes.c_int
+    L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_f32.restype = ctypes.c_float
+    L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.oracle_exp_f32.argtypes = [ctypes.c_float]
+    L.oracle_exp_f32.restype = ctypes.c_float
+    L.oracle_dynamic_quant.argtypes = [_vp, _c_i64, _c_i64, _vp, _vp]
+    L.oracle_int8_gemm_acc.argtypes = [_vp, _c_i64, _c_i64, _vp, _c_i64, _vp]
+    L.oracle_epilogue.argtypes = [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _vp]
+    L.oracle_quant_matmul.argtypes = [_vp, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _vp, _vp]
+    L.oracle_check_group_list.argtypes = [_vp, _c_i64, _c_i64]
+    L.oracle_grouped_matmul.argtypes = [_vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _vp, _vp,
+                                        _c_i64, _vp, _vp]
+    L.oracle_swiglu.argtypes = [_vp, _c_i64, _c_i64, _vp]
+    L.oracle_moe_w13_swiglu_requant_w2.argtypes = [
+        _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, _vp,
+        _vp, _vp, _vp, _vp, _vp, _vp]
+    return L
+
+
+class OracleError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned status {code}")
+        self.code = code
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.dtype(dtype):
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise OracleError(fn, rc)
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()
+
+
+def bf16_to_f32(b: int) -> float:
+    return lib().oracle_bf16_to_f32(int(b))
+
+
+def f32_to_bf16(f: float) -> int:
+    return lib().oracle_f32_to_bf16(float(f))
+
+
+def exp_f32(x: float) -> float:
+    """The binary32 exp specification used by SwiGLU (scalar)."""
+    return lib().oracle_exp_f32(float(x))
+
+
+def dynamic_quant(x_bf16: np.ndarray):
+    """BF16 bits [M,K] -> (int8 q [M,K], fp32 scale [M])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.int8)
+    s = np.empty((M,), np.float32)
+    _check("oracle_dynamic_quant", lib().oracle_dynamic_quant(_p(x), M, K, _p(q), _p(s)))
+    return q, s
+
+
+def int8_gemm_acc(q: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """int8 q [M,K] x int8 W [N,K] -> exact int32 acc [M,N]."""
+    q = _c(q, np.int8)
+    w = _c(w, np.int8)
+    M, K = q.shape
+    N = w.shape[0]
+    assert w.shape[1] == K
+    acc = np.empty((M, N), np.int32)
+    _check("oracle_int8_gemm_acc", lib().oracle_int8_gemm_acc(_p(q), M, K, _p(w), N, _p(acc)))
+    return acc
+
+
+def epilogue(acc, x_scale, w_scale, bias=None) -> np.ndarray:
+    acc = _c(acc, np.int32)
+    M, N = acc.shape
+    xs = _c(x_scale, np.float32)
+    ws = _c(w_scale, np.float32)
+    b = None if bias is None else _c(bias, np.uint16)
+    y = np.empty((M, N), np.uint16)
+    _check("oracle_epilogue", lib().oracle_epilogue(_p(acc), M, N, _p(xs), _p(ws), _p(b), _p(y)))
+    return y
+
+
+def quant_matmul(q, x_scale, w, w_scale, bias=None) -> np.ndarray:
+    """int8 q [M,K], fp32 x_scale [M], int8 W [N,K], fp32 w_scale [N], bf16 bias [N]|None -> bf16 [M,N]."""
+    q = _c(q, np.int8)
+    xs = _c(x_scale, np.float32)
+    w = _c(w, np.int8)
+    ws = _c(w_scale, np.float32)
+    b = None if bias is None else _c(bias, np.uint16)
+    M, K = q.shape
+    N = w.shape[0]
+    y = np.empty((M, N), np.uint16)
+    _check("oracle_quant_matmul",
+           lib().oracle_quant_matmul(_p(q), _p(xs), M, K, _p(w), _p(ws), N, _p(b), _p(y)))
+    return y
+
+
+def check_group_list(group_list, R) -> int:
+    g = _c(group_list, np.int64)
+    return lib().oracle_check_group_list(_p(g), g.shape[0], int(R))
+
+
+def grouped_matmul(q, x_scale, group_list, w, w_scale, want_acc=False):
+    """int8 q [R,K], fp32 x_scale [R], int64 counts [E], int8 W [E,N,K], fp32 w_scale [E,N] -> bf16 [R,N] (, int32 acc)."""
+    q = _c(q, np.int8)
+    xs = _c(x_scale, np.float32)
+    g = _c(group_list, np.int64)
+    w = _c(w, np.int8)
+    ws = _c(w_scale, np.float32)
+    R, K = q.shape
+    E, N, K2 = w.shape
+    assert K2 == K and g.shape[0] == E
+    y = np.empty((R, N), np.uint16)
+    acc = np.empty((R, N), np.int32) if want_acc else None
+    _check("oracle_grouped_matmul",
+           lib().oracle_grouped_matmul(_p(q), _p(xs), _p(g), E, R, K, _p(w), _p(ws), N, _p(y), _p(acc)))
+    return (y, acc) if want_acc else y
+
+
+def swiglu(y13: np.ndarray, I: int) -> np.ndarray:
+    y13 = _c(y13, np.uint16)
+    R = y13.shape[0]
+    assert y13.shape[1] == 2 * I
+    h = np.empty((R, I), np.uint16)
+    _check("oracle_swiglu", lib().oracle_swiglu(_p(y13), R, I, _p(h)))
+    return h
+
+
+def moe_w13_swiglu_requant_w2(x, x_scale, group_list, w13, s13, w2, s2, intermediates=False):
+    """MoE expert FFN.  x: bf16 bits [R,H] if x_scale is None, else int8 [R,H]."""
+    g = _c(group_list, np.int64)
+    w13 = _c(w13, np.int8)
+    s13 = _c(s13, np.float32)
+    w2 = _c(w2, np.int8)
+    s2 = _c(s2, np.float32)
+    E, twoI, H = w13.shape
+    I = twoI // 2
+    assert w2.shape == (E, H, I) and s13.shape == (E, twoI) and s2.shape == (E, H)
+    if x_scale is None:
+        x = _c(x, np.uint16)
+        xs_in = None
+    else:
+        x = _c(x, np.int8)
+        xs_in = _c(x_scale, np.float32)
+    R = x.shape[0]
+    assert x.shape[1] == H
+    y = np.empty((R, H), np.uint16)
+    inter = {}
+    if intermediates:
+        inter = dict(xq=np.empty((R, H), np.int8), xs=np.empty((R,), np.float32),
+                     y13=np.empty((R, twoI), np.uint16), h=np.empty((R, I), np.uint16),
+                     hq=np.empty((R, I), np.int8), hs=np.empty((R,), np.float32))
+    _check("oracle_moe_w13_swiglu_requant_w2",
+           lib().oracle_moe_w13_swiglu_requant_w2(
+               _p(x), _p(xs_in), _p(g), E, R, H, I, _p(w13), _p(s13), _p(w2), _p(s2), _p(y),
+               _p(inter.get("xq")), _p(inter.get("xs")), _p(inter.get("y13")),
+               _p(inter.get("h")), _p(inter.get("hq")), _p(inter.get("hs"))))
+    return (y, inter) if intermediates else y

@@ -1,0 +1,364 @@
+/*
+ * w8a8_oracle.c -- plain, slow, obviously-correct CPU oracle for the
+ * W8A8_DYNAMIC linear layer and its MoE-expert counterpart.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this library.  The product path
+ * (the CUDA library) shares no code, header, table or helper with it.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [P1] "DeepSeek-V4 W8A8 执行链从量化权重到 Ascend INT8 算子"
+ *        §一  (quantisation recipe: act per_token int8 symmetric,
+ *              weight per_channel int8 symmetric; W13 = gate_proj + up_proj,
+ *              W2 = down_proj)
+ *        §二  (Dense: npu_dynamic_quant -> INT8 [M,K] + per-token scale [M];
+ *              npu_quant_matmul(q, W, weight_scale, pertoken_scale, bias,
+ *              output_dtype=bf16) -> BF16 [M,N])
+ *        §三  (MoE: npu_grouped_matmul over group_list = rows per expert;
+ *              Routed Hidden -> W13 GMM -> SwiGLU -> Requant -> W2 GMM -> BF16;
+ *              "if pertoken_scale is None: quantise", i.e. no double quant)
+ *        §四  (Atlas A3 operator contract: INT8 x1, INT8 x2, FLOAT32 per-token
+ *              scale, BF16 output)
+ *   [P3] "超大 MoE 的低比特推理：INT4、FP4 与量化感知训练", section
+ *        "为什么要量化感知训练" (fake_int4: scale = group absmax / qmax, then
+ *        divide, round half-to-even, clamp).
+ *
+ * Arithmetic (readings where the pages are silent are marked READING):
+ *   quant    amax = max_k |x|, s = amax / 127 (binary32 divide),
+ *            q = clamp(rint(x / s), -127, 127), rint = ties-to-even;
+ *            READING: divide by s (not multiply by a reciprocal), as in [P3];
+ *            READING: a row with amax == 0 gets s = 0 and q = 0.
+ *   gemm     acc[m,n] = sum_k int32(q[m,k]) * int32(W[n,k])  (exact int32).
+ *   epilogue t = float(acc) (RNE); t = t * s_x[m]; t = t * s_w[n];
+ *            t = t + float(bias[n]) if bias; y = bf16_rne(t).  No FMA.
+ *            READING: scale order x-scale first, bias added after scaling.
+ *   grouped  group_list holds per-expert ROW COUNTS (not offsets); rows of
+ *            expert e are [sum_{j<e} cnt_j, + cnt_e); counts >= 0, sum == R.
+ *   swiglu   g = y13[r, j], u = y13[r, I + j] (bf16 values of the W13 output,
+ *            gate = first I output channels, up = last I);
+ *            h = bf16_rne((g * sigmoid(g)) * u), sigmoid(g) = 1 / (1 + exp(-g))
+ *            in binary32, exp = the specification in oracle_exp_f32 below.
+ *   requant  quant applied to h over its I columns.
+ *   W2       grouped GEMM with W2 [E,H,I], no bias, BF16 out.
+ *   skip     a non-NULL x_scale means x is already INT8 + per-token scale and
+ *            is not quantised again.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared
+ * (contraction off: no hidden FMA may change a rounding).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_SHAPE 2
+#define ORC_ERR_GROUP_LIST 5
+#define ORC_ERR_ALLOC 9
+
+/* Largest reduction depth for which |acc| <= K * 128 * 127 < 2^31. */
+#define ORC_MAX_K 131072
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+float oracle_bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* binary32 -> bfloat16, round to nearest, ties to even. */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+    return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays a quiet NaN */
+  uint32_t keep_lsb = (u >> 16) & 1u;
+  u += 0x7fffu + keep_lsb;
+  return (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------- exp (binary32) -- */
+/*
+ * e^x by Cody & Waite argument reduction (W. J. Cody, W. Waite, "Software
+ * Manual for the Elementary Functions", 1980) and the degree-7 Taylor
+ * polynomial of e^r, evaluated by Horner's rule with fused multiply-adds:
+ *
+ *   n  = rint(x * log2e)                 log2e  = binary32(1 / ln 2)
+ *   r  = fma(-n, ln2_hi, x)              ln2_hi = ln 2 cut to 15 significant
+ *   r  = fma(-n, ln2_lo, r)                       bits, so n*ln2_hi is exact
+ *                                        ln2_lo = binary32(ln 2 - ln2_hi)
+ *   p  = c7; p = fma(p, r, c_k) for k = 6..0,  c_k = binary32(1 / k!)
+ *   e^x = (p * 2^(n/2)) * 2^(n - n/2)    (n/2 truncates; both factors normal)
+ *
+ * x > 89 gives +inf, x < -104 gives +0, NaN propagates.  Every step is a
+ * correctly rounded binary32 operation, so any implementation that follows
+ * these steps gets the same bits.  The constants are the mathematical values
+ * above rounded to binary32 (hex given for checking).
+ */
+static float pow2_normal(int k) { /* 2^k for -126 <= k <= 127 */
+  uint32_t u = (uint32_t)(k + 127) << 23;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+float oracle_exp_f32(float x) {
+  if (x != x) return x;
+  if (x > 89.0f) return INFINITY;
+  if (x < -104.0f) return 0.0f;
+  const float log2e = 1.44269502162933349609375f;          /* 0x3fb8aa3b */
+  const float ln2_hi = 0.693145751953125f;                 /* 0x3f317200 */
+  const float ln2_lo = 1.428606765330187045037746429443359375e-6f; /* 0x35bfbe8e */
+  const float c7 = 1.98412701138295233249664306640625e-4f; /* 0x39500d01 = 1/5040 */
+  const float c6 = 1.38888892251998186111450195312500e-3f; /* 0x3ab60b61 = 1/720  */
+  const float c5 = 8.33333376795053482055664062500000e-3f; /* 0x3c088889 = 1/120  */
+  const float c4 = 4.16666679084300994873046875000000e-2f; /* 0x3d2aaaab = 1/24   */
+  const float c3 = 1.66666671633720397949218750000000e-1f; /* 0x3e2aaaab = 1/6    */
+  const float c2 = 0.5f;
+  const float c1 = 1.0f;
+  const float c0 = 1.0f;
+  float t = x * log2e;
+  float n = rintf(t);
+  float r = fmaf(-n, ln2_hi, x);
+  r = fmaf(-n, ln2_lo, r);
+  float p = c7;
+  p = fmaf(p, r, c6);
+  p = fmaf(p, r, c5);
+  p = fmaf(p, r, c4);
+  p = fmaf(p, r, c3);
+  p = fmaf(p, r, c2);
+  p = fmaf(p, r, c1);
+  p = fmaf(p, r, c0);
+  int ni = (int)n;
+  int n1 = ni / 2; /* C division truncates toward zero */
+  int n2 = ni - n1;
+  return (p * pow2_normal(n1)) * pow2_normal(n2);
+}
+
+/* ------------------------------------------------ dynamic per-token quant -- */
+
+/* [P1] §二 npu_dynamic_quant: BF16 x [M,K] -> INT8 q [M,K] + fp32 scale [M]. */
+int oracle_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale) {
+  if (M < 0 || K <= 0) return ORC_ERR_SHAPE;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m) {
+    const uint16_t* xr = x + m * K;
+    int8_t* qr = q + m * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      float a = fabsf(oracle_bf16_to_f32(xr[k]));
+      if (a > amax) amax = a;
+    }
+    float s = amax / 127.0f;
+    scale[m] = s;
+    for (int64_t k = 0; k < K; ++k) {
+      int8_t v = 0;
+      if (s > 0.0f) {
+        float t = oracle_bf16_to_f32(xr[k]) / s;
+        float r = rintf(t);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        v = (int8_t)r;
+      }
+      qr[k] = v;
+    }
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------- INT8 GEMM, int32 -- */
+
+/* acc[m,n] = sum_k q[m,k] * W[n,k]; W is [N,K] row-major (the checkpoint
+ * layout of [P1] §二, output channel major). */
+int oracle_int8_gemm_acc(const int8_t* q, int64_t M, int64_t K, const int8_t* w, int64_t N,
+                         int32_t* acc) {
+  if (M < 0 || N <= 0 || K <= 0 || K > ORC_MAX_K) return ORC_ERR_SHAPE;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m) {
+    const int8_t* qr = q + m * K;
+    for (int64_t n = 0; n < N; ++n) {
+      const int8_t* wr = w + n * K;
+      int32_t a = 0;
+      for (int64_t k = 0; k < K; ++k) a += (int32_t)qr[k] * (int32_t)wr[k];
+      acc[m * N + n] = a;
+    }
+  }
+  return ORC_OK;
+}
+
+/* One output element of the fused dequant epilogue ([P1] §二, §四). */
+static uint16_t epilogue_one(int32_t acc, float sx, float sw, const uint16_t* bias, int64_t n) {
+  float t = (float)acc;
+  t = t * sx;
+  t = t * sw;
+  if (bias) t = t + oracle_bf16_to_f32(bias[n]);
+  return oracle_f32_to_bf16(t);
+}
+
+int oracle_epilogue(const int32_t* acc, int64_t M, int64_t N, const float* x_scale,
+                    const float* w_scale, const uint16_t* bias, uint16_t* y) {
+  if (M < 0 || N <= 0) return ORC_ERR_SHAPE;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n)
+      y[m * N + n] = epilogue_one(acc[m * N + n], x_scale[m], w_scale[n], bias, n);
+  return ORC_OK;
+}
+
+/* [P1] §二 npu_quant_matmul: INT8 x INT8 -> INT32 -> * x_scale * w_scale (+bias) -> BF16. */
+int oracle_quant_matmul(const int8_t* q, const float* x_scale, int64_t M, int64_t K,
+                        const int8_t* w, const float* w_scale, int64_t N, const uint16_t* bias,
+                        uint16_t* y) {
+  if (M < 0 || N <= 0 || K <= 0 || K > ORC_MAX_K) return ORC_ERR_SHAPE;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m) {
+    const int8_t* qr = q + m * K;
+    for (int64_t n = 0; n < N; ++n) {
+      const int8_t* wr = w + n * K;
+      int32_t a = 0;
+      for (int64_t k = 0; k < K; ++k) a += (int32_t)qr[k] * (int32_t)wr[k];
+      y[m * N + n] = epilogue_one(a, x_scale[m], w_scale[n], bias, n);
+    }
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------- grouped GEMM -- */
+
+int oracle_check_group_list(const int64_t* group_list, int64_t E, int64_t R) {
+  int64_t total = 0;
+  for (int64_t e = 0; e < E; ++e) {
+    if (group_list[e] < 0) return ORC_ERR_GROUP_LIST;
+    total += group_list[e];
+  }
+  return total == R ? ORC_OK : ORC_ERR_GROUP_LIST;
+}
+
+/* [P1] §三 npu_grouped_matmul(x, weight, scale, per_token_scale, group_list):
+ * rows of expert e use W[e] ([E,N,K]) and w_scale[e] ([E,N]).  acc (optional,
+ * [R,N] int32) receives the exact accumulators. */
+int oracle_grouped_matmul(const int8_t* q, const float* x_scale, const int64_t* group_list,
+                          int64_t E, int64_t R, int64_t K, const int8_t* w,
+                          const float* w_scale, int64_t N, uint16_t* y, int32_t* acc) {
+  if (E <= 0 || R < 0 || N <= 0 || K <= 0 || K > ORC_MAX_K) return ORC_ERR_SHAPE;
+  if (oracle_check_group_list(group_list, E, R) != ORC_OK) return ORC_ERR_GROUP_LIST;
+  int64_t off = 0;
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t rows = group_list[e];
+    const int8_t* we = w + e * N * K;
+    const float* se = w_scale + e * N;
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = off; r < off + rows; ++r) {
+      const int8_t* qr = q + r * K;
+      for (int64_t n = 0; n < N; ++n) {
+        const int8_t* wr = we + n * K;
+        int32_t a = 0;
+        for (int64_t k = 0; k < K; ++k) a += (int32_t)qr[k] * (int32_t)wr[k];
+        if (acc) acc[r * N + n] = a;
+        y[r * N + n] = epilogue_one(a, x_scale[r], se[n], NULL, n);
+      }
+    }
+    off += rows;
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------- SwiGLU -- */
+
+/* [P1] §三 runner chain "W13 Grouped MatMul -> SwiGLU": y13 [R, 2I] bf16 ->
+ * h [R, I] bf16. */
+int oracle_swiglu(const uint16_t* y13, int64_t R, int64_t I, uint16_t* h) {
+  if (R < 0 || I <= 0) return ORC_ERR_SHAPE;
+  int64_t r;
+#pragma omp parallel for schedule(static)
+  for (r = 0; r < R; ++r) {
+    for (int64_t j = 0; j < I; ++j) {
+      float g = oracle_bf16_to_f32(y13[r * 2 * I + j]);
+      float u = oracle_bf16_to_f32(y13[r * 2 * I + I + j]);
+      float e = oracle_exp_f32(-g);
+      float sig = 1.0f / (1.0f + e);
+      float v = (g * sig) * u;
+      h[r * I + j] = oracle_f32_to_bf16(v);
+    }
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------- MoE expert FFN chain -- */
+/*
+ * [P1] §三: Routed Hidden -> (quant if no per-token scale) -> W13 GMM ->
+ * SwiGLU -> Requant -> W2 GMM -> BF16.
+ *   x        bf16 [R,H] when x_scale == NULL, else int8 [R,H]
+ *   x_scale  fp32 [R] or NULL
+ *   w13      int8 [E,2I,H], s13 fp32 [E,2I];  w2 int8 [E,H,I], s2 fp32 [E,H]
+ *   y        bf16 [R,H]
+ * Optional intermediates (NULL to skip): xq [R,H] int8, xs [R], y13 [R,2I]
+ * bf16, h [R,I] bf16, hq [R,I] int8, hs [R].
+ */
+int oracle_moe_w13_swiglu_requant_w2(const void* x, const float* x_scale,
+                                     const int64_t* group_list, int64_t E, int64_t R,
+                                     int64_t H, int64_t I, const int8_t* w13, const float* s13,
+                                     const int8_t* w2, const float* s2, uint16_t* y,
+                                     int8_t* xq_out, float* xs_out, uint16_t* y13_out,
+                                     uint16_t* h_out, int8_t* hq_out, float* hs_out) {
+  if (E <= 0 || R < 0 || H <= 0 || I <= 0) return ORC_ERR_SHAPE;
+  if (oracle_check_group_list(group_list, E, R) != ORC_OK) return ORC_ERR_GROUP_LIST;
+  const size_t r = (size_t)R;
+  int8_t* xq = malloc(r * (size_t)H + 1);
+  float* xs = malloc(r * sizeof(float) + 4);
+  uint16_t* y13 = malloc(r * 2 * (size_t)I * sizeof(uint16_t) + 2);
+  uint16_t* h = malloc(r * (size_t)I * sizeof(uint16_t) + 2);
+  int8_t* hq = malloc(r * (size_t)I + 1);
+  float* hs = malloc(r * sizeof(float) + 4);
+  int rc = ORC_ERR_ALLOC;
+  if (!xq || !xs || !y13 || !h || !hq || !hs) goto done;
+
+  if (x_scale == NULL) {
+    rc = oracle_dynamic_quant((const uint16_t*)x, R, H, xq, xs);
+    if (rc) goto done;
+  } else {
+    memcpy(xq, x, r * (size_t)H);
+    memcpy(xs, x_scale, r * sizeof(float));
+  }
+  rc = oracle_grouped_matmul(xq, xs, group_list, E, R, H, w13, s13, 2 * I, y13, NULL);
+  if (rc) goto done;
+  rc = oracle_swiglu(y13, R, I, h);
+  if (rc) goto done;
+  rc = oracle_dynamic_quant(h, R, I, hq, hs);
+  if (rc) goto done;
+  rc = oracle_grouped_matmul(hq, hs, group_list, E, R, I, w2, s2, H, y, NULL);
+  if (rc) goto done;
+
+  if (xq_out) memcpy(xq_out, xq, r * (size_t)H);
+  if (xs_out) memcpy(xs_out, xs, r * sizeof(float));
+  if (y13_out) memcpy(y13_out, y13, r * 2 * (size_t)I * sizeof(uint16_t));
+  if (h_out) memcpy(h_out, h, r * (size_t)I * sizeof(uint16_t));
+  if (hq_out) memcpy(hq_out, hq, r * (size_t)I);
+  if (hs_out) memcpy(hs_out, hs, r * sizeof(float));
+done:
+  free(xq);
+  free(xs);
+  free(y13);
+  free(h);
+  free(hq);
+  free(hs);
+  return rc;
+}

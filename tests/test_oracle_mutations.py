@@ -1,0 +1,57 @@
+"""The oracle's pins bite: plant one plausible slip at a time in a temporary
+copy of the oracle's C source (CPU only), rebuild it, and check that a pin in
+test_oracle_pins fails against that build."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+
+import test_oracle_pins as pins
+
+MUTATIONS = [
+    ("scale divides by 128", "float s = amax / 127.0f;", "float s = amax / 128.0f;",
+     "test_quant_invariants_and_closed_forms", ()),
+    ("ties away from zero", "float r = rintf(t);", "float r = roundf(t);",
+     "test_quant_matches_torch_round_half_even", ()),
+    ("exp drops the low part of ln 2", "r = fmaf(-n, ln2_lo, r);", "r = r + 0.0f;",
+     "test_exp_spec_accuracy_and_special_values", ()),
+    ("exp cubic coefficient off", "const float c3 = 1.66666671633720397949218750000000e-1f;",
+     "const float c3 = 1.6660e-1f;", "test_exp_spec_accuracy_and_special_values", ()),
+    ("sigmoid sign", "float e = oracle_exp_f32(-g);", "float e = oracle_exp_f32(g);",
+     "test_swiglu_against_float64_and_closed_forms", ()),
+    ("gate and up swapped", "float g = oracle_bf16_to_f32(y13[r * 2 * I + j]);",
+     "float g = oracle_bf16_to_f32(y13[r * 2 * I + I + j]);", "test_swiglu_gate_is_first_half", ()),
+    ("bias from the wrong column", "t = t + oracle_bf16_to_f32(bias[n]);",
+     "t = t + oracle_bf16_to_f32(bias[0]);", "test_epilogue_against_float64", ()),
+    ("weight read transposed", "for (int64_t k = 0; k < K; ++k) a += (int32_t)qr[k] * (int32_t)wr[k];\n      acc[m * N + n] = a;",
+     "for (int64_t k = 0; k < K; ++k) a += (int32_t)qr[k] * (int32_t)w[k * N + n];\n      acc[m * N + n] = a;",
+     "test_gemm_acc_matches_int64_matmul", (7, 96, 13)),
+    ("grouped row scale indexed inside the group", "y[r * N + n] = epilogue_one(a, x_scale[r], se[n], NULL, n);",
+     "y[r * N + n] = epilogue_one(a, x_scale[r - off], se[n], NULL, n);",
+     "test_grouped_golden_example_against_numpy", ()),
+    ("group-list sum not checked", "return total == R ? ORC_OK : ORC_ERR_GROUP_LIST;", "return ORC_OK;",
+     "test_grouped_rejects_bad_group_lists", ()),
+    ("pre-quantised input quantised again", "if (x_scale == NULL) {", "if (1) {",
+     "test_moe_chain_composition_and_no_double_quant", ()),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pin,args", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_slip_is_caught(tmp_path, name, old, new, pin, args):
+    src = open(obuild.SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mutated = src.replace(old, new, 1)
+    c_path = tmp_path / "mutant.c"
+    c_path.write_text(mutated)
+    so_path = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", *obuild.CFLAGS, str(c_path), "-o", so_path, "-lm"], check=True,
+                   capture_output=True)
+    prev = oracle.use_library(so_path)
+    try:
+        with pytest.raises((AssertionError, oracle.OracleError)):
+            getattr(pins, pin)(*args)
+    finally:
+        oracle.restore_library(prev)
