@@ -1,0 +1,204 @@
+/*
+ * w8a8.h -- C ABI of the GB300 (sm_103a) W8A8_DYNAMIC linear-layer and
+ * MoE-expert library (libw8a8.so).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "DeepSeek-V4 W8A8 执行链从量化权重到 Ascend INT8 算子"
+ *        §一 quantisation recipe (activations per-token symmetric INT8,
+ *            weights per-channel symmetric INT8; W13 = gate_proj + up_proj,
+ *            W2 = down_proj);
+ *        §二 Dense path: load-time transpose + format cast of the INT8
+ *            weight, npu_dynamic_quant, npu_quant_matmul, output dtype BF16;
+ *        §三 MoE path: npu_grouped_matmul over group_list (rows per expert),
+ *            W13 GMM -> SwiGLU -> Requant -> W2 GMM, and the rule that an
+ *            input that already carries a per-token scale is not quantised
+ *            again;
+ *        §四 operator contract: INT8 x1, INT8 x2, FLOAT32 per-token scale,
+ *            BF16 output.
+ *   [P2] "Qwen3.8-FP8 on Ascend 950: Why Weights Become MXFP8 at Load Time",
+ *        Deep Dive 4 (load-time repack into persistent buffers whose addresses
+ *        stay fixed for graph replay) and 6 (MoE weights prepared one expert
+ *        at a time); "Where It Breaks or Falls Back" (error conventions).
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *     contiguous.  BF16 tensors are passed as uint16_t bit patterns.
+ *   - Work is enqueued on `stream` and returns without synchronising; the
+ *     library allocates nothing and never synchronises in these calls.  The
+ *     caller keeps every buffer alive until the stream work completes.
+ *   - Argument errors are detected on the host and returned synchronously;
+ *     nothing is launched then.  Errors that depend on device data (a bad
+ *     group_list, a packed weight that does not match the call, an exhausted
+ *     wait) are written to the status word at the start of the caller's
+ *     workspace; read them with w8a8_read_device_status().
+ *   - Workspaces must be zero-filled once before their first use; every call
+ *     leaves its workspace zeroed again (except for the status word after an
+ *     error, which w8a8_read_device_status() clears).
+ *   - K (the reduction depth) must be a multiple of 16 and at most
+ *     W8A8_MAX_K; M, N and group sizes are arbitrary (>= 0 / >= 1).
+ *   - Integer results (INT8 payloads, INT32 accumulators) and FP32 scales are
+ *     exact; BF16 outputs are the binary32 epilogue rounded to nearest-even.
+ */
+#ifndef W8A8_H
+#define W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W8A8_API __attribute__((visibility("default")))
+#else
+#define W8A8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t), passed through untouched; NULL = legacy default stream. */
+typedef struct CUstream_st* w8a8_stream_t;
+
+typedef enum {
+  W8A8_OK = 0,
+  W8A8_ERR_NULL = 1,           /* a required pointer is NULL */
+  W8A8_ERR_SHAPE = 2,          /* a size is negative, zero where it must not be, or too large */
+  W8A8_ERR_ALIGN = 3,          /* K % 16 != 0, or a pointer is not 16-byte aligned */
+  W8A8_ERR_WORKSPACE = 4,      /* workspace NULL or smaller than the matching *_workspace_bytes() */
+  W8A8_ERR_GROUP_LIST = 5,     /* device: a count < 0 or the counts do not sum to R */
+  W8A8_ERR_DEVICE_TIMEOUT = 6, /* device: a bounded wait gave up */
+  W8A8_ERR_CUDA = 7,           /* a CUDA runtime call failed (launch error etc.) */
+  W8A8_ERR_UNSUPPORTED = 8,    /* the device is not sm_103 / a mode is not built */
+  W8A8_ERR_PACKED = 9          /* device: packed weight header does not match the call */
+} w8a8_status;
+
+#define W8A8_MAX_K 65536
+
+/* Human-readable name of a status code (static string). */
+W8A8_API const char* w8a8_status_string(int status);
+
+/* Library version (major*10000 + minor*100 + patch). */
+W8A8_API int w8a8_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Weight prepack -- [P1] §二 (INT8 weight [N,K] transposed and cast to the  */
+/* kernel's layout once at load time, reused by every forward) and [P2] Deep */
+/* Dive 4 and 6 (persistent repacked buffers; MoE experts one at a time).    */
+/* ------------------------------------------------------------------------ */
+
+/* Pack flags. */
+#define W8A8_PACK_GATE_UP 1u /* W13 [E,2I,K]: interleave gate rows [0,I) and up rows [I,2I)
+                                in blocks of 64 so one tile holds matching gate/up channels;
+                                requires N even and (N/2) % 64 == 0 */
+#define W8A8_PACK_F16 2u     /* also store an integer-valued FP16 copy of the weights
+                                (operand of the tensor-core engine used for large M) */
+
+/* Bytes of the packed buffer for E experts of [N,K] INT8 weights (E = 1 for a dense layer). */
+W8A8_API size_t w8a8_prepacked_bytes(int64_t E, int64_t N, int64_t K, uint32_t flags);
+
+/* w [E,N,K] int8 row-major (the checkpoint layout: output channel major, K
+ * contiguous) -> packed (device buffer of w8a8_prepacked_bytes() bytes,
+ * 256-byte aligned).  The packed buffer starts with a header recording
+ * E, N, K and flags; later calls check it on the device.  Runs once per weight
+ * at load time; the source may be freed after the stream work completes. */
+W8A8_API w8a8_status w8a8_prepack_weight(const int8_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags,
+                                void* packed, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dynamic per-token quantisation -- [P1] §二 npu_dynamic_quant and §三      */
+/* HiddenStatesDynamicQuant: amax = max_k |x[m,k]|, scale[m] = amax / 127    */
+/* (binary32 divide), q = clamp(rint(x / scale), -127, 127), rint = ties to  */
+/* even; a row of zeros gets scale 0 and q = 0.                              */
+/* ------------------------------------------------------------------------ */
+
+/* x [M,K] bf16 -> q [M,K] int8, scale [M] fp32.  M >= 0, K % 16 == 0, x and q 16-byte aligned. */
+W8A8_API w8a8_status w8a8_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
+                               w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dense quantised matmul -- [P1] §二 npu_quant_matmul and §四:              */
+/* acc[m,n] = sum_k q[m,k] * W[n,k] (exact INT32);                          */
+/* y[m,n] = bf16_rne(((float)acc * x_scale[m]) * w_scale[n] + bias[n]).      */
+/* ------------------------------------------------------------------------ */
+
+W8A8_API size_t w8a8_quant_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* q [M,K] int8, x_scale [M] fp32, w_packed (from w8a8_prepack_weight with E = 1,
+ * flags 0 or W8A8_PACK_F16), w_scale [N] fp32, bias [N] bf16 or NULL -> y [M,N] bf16.
+ * ws: zero-filled device workspace of at least w8a8_quant_matmul_workspace_bytes(). */
+W8A8_API w8a8_status w8a8_quant_matmul(const int8_t* q, const float* x_scale, int64_t M, int64_t K,
+                              const void* w_packed, const float* w_scale, int64_t N,
+                              const uint16_t* bias, uint16_t* y, void* ws, size_t ws_bytes,
+                              w8a8_stream_t stream);
+
+/* Same contraction, writing the exact INT32 accumulators acc [M,N] instead of
+ * the dequantised output (validation entry point for bit-exact checks). */
+W8A8_API w8a8_status w8a8_int8_matmul_acc(const int8_t* q, int64_t M, int64_t K, const void* w_packed,
+                                 int64_t N, int32_t* acc, void* ws, size_t ws_bytes,
+                                 w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped matmul -- [P1] §三 npu_grouped_matmul(x, weight, scale,           */
+/* per_token_scale, group_list): group_list[e] = number of rows of expert e; */
+/* rows are contiguous per expert in expert order; rows of expert e use      */
+/* W[e] and w_scale[e,:]; experts with 0 rows are skipped.                   */
+/* ------------------------------------------------------------------------ */
+
+W8A8_API size_t w8a8_grouped_matmul_workspace_bytes(int64_t E, int64_t R, int64_t N, int64_t K);
+
+/* q [R,K] int8, x_scale [R] fp32, group_list [E] int64 (device) counts,
+ * w_packed (E experts, flags 0 or W8A8_PACK_F16), w_scale [E,N] fp32 -> y [R,N] bf16.
+ * Counts < 0 or a sum != R set W8A8_ERR_GROUP_LIST on the device and write nothing. */
+W8A8_API w8a8_status w8a8_grouped_matmul(const int8_t* q, const float* x_scale, const int64_t* group_list,
+                                int64_t E, int64_t R, int64_t K, const void* w_packed,
+                                const float* w_scale, int64_t N, uint16_t* y, void* ws,
+                                size_t ws_bytes, w8a8_stream_t stream);
+
+/* Grouped contraction writing the exact INT32 accumulators acc [R,N] (validation). */
+W8A8_API w8a8_status w8a8_grouped_matmul_acc(const int8_t* q, const int64_t* group_list, int64_t E,
+                                    int64_t R, int64_t K, const void* w_packed, int64_t N,
+                                    int32_t* acc, void* ws, size_t ws_bytes, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* MoE expert FFN -- [P1] §三 runner chain: (quantise only if no per-token   */
+/* scale was supplied) -> W13 grouped matmul -> SwiGLU -> per-token INT8     */
+/* requant -> W2 grouped matmul -> BF16.                                     */
+/*   y13 = grouped(x, W13) rounded to bf16, gate = channels [0,I), up = [I,2I) */
+/*   h   = bf16_rne((g * sigmoid(g)) * u), sigmoid(g) = 1 / (1 + exp(-g)) in  */
+/*         binary32, exp by Cody-Waite reduction + degree-7 Taylor polynomial */
+/*         evaluated with fused multiply-adds (Cody & Waite, 1980)            */
+/*   (hq, hs) = dynamic quant of h over I;  y = grouped(hq, W2) -> bf16        */
+/* ------------------------------------------------------------------------ */
+
+W8A8_API size_t moe_workspace_bytes(int64_t R, int64_t H, int64_t I, int64_t E);
+
+/* x: bf16 [R,H] when x_scale == NULL (quantised here), else int8 [R,H] already
+ * quantised with per-token scales x_scale [R] (used as is, not quantised again).
+ * group_list [E] int64 device counts; w13_packed from W8A8_PACK_GATE_UP
+ * (+ optional W8A8_PACK_F16) of W13 [E,2I,H]; w13_scale [E,2I] in the ORIGINAL
+ * channel order; w2_packed of W2 [E,H,I]; w2_scale [E,H]; y [R,H] bf16.
+ * I % 64 == 0, H % 16 == 0. */
+W8A8_API w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale,
+                                      const int64_t* group_list, int64_t E, int64_t R, int64_t H,
+                                      int64_t I, const void* w13_packed, const float* w13_scale,
+                                      const void* w2_packed, const float* w2_scale, void* ws,
+                                      size_t ws_bytes, uint16_t* y, w8a8_stream_t stream);
+
+/* Offsets (bytes from ws) of the MoE intermediates kept in the workspace after
+ * a call: 0 xq int8 [R,H], 1 xs fp32 [R], 2 h bf16 [R,I], 3 hq int8 [R,I],
+ * 4 hs fp32 [R].  Returns -1 for an unknown index.  (Validation aid.) */
+W8A8_API int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int which);
+
+/* ------------------------------------------------------------------------ */
+/* Device status                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, returns the status word that kernels wrote into the
+ * workspace `ws` (W8A8_OK if none) and clears it.  `ws` is any workspace
+ * passed to the calls above. */
+W8A8_API w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_H */

@@ -1,0 +1,216 @@
+"""GB300 (sm_103a) W8A8_DYNAMIC linear layer and MoE-expert path.
+
+A thin torch binding over the C ABI of libw8a8.so (include/w8a8.h): every
+function below only checks tensor shapes/dtypes/devices, takes data pointers
+and the current CUDA stream, and calls the library.  All arithmetic runs in
+the library's CUDA kernels; nothing here computes, and there is no fallback.
+
+BF16 tensors are torch.bfloat16; INT8 tensors torch.int8; scales float32;
+group lists int64 (on the device).  Workspaces are zero-filled uint8 device
+tensors that can be reused across calls on one stream.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _capi
+from ._capi import PACK_F16, PACK_GATE_UP, W8A8Error
+
+__all__ = [
+    "PACK_F16", "PACK_GATE_UP", "W8A8Error", "prepacked_bytes", "w8a8_prepack_weight",
+    "w8a8_dynamic_quant", "quant_matmul_workspace_bytes", "w8a8_quant_matmul",
+    "w8a8_int8_matmul_acc", "grouped_matmul_workspace_bytes", "w8a8_grouped_matmul",
+    "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
+    "moe_w13_swiglu_requant_w2", "read_device_status", "workspace",
+]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-filled device workspace of `nbytes` bytes (256-byte aligned by the caching allocator)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def prepacked_bytes(E: int, N: int, K: int, flags: int = 0) -> int:
+    return int(_capi.lib().w8a8_prepacked_bytes(E, N, K, flags))
+
+
+def w8a8_prepack_weight(w: torch.Tensor, flags: int = 0) -> torch.Tensor:
+    """INT8 weight [N,K] or expert stack [E,N,K] -> packed device buffer (uint8)."""
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    if w3.dim() != 3:
+        raise ValueError("w must be [N,K] or [E,N,K]")
+    _need(w3, "w", torch.int8)
+    E, N, K = w3.shape
+    nbytes = prepacked_bytes(E, N, K, flags)
+    if nbytes == 0:
+        raise ValueError("bad weight shape")
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    with torch.cuda.device(w.device):
+        _capi.check("w8a8_prepack_weight", _capi.lib().w8a8_prepack_weight(
+            w3.data_ptr(), E, N, K, flags, packed.data_ptr(), _stream(w.device)))
+    return packed
+
+
+def w8a8_dynamic_quant(x: torch.Tensor, q: Optional[torch.Tensor] = None,
+                       scale: Optional[torch.Tensor] = None):
+    """BF16 x [M,K] -> (int8 q [M,K], float32 scale [M])."""
+    _need(x, "x", torch.bfloat16)
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device) if q is None else q
+    scale = torch.empty((M,), dtype=torch.float32, device=x.device) if scale is None else scale
+    _need(q, "q", torch.int8, (M, K), x.device)
+    _need(scale, "scale", torch.float32, (M,), x.device)
+    with torch.cuda.device(x.device):
+        _capi.check("w8a8_dynamic_quant", _capi.lib().w8a8_dynamic_quant(
+            x.data_ptr(), M, K, q.data_ptr(), scale.data_ptr(), _stream(x.device)))
+    return q, scale
+
+
+def quant_matmul_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_capi.lib().w8a8_quant_matmul_workspace_bytes(M, N, K))
+
+
+def w8a8_quant_matmul(q: torch.Tensor, x_scale: torch.Tensor, w_packed: torch.Tensor,
+                      w_scale: torch.Tensor, N: int, bias: Optional[torch.Tensor] = None,
+                      ws: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None):
+    """int8 q [M,K] x packed W [N,K] -> bf16 y [M,N] = ((acc * x_scale) * w_scale) + bias."""
+    _need(q, "q", torch.int8)
+    M, K = q.shape
+    dev = q.device
+    _need(x_scale, "x_scale", torch.float32, (M,), dev)
+    _need(w_packed, "w_packed", torch.uint8, None, dev)
+    _need(w_scale, "w_scale", torch.float32, (N,), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, (N,), dev)
+    ws = workspace(quant_matmul_workspace_bytes(M, N, K), dev) if ws is None else ws
+    _need(ws, "ws", torch.uint8, None, dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if y is None else y
+    _need(y, "y", torch.bfloat16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_quant_matmul", _capi.lib().w8a8_quant_matmul(
+            q.data_ptr(), x_scale.data_ptr(), M, K, w_packed.data_ptr(), w_scale.data_ptr(), N,
+            _ptr(bias), y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)))
+    return y
+
+
+def w8a8_int8_matmul_acc(q: torch.Tensor, w_packed: torch.Tensor, N: int,
+                         ws: Optional[torch.Tensor] = None):
+    """Exact INT32 accumulators acc [M,N] = q [M,K] x W[N,K]^T (validation entry)."""
+    _need(q, "q", torch.int8)
+    M, K = q.shape
+    dev = q.device
+    ws = workspace(quant_matmul_workspace_bytes(M, N, K), dev) if ws is None else ws
+    acc = torch.empty((M, N), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_int8_matmul_acc", _capi.lib().w8a8_int8_matmul_acc(
+            q.data_ptr(), M, K, w_packed.data_ptr(), N, acc.data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(dev)))
+    return acc
+
+
+def grouped_matmul_workspace_bytes(E: int, R: int, N: int, K: int) -> int:
+    return int(_capi.lib().w8a8_grouped_matmul_workspace_bytes(E, R, N, K))
+
+
+def w8a8_grouped_matmul(q: torch.Tensor, x_scale: torch.Tensor, group_list: torch.Tensor,
+                        w_packed: torch.Tensor, w_scale: torch.Tensor,
+                        ws: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None):
+    """int8 q [R,K] (rows grouped by expert) x packed W [E,N,K] -> bf16 [R,N]."""
+    _need(q, "q", torch.int8)
+    R, K = q.shape
+    dev = q.device
+    _need(group_list, "group_list", torch.int64, None, dev)
+    E = group_list.numel()
+    _need(w_scale, "w_scale", torch.float32, None, dev)
+    N = w_scale.shape[-1]
+    _need(x_scale, "x_scale", torch.float32, (R,), dev)
+    ws = workspace(grouped_matmul_workspace_bytes(E, R, N, K), dev) if ws is None else ws
+    y = torch.empty((R, N), dtype=torch.bfloat16, device=dev) if y is None else y
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_grouped_matmul", _capi.lib().w8a8_grouped_matmul(
+            q.data_ptr(), x_scale.data_ptr(), group_list.data_ptr(), E, R, K, w_packed.data_ptr(),
+            w_scale.data_ptr(), N, y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)))
+    return y
+
+
+def w8a8_grouped_matmul_acc(q: torch.Tensor, group_list: torch.Tensor, w_packed: torch.Tensor,
+                            N: int, ws: Optional[torch.Tensor] = None):
+    _need(q, "q", torch.int8)
+    R, K = q.shape
+    dev = q.device
+    _need(group_list, "group_list", torch.int64, None, dev)
+    E = group_list.numel()
+    ws = workspace(grouped_matmul_workspace_bytes(E, R, N, K), dev) if ws is None else ws
+    acc = torch.empty((R, N), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_grouped_matmul_acc", _capi.lib().w8a8_grouped_matmul_acc(
+            q.data_ptr(), group_list.data_ptr(), E, R, K, w_packed.data_ptr(), N, acc.data_ptr(),
+            ws.data_ptr(), ws.numel(), _stream(dev)))
+    return acc
+
+
+def moe_workspace_bytes(R: int, H: int, I: int, E: int) -> int:
+    return int(_capi.lib().moe_workspace_bytes(R, H, I, E))
+
+
+def moe_workspace_offset(R: int, H: int, I: int, E: int, which: int) -> int:
+    return int(_capi.lib().moe_workspace_offset(R, H, I, E, which))
+
+
+def moe_w13_swiglu_requant_w2(x: torch.Tensor, x_scale: Optional[torch.Tensor],
+                              group_list: torch.Tensor, w13_packed: torch.Tensor,
+                              w13_scale: torch.Tensor, w2_packed: torch.Tensor,
+                              w2_scale: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                              y: Optional[torch.Tensor] = None):
+    """MoE expert FFN: x bf16 [R,H] (x_scale None) or int8 [R,H] with x_scale [R] -> bf16 [R,H]."""
+    R, H = x.shape
+    dev = x.device
+    if x_scale is None:
+        _need(x, "x", torch.bfloat16)
+    else:
+        _need(x, "x", torch.int8)
+        _need(x_scale, "x_scale", torch.float32, (R,), dev)
+    _need(group_list, "group_list", torch.int64, None, dev)
+    E = group_list.numel()
+    _need(w13_scale, "w13_scale", torch.float32, None, dev)
+    I = w13_scale.shape[-1] // 2
+    _need(w2_scale, "w2_scale", torch.float32, (E, H), dev)
+    ws = workspace(moe_workspace_bytes(R, H, I, E), dev) if ws is None else ws
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=dev) if y is None else y
+    with torch.cuda.device(dev):
+        _capi.check("moe_w13_swiglu_requant_w2", _capi.lib().moe_w13_swiglu_requant_w2(
+            x.data_ptr(), _ptr(x_scale), group_list.data_ptr(), E, R, H, I, w13_packed.data_ptr(),
+            w13_scale.data_ptr(), w2_packed.data_ptr(), w2_scale.data_ptr(), ws.data_ptr(),
+            ws.numel(), y.data_ptr(), _stream(dev)))
+    return y
+
+
+def read_device_status(ws: torch.Tensor) -> int:
+    """Synchronise the current stream and return (and clear) the device status word of `ws`."""
+    with torch.cuda.device(ws.device):
+        return int(_capi.lib().w8a8_read_device_status(ws.data_ptr(), _stream(ws.device)))

@@ -1,0 +1,361 @@
+// capi.cu -- the extern "C" boundary of libw8a8.so (declared in include/w8a8.h).
+//
+// Host side only: argument validation (errors returned before any launch, in
+// the spirit of the error table of page "Qwen3.8-FP8 on Ascend 950: Why
+// Weights Become MXFP8 at Load Time", "Where It Breaks or Falls Back", but
+// with no fallback path), workspace layouts, tile-plan choice (decode- vs
+// prefill-sized tiles, as the operator host of page "DeepSeek-V4 W8A8 执行链
+// 从量化权重到 Ascend INT8 算子" §四 picks a tiling per M/N/K) and stream-ordered
+// launches.  Nothing here allocates or synchronises except
+// w8a8_read_device_status().
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+
+using namespace w8a8;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxE = 1024;
+
+struct DevInfo {
+  int sms = 0;
+  int supported = -1;  // -1 unknown, 0 no, 1 yes
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+w8a8_status device_info(int& sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W8A8_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.supported < 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return W8A8_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  if (!d.supported) return W8A8_ERR_UNSUPPORTED;
+  sms = d.sms;
+  return W8A8_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
+inline w8a8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA; }
+
+w8a8_status check_k(int64_t K) {
+  if (K <= 0 || K > W8A8_MAX_K) return W8A8_ERR_SHAPE;
+  if (K % 16 != 0) return W8A8_ERR_ALIGN;
+  return W8A8_OK;
+}
+
+// Workspace of one contraction: status word, then split-K partials + counters.
+struct GemmWs {
+  size_t status = 0, acc = 0, count = 0, total = 0;
+  int64_t count_len = 0;
+};
+GemmWs gemm_ws_layout(int64_t E, int64_t R, int64_t N, int64_t K) {
+  GemmWs L;
+  L.status = 0;
+  L.acc = kStatusBytes;
+  const size_t acc_bytes = align_up(static_cast<uint64_t>(R) * N * 4, 256);
+  L.count = L.acc + acc_bytes;
+  const int64_t nb = (N + 127) / 128;
+  L.count_len = ((R + 7) / 8 + (E > 1 ? E : 0)) * nb;
+  L.total = L.count + align_up(static_cast<uint64_t>(L.count_len) * 4, 256);
+  (void)K;
+  return L;
+}
+
+void bind_ws(GemmArgs& a, void* ws, const GemmWs& L) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  a.status = reinterpret_cast<DeviceStatus*>(b + L.status);
+  a.ws_acc = reinterpret_cast<int32_t*>(b + L.acc);
+  a.ws_count = reinterpret_cast<uint32_t*>(b + L.count);
+  a.ws_count_len = L.count_len;
+}
+
+struct MoeWs {
+  size_t xq, xs, h, hq, hs, gemm, total;
+  GemmWs g;
+};
+MoeWs moe_layout(int64_t R, int64_t H, int64_t I, int64_t E) {
+  MoeWs L;
+  size_t off = kStatusBytes;
+  L.xq = off; off = align_up(off + static_cast<uint64_t>(R) * H, 256);
+  L.xs = off; off = align_up(off + static_cast<uint64_t>(R) * 4, 256);
+  L.h = off;  off = align_up(off + static_cast<uint64_t>(R) * I * 2, 256);
+  L.hq = off; off = align_up(off + static_cast<uint64_t>(R) * I, 256);
+  L.hs = off; off = align_up(off + static_cast<uint64_t>(R) * 4, 256);
+  // one split-K region serves both contractions (they run one after the other)
+  const GemmWs g13 = gemm_ws_layout(E, R, 2 * I, H);
+  const GemmWs g2 = gemm_ws_layout(E, R, H, I);
+  L.g = g13.total >= g2.total ? g13 : g2;
+  L.gemm = off;
+  L.total = off + L.g.total;
+  return L;
+}
+
+w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream, int sms) {
+  bind_ws(a, ws, L);
+  // the status word of a contraction inside a bigger workspace is the
+  // workspace's own first word
+  a.status = static_cast<DeviceStatus*>(ws);
+  const GemmPlan p = plan_reg_gemm(a, sms);
+  return cuda_status(launch_reg_gemm(a, p, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w8a8_status_string(int s) {
+  switch (s) {
+    case W8A8_OK: return "W8A8_OK";
+    case W8A8_ERR_NULL: return "W8A8_ERR_NULL: a required pointer is NULL";
+    case W8A8_ERR_SHAPE: return "W8A8_ERR_SHAPE: a size is out of range";
+    case W8A8_ERR_ALIGN: return "W8A8_ERR_ALIGN: K % 16 != 0 or a pointer is not 16-byte aligned";
+    case W8A8_ERR_WORKSPACE: return "W8A8_ERR_WORKSPACE: workspace missing or too small";
+    case W8A8_ERR_GROUP_LIST: return "W8A8_ERR_GROUP_LIST: group_list has a negative count or does not sum to R";
+    case W8A8_ERR_DEVICE_TIMEOUT: return "W8A8_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    case W8A8_ERR_CUDA: return "W8A8_ERR_CUDA: a CUDA runtime call failed";
+    case W8A8_ERR_UNSUPPORTED: return "W8A8_ERR_UNSUPPORTED: needs a compute capability 10.3 (GB300) device";
+    case W8A8_ERR_PACKED: return "W8A8_ERR_PACKED: packed weight header does not match the call";
+    default: return "W8A8 unknown status";
+  }
+}
+
+int w8a8_version(void) { return 100; }
+
+size_t w8a8_prepacked_bytes(int64_t E, int64_t N, int64_t K, uint32_t flags) {
+  if (E <= 0 || N <= 0 || K <= 0) return 0;
+  return pack_layout(E, N, K, flags).total;
+}
+
+w8a8_status w8a8_prepack_weight(const int8_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags,
+                                void* packed, w8a8_stream_t stream) {
+  if (!w || !packed) return W8A8_ERR_NULL;
+  if (E <= 0 || N <= 0 || E > kMaxE) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (flags & ~(W8A8_PACK_GATE_UP | W8A8_PACK_F16)) return W8A8_ERR_SHAPE;
+  if ((flags & W8A8_PACK_GATE_UP) && (N % 2 != 0 || (N / 2) % kGateUpBlock != 0)) return W8A8_ERR_SHAPE;
+  if (!aligned16(w) || (reinterpret_cast<uintptr_t>(packed) & 255u)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_prepack(w, E, N, K, flags, packed, reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+w8a8_status w8a8_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
+                               w8a8_stream_t stream) {
+  if (M < 0 || M > INT32_MAX) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (M == 0) return W8A8_OK;
+  if (!x || !q || !scale) return W8A8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_dynamic_quant(x, M, K, q, scale, reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+size_t w8a8_quant_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N <= 0 || K <= 0) return 0;
+  return gemm_ws_layout(1, M, N, K).total;
+}
+
+static w8a8_status dense_common(const int8_t* q, const float* x_scale, int64_t M, int64_t K, const void* w_packed,
+                                const float* w_scale, int64_t N, const uint16_t* bias, void* out, int mode,
+                                void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+  if (M < 0 || M > INT32_MAX || N <= 0 || N > INT32_MAX) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (M == 0) return W8A8_OK;
+  if (!q || !w_packed || !out || !ws) return (!ws && q && w_packed && out) ? W8A8_ERR_WORKSPACE : W8A8_ERR_NULL;
+  if (mode == EPI_BF16 && (!x_scale || !w_scale)) return W8A8_ERR_NULL;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(w_packed) & 255u)) return W8A8_ERR_ALIGN;
+  const GemmWs L = gemm_ws_layout(1, M, N, K);
+  if (ws_bytes < L.total || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  GemmArgs a;
+  a.q = q;
+  a.x_scale = x_scale;
+  a.group_list = nullptr;
+  a.E = 1;
+  a.R = M;
+  a.K = K;
+  a.N = N;
+  a.packed = w_packed;
+  a.pack_flags = 0u;
+  a.w_scale = w_scale;
+  a.bias = bias;
+  a.out = out;
+  a.mode = mode;
+  return run_gemm(a, ws, L, reinterpret_cast<cudaStream_t>(stream), sms);
+}
+
+w8a8_status w8a8_quant_matmul(const int8_t* q, const float* x_scale, int64_t M, int64_t K, const void* w_packed,
+                              const float* w_scale, int64_t N, const uint16_t* bias, uint16_t* y, void* ws,
+                              size_t ws_bytes, w8a8_stream_t stream) {
+  return dense_common(q, x_scale, M, K, w_packed, w_scale, N, bias, y, EPI_BF16, ws, ws_bytes, stream);
+}
+
+w8a8_status w8a8_int8_matmul_acc(const int8_t* q, int64_t M, int64_t K, const void* w_packed, int64_t N,
+                                 int32_t* acc, void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+  return dense_common(q, nullptr, M, K, w_packed, nullptr, N, nullptr, acc, EPI_ACC, ws, ws_bytes, stream);
+}
+
+size_t w8a8_grouped_matmul_workspace_bytes(int64_t E, int64_t R, int64_t N, int64_t K) {
+  if (E <= 0 || R < 0 || N <= 0 || K <= 0) return 0;
+  return gemm_ws_layout(E, R, N, K).total;
+}
+
+static w8a8_status grouped_common(const int8_t* q, const float* x_scale, const int64_t* group_list, int64_t E,
+                                  int64_t R, int64_t K, const void* w_packed, const float* w_scale, int64_t N,
+                                  void* out, int mode, void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+  if (E <= 0 || E > kMaxE || R < 0 || R > INT32_MAX || N <= 0 || N > INT32_MAX) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (R == 0) return W8A8_OK;
+  if (!q || !group_list || !w_packed || !out) return W8A8_ERR_NULL;
+  if (mode == EPI_BF16 && (!x_scale || !w_scale)) return W8A8_ERR_NULL;
+  if (!ws) return W8A8_ERR_WORKSPACE;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(w_packed) & 255u)) return W8A8_ERR_ALIGN;
+  const GemmWs L = gemm_ws_layout(E, R, N, K);
+  if (ws_bytes < L.total || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  GemmArgs a;
+  a.q = q;
+  a.x_scale = x_scale;
+  a.group_list = group_list;
+  a.E = E;
+  a.R = R;
+  a.K = K;
+  a.N = N;
+  a.packed = w_packed;
+  a.pack_flags = 0u;
+  a.w_scale = w_scale;
+  a.out = out;
+  a.mode = mode;
+  return run_gemm(a, ws, L, reinterpret_cast<cudaStream_t>(stream), sms);
+}
+
+w8a8_status w8a8_grouped_matmul(const int8_t* q, const float* x_scale, const int64_t* group_list, int64_t E,
+                                int64_t R, int64_t K, const void* w_packed, const float* w_scale, int64_t N,
+                                uint16_t* y, void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+  return grouped_common(q, x_scale, group_list, E, R, K, w_packed, w_scale, N, y, EPI_BF16, ws, ws_bytes, stream);
+}
+
+w8a8_status w8a8_grouped_matmul_acc(const int8_t* q, const int64_t* group_list, int64_t E, int64_t R, int64_t K,
+                                    const void* w_packed, int64_t N, int32_t* acc, void* ws, size_t ws_bytes,
+                                    w8a8_stream_t stream) {
+  return grouped_common(q, nullptr, group_list, E, R, K, w_packed, nullptr, N, acc, EPI_ACC, ws, ws_bytes, stream);
+}
+
+size_t moe_workspace_bytes(int64_t R, int64_t H, int64_t I, int64_t E) {
+  if (R < 0 || H <= 0 || I <= 0 || E <= 0) return 0;
+  return moe_layout(R, H, I, E).total;
+}
+
+int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int which) {
+  if (R < 0 || H <= 0 || I <= 0 || E <= 0) return -1;
+  const MoeWs L = moe_layout(R, H, I, E);
+  switch (which) {
+    case 0: return static_cast<int64_t>(L.xq);
+    case 1: return static_cast<int64_t>(L.xs);
+    case 2: return static_cast<int64_t>(L.h);
+    case 3: return static_cast<int64_t>(L.hq);
+    case 4: return static_cast<int64_t>(L.hs);
+    default: return -1;
+  }
+}
+
+w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const int64_t* group_list, int64_t E,
+                                      int64_t R, int64_t H, int64_t I, const void* w13_packed,
+                                      const float* w13_scale, const void* w2_packed, const float* w2_scale,
+                                      void* ws, size_t ws_bytes, uint16_t* y, w8a8_stream_t stream) {
+  if (E <= 0 || E > kMaxE || R < 0 || R > INT32_MAX || H <= 0 || I <= 0) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(H)) return s;
+  if (w8a8_status s = check_k(I)) return s;
+  if (I % kGateUpBlock != 0) return W8A8_ERR_SHAPE;
+  if (R == 0) return W8A8_OK;
+  if (!x || !group_list || !w13_packed || !w13_scale || !w2_packed || !w2_scale || !y) return W8A8_ERR_NULL;
+  if (!ws) return W8A8_ERR_WORKSPACE;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(w13_packed) & 255u) ||
+      (reinterpret_cast<uintptr_t>(w2_packed) & 255u))
+    return W8A8_ERR_ALIGN;
+  const MoeWs L = moe_layout(R, H, I, E);
+  if (ws_bytes < L.total || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  void* gws = b + L.gemm;
+
+  const int8_t* xq = static_cast<const int8_t*>(x);
+  const float* xs = x_scale;
+  if (x_scale == nullptr) {  // BF16 input: quantise once; an INT8 input with its scale is used as is
+    int8_t* q = reinterpret_cast<int8_t*>(b + L.xq);
+    float* s = reinterpret_cast<float*>(b + L.xs);
+    if (w8a8_status e = cuda_status(launch_dynamic_quant(static_cast<const uint16_t*>(x), R, H, q, s, st, sms)))
+      return e;
+    xq = q;
+    xs = s;
+  }
+  uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
+  int8_t* hq = reinterpret_cast<int8_t*>(b + L.hq);
+  float* hs = reinterpret_cast<float*>(b + L.hs);
+
+  GemmArgs a13;
+  a13.q = xq;
+  a13.x_scale = xs;
+  a13.group_list = group_list;
+  a13.E = E;
+  a13.R = R;
+  a13.K = H;
+  a13.N = 2 * I;
+  a13.packed = w13_packed;
+  a13.pack_flags = W8A8_PACK_GATE_UP;
+  a13.w_scale = w13_scale;
+  a13.out = h;
+  a13.mode = EPI_SWIGLU;
+  bind_ws(a13, gws, L.g);
+  a13.status = static_cast<DeviceStatus*>(ws);
+  if (w8a8_status e = cuda_status(launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st))) return e;
+
+  if (w8a8_status e = cuda_status(launch_dynamic_quant(h, R, I, hq, hs, st, sms))) return e;
+
+  GemmArgs a2;
+  a2.q = hq;
+  a2.x_scale = hs;
+  a2.group_list = group_list;
+  a2.E = E;
+  a2.R = R;
+  a2.K = I;
+  a2.N = H;
+  a2.packed = w2_packed;
+  a2.pack_flags = 0u;
+  a2.w_scale = w2_scale;
+  a2.out = y;
+  a2.mode = EPI_BF16;
+  bind_ws(a2, gws, L.g);
+  a2.status = static_cast<DeviceStatus*>(ws);
+  return cuda_status(launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st));
+}
+
+w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream) {
+  if (!ws) return W8A8_ERR_NULL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return W8A8_ERR_CUDA;
+  DeviceStatus s;
+  if (cudaMemcpy(&s, ws, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess) return W8A8_ERR_CUDA;
+  if (s.code != 0u) {
+    if (cudaMemset(ws, 0, sizeof(s)) != cudaSuccess) return W8A8_ERR_CUDA;
+  }
+  return static_cast<w8a8_status>(s.code);
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// kernels.cuh -- launchers of the kernels in libw8a8.so (internal interface).
+#pragma once
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace w8a8 {
+
+struct PackLayout {
+  uint64_t i8_offset;
+  uint64_t f16_offset;  // 0 when the fp16 copy is absent
+  uint64_t total;
+};
+PackLayout pack_layout(int64_t E, int64_t N, int64_t K, uint32_t flags);
+
+cudaError_t launch_prepack(const int8_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags, void* packed,
+                           cudaStream_t stream, int num_sms);
+
+cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
+                                 cudaStream_t stream, int num_sms);
+cudaError_t launch_dynamic_quant_f16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q_f16, float* scale,
+                                     cudaStream_t stream, int num_sms);
+
+// Epilogue of the contraction.
+enum EpiMode : int {
+  EPI_BF16 = 0,    // y[r,n] = bf16(((float)acc * sx[r]) * sw[e,n] (+ bias[n]))
+  EPI_ACC = 1,     // acc[r,n] = exact int32
+  EPI_SWIGLU = 2,  // W13 with gate/up interleave: h[r,j] = swiglu(bf16 gate, bf16 up)
+};
+
+// One grouped (or dense: group_list == nullptr, one group of R rows) contraction.
+struct GemmArgs {
+  const int8_t* q = nullptr;          // [R,K] int8 activations
+  const float* x_scale = nullptr;     // [R]
+  const int64_t* group_list = nullptr;  // [E] counts, or nullptr for one group of R rows
+  int64_t E = 1, R = 0, K = 0, N = 0; // N = rows per expert of the packed weight
+  const void* packed = nullptr;       // packed weight buffer (header first)
+  uint32_t pack_flags = 0;            // flags the call expects in the header
+  const float* w_scale = nullptr;     // [E,N] in ORIGINAL channel order
+  const uint16_t* bias = nullptr;     // [N] bf16 or nullptr (dense only)
+  void* out = nullptr;                // bf16 [R,N] | int32 [R,N] | bf16 h [R,N/2]
+  int mode = EPI_BF16;
+  DeviceStatus* status = nullptr;
+  int32_t* ws_acc = nullptr;          // split-K partial sums [R,N] (zero on entry and exit)
+  uint32_t* ws_count = nullptr;       // split-K arrival counters (zero on entry and exit)
+  int64_t ws_count_len = 0;
+};
+
+struct GemmPlan {
+  int variant;   // tile shape id
+  int ksplit;
+  int grid;
+  size_t smem;
+};
+
+// Host: choose the tile shape and split for the register-path engine.
+GemmPlan plan_reg_gemm(const GemmArgs& a, int num_sms);
+// Workspace (split-K partials + counters) the plan needs, in bytes.
+size_t reg_gemm_ws_bytes(int64_t E, int64_t R, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_reg_gemm(const GemmArgs& a, const GemmPlan& p, cudaStream_t stream);
+
+}  // namespace w8a8

@@ -1,0 +1,232 @@
+// quant.cu -- K1: dynamic per-token INT8 quantisation of BF16 activations.
+//
+// Page "DeepSeek-V4 W8A8 执行链从量化权重到 Ascend INT8 算子":
+//   §一 recipe: activations per_token, int8, symmetric;
+//   §二 npu_dynamic_quant(x) -> INT8 [M,K] + per-token scale [M];
+//   §三 HiddenStatesDynamicQuant (the same operation on MoE hidden states and
+//       as the Requant after SwiGLU).
+//   amax = max_k |x|, s = amax / 127 (binary32 divide), q = clamp(rint(x/s),
+//   -127, 127) with ties to even; an all-zero row gets s = 0, q = 0.
+//
+// HBM-bound: 2 bytes read + 1 byte written per element (+4 bytes per row).
+// Each row is read once with 16-byte vector loads and held in registers
+// between the absmax pass and the quantise pass; absmax is reduced with warp
+// shuffles (and shared memory across the warps of a CTA).
+#include "kernels.cuh"
+
+namespace w8a8 {
+
+namespace {
+
+__device__ __forceinline__ float absmax8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+    m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+  }
+  return m;
+}
+
+__device__ __forceinline__ int q1(float xf, float s) {
+  // s > 0 here; binary32 divide, round half to even, clamp to +-127
+  int r = __float2int_rn(__fdiv_rn(xf, s));
+  return max(-127, min(127, r));
+}
+
+// 8 bf16 -> 8 int8 packed in a uint2.
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2] = {0u, 0u};
+  if (s > 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int lo = q1(__uint_as_float(w[i] << 16), s);
+      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s);
+      const uint32_t pair = (static_cast<uint32_t>(lo) & 0xffu) | ((static_cast<uint32_t>(hi) & 0xffu) << 8);
+      out[i >> 1] |= pair << ((i & 1) * 16);
+    }
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// 8 bf16 -> 8 integer-valued fp16 (same codes as quant8) packed in a uint4.
+__device__ __forceinline__ uint4 quant8_f16(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[4] = {0u, 0u, 0u, 0u};
+  if (s > 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int lo = q1(__uint_as_float(w[i] << 16), s);
+      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s);
+      out[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
+               (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).
+template <int CH, bool F16OUT>
+__global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
+                                                       int64_t K, void* __restrict__ q,
+                                                       float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nchunk = K / 8;
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; row < M;
+       row += warps_total) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
+    uint4 v[CH];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int64_t idx = lane + 32 * c;
+      if (idx < nchunk) {
+        v[c] = ldg_stream(xr + idx);
+        amax = fmaxf(amax, absmax8(v[c]));
+      }
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) scale[row] = s;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int64_t idx = lane + 32 * c;
+      if (idx < nchunk) {
+        if (F16OUT) {
+          reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + row * K)[idx] = quant8_f16(v[c], s);
+        } else {
+          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v[c], s);
+        }
+      }
+    }
+  }
+}
+
+// One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).
+template <int CH, bool F16OUT>
+__global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
+                                                      int64_t K, void* __restrict__ q,
+                                                      float* __restrict__ scale) {
+  __shared__ float red[8];
+  const int64_t nchunk = K / 8;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
+    uint4 v[CH];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int64_t idx = threadIdx.x + 256 * c;
+      if (idx < nchunk) {
+        v[c] = ldg_stream(xr + idx);
+        amax = fmaxf(amax, absmax8(v[c]));
+      }
+    }
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int64_t idx = threadIdx.x + 256 * c;
+      if (idx < nchunk) {
+        if (F16OUT) {
+          reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + row * K)[idx] = quant8_f16(v[c], s);
+        } else {
+          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v[c], s);
+        }
+      }
+    }
+    __syncthreads();  // red[] is reused by the next row
+  }
+}
+
+// Any K: two passes over the row (the second read mostly hits L2).
+template <bool F16OUT>
+__global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __restrict__ x, int64_t M,
+                                                          int64_t K, void* __restrict__ q,
+                                                          float* __restrict__ scale) {
+  __shared__ float red[8];
+  const int64_t nchunk = K / 8;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
+    float amax = 0.0f;
+    for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) amax = fmaxf(amax, absmax8(xr[idx]));
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+    for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) {
+      if (F16OUT) {
+        reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + row * K)[idx] = quant8_f16(xr[idx], s);
+      } else {
+        reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(xr[idx], s);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <bool F16OUT>
+cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, float* scale,
+                           cudaStream_t stream, int num_sms) {
+  if (M == 0) return cudaSuccess;
+  const int64_t nchunk = K / 8;
+  const int64_t max_grid = static_cast<int64_t>(num_sms) * 64;
+  if (nchunk <= 32 * 8) {
+    // warp per row, 8 rows per CTA
+    const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
+    const int ch = static_cast<int>((nchunk + 31) / 32);
+    dim3 g(static_cast<unsigned>(blocks)), b(256);
+    if (ch <= 1) quant_warp_rows<1, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    else if (ch <= 2) quant_warp_rows<2, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    else if (ch <= 4) quant_warp_rows<4, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    else quant_warp_rows<8, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+  } else {
+    const int64_t blocks = std::min<int64_t>(M, max_grid);
+    const int ch = static_cast<int>((nchunk + 255) / 256);
+    dim3 g(static_cast<unsigned>(blocks)), b(256);
+    if (ch <= 2) quant_cta_rows<2, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    else if (ch <= 4) quant_cta_rows<4, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    else if (ch <= 8) quant_cta_rows<8, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    else quant_cta_rows_any<F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
+                                 cudaStream_t stream, int num_sms) {
+  return launch_quant_t<false>(x, M, K, q, scale, stream, num_sms);
+}
+
+cudaError_t launch_dynamic_quant_f16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q_f16,
+                                     float* scale, cudaStream_t stream, int num_sms) {
+  return launch_quant_t<true>(x, M, K, q_f16, scale, stream, num_sms);
+}
+
+}  // namespace w8a8
