@@ -1,0 +1,595 @@
+#!/usr/bin/env python3
+"""Benchmark of the W8A8_DYNAMIC hot path on GB300 (one JSON line on stdout).
+
+Default workload: the dense decode linear X BF16 [64,7168] x W INT8
+[2048,7168] (per-channel scales, no bias); one step = dynamic per-token quant
++ INT8 GEMM with the fused dequant epilogue.  `--workload N` selects one of
+the five workloads (1 tiny dense, 2 dense decode, 3 dense prefill, 4 MoE
+prefill, 5 MoE decode with pre-quantised input).
+
+Timing: W warm-up steps, then exactly K steps between a barrier +
+synchronize on both sides.  Each kernel type is captured into a CUDA graph
+over rotating input sets whose total size exceeds the 129 MB L2 (or a single
+set when one set already exceeds it), and timed with CUDA events on the
+stream it runs on; the step time is the sum of the per-kernel times.  The
+`e2e` leg runs the same step through the public Python API with the inputs
+copied from pinned host memory and the result copied back every step.
+`cpu_baseline` times the CPU oracle on the host cores on a bounded sample.
+`--impl reference` runs that oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W8A8 GEMM TOPS & % INT8 peak; grouped-MoE layer tokens/s; quant GB/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers --
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        d = dict(FALLBACK_PEAKS)
+        d["source"] = "fallback"
+        return d
+
+
+def weight_read_bound_ms(active_params: float, bytes_per_param: float, n_gpus: int, hbm_bytes_per_s: float):
+    """Decode lower bound: every active weight byte is read once per token, spread over n_gpus."""
+    return active_params * bytes_per_param / (n_gpus * hbm_bytes_per_s) * 1e3
+
+
+# CUDA sources each timed kernel is built from (a recorded ncu figure is valid
+# only while these files are unchanged)
+KERNEL_SOURCES = {
+    "dynamic_quant": ["quant.cu", "common.cuh", "kernels.cuh"],
+    "quant_matmul": ["gemm_reg.cu", "common.cuh", "kernels.cuh"],
+    "moe_layer": ["gemm_reg.cu", "quant.cu", "capi.cu", "common.cuh", "kernels.cuh"],
+}
+
+
+def source_digest(kernel: str) -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w8a8_dynamic_quant_gb300", "csrc")
+    for f in KERNEL_SOURCES.get(kernel, sorted(os.listdir(csrc))):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/ncu_traffic.md), if the
+    kernel sources are unchanged since; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest(kernel)
+    for ln in open(path):
+        parts = [p.strip() for p in ln.strip().strip("|").split("|")]
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[3] == digest:
+            try:
+                return float(parts[2])
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def aggregate(units: float, seconds: float, group=None):
+    """Whole-job figures across ranks: total units and the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if group is None and not (dist.is_available() and dist.is_initialized()):
+        return units, seconds
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend(group) == "nccl" else torch.device("cpu")
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    s = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX, group=group)
+    return float(u.item()), float(s.item())
+
+
+# --------------------------------------------------------------- workloads --
+
+class Dense:
+    """Dense W8A8_DYNAMIC linear: quant + quantised matmul."""
+
+    def __init__(self, cfg_id: int, device):
+        import torch
+        import w8a8_dynamic_quant_gb300 as W
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        self.W, self.torch = W, torch
+        d = S.dense_config(cfg_id)
+        self.d = d
+        self.name = d.name
+        M, N, K = d.M, d.N, d.K
+        self.M, self.N, self.K = M, N, K
+        set_bytes = 2 * M * K + M * K + N * K + 2 * M * N
+        self.n_sets = max(1, -(-int(1.2 * L2_BYTES) // set_bytes))
+        self.n_sets = min(self.n_sets, 16)
+        xd = torch.from_numpy(d.x.view("int16")).to(device).view(torch.bfloat16)
+        wp = W.w8a8_prepack_weight(torch.from_numpy(d.w).to(device))
+        sw = torch.from_numpy(d.w_scale).to(device)
+        bias = None if d.bias is None else torch.from_numpy(d.bias.view("int16")).to(device).view(torch.bfloat16)
+        self.sets = []
+        for i in range(self.n_sets):
+            self.sets.append(dict(
+                x=xd.clone(), wp=wp.clone() if i else wp, sw=sw.clone(), bias=None if bias is None else bias.clone(),
+                q=torch.empty((M, K), dtype=torch.int8, device=device),
+                s=torch.empty((M,), dtype=torch.float32, device=device),
+                y=torch.empty((M, N), dtype=torch.bfloat16, device=device),
+                ws=W.workspace(W.quant_matmul_workspace_bytes(M, N, K), device)))
+        self.units_per_step = 2.0 * M * N * K  # GEMM ops
+        self.unit = "TOPS"
+        self.kernels = ["dynamic_quant", "quant_matmul"]
+        # algorithmic bytes per launch
+        self.alg_bytes = {"dynamic_quant": 2 * M * K + M * K + 4 * M,
+                          "quant_matmul": M * K + N * K + 4 * M + 4 * N + 2 * M * N + (2 * N if bias is not None else 0)}
+        self.alg_flops = {"quant_matmul": 2.0 * M * N * K}
+        self.bound = "hbm" if M <= 256 else "tensor"
+        self.launches_per_step = 2
+        self.input_note = (f"{self.n_sets} rotating input sets of {set_bytes / 1e6:.1f} MB "
+                           f"({self.n_sets * set_bytes / 1e6:.0f} MB > 129 MB L2)" if self.n_sets > 1
+                           else f"one input set of {set_bytes / 1e6:.0f} MB > 129 MB L2")
+
+    def launch(self, kernel: str, i: int):
+        st = self.sets[i]
+        if kernel == "dynamic_quant":
+            self.W.w8a8_dynamic_quant(st["x"], st["q"], st["s"])
+        else:
+            self.W.w8a8_quant_matmul(st["q"], st["s"], st["wp"], st["sw"], self.N, st["bias"], st["ws"], st["y"])
+
+    def config(self):
+        return {"workload": self.name, "M": self.M, "N": self.N, "K": self.K, "bias": self.d.bias is not None,
+                "seed": 0, "inputs": self.input_note}
+
+    def value(self, units, seconds):
+        return units / seconds / 1e12
+
+    # end to end through the public API, host buffers
+    def e2e_setup(self, device):
+        torch = self.torch
+        self.hx = torch.from_numpy(self.d.x.view("int16")).view(torch.bfloat16).pin_memory()
+        self.hy = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.hx.numel() * 2
+        self.d2h = self.hy.numel() * 2
+
+    def e2e_step(self):
+        st = self.sets[0]
+        st["x"].copy_(self.hx, non_blocking=True)
+        q, s = self.W.w8a8_dynamic_quant(st["x"], st["q"], st["s"])
+        y = self.W.w8a8_quant_matmul(q, s, st["wp"], st["sw"], self.N, st["bias"], st["ws"], st["y"])
+        self.hy.copy_(y, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    # CPU oracle on `rows` rows of the same workload
+    def oracle_units(self, rows):
+        return 2.0 * rows * self.N * self.K
+
+    def oracle_step(self, rows):
+        import oracle
+        x = self.d.x[:rows]
+        q, s = oracle.dynamic_quant(x)
+        oracle.quant_matmul(q, s, self.d.w, self.d.w_scale, self.d.bias)
+
+    @property
+    def oracle_full_rows(self):
+        return self.M
+
+
+class MoE:
+    """MoE expert FFN: (quant) -> W13 grouped GEMM + SwiGLU -> requant -> W2 grouped GEMM."""
+
+    def __init__(self, cfg_id: int, device):
+        import numpy as np
+        import torch
+        import w8a8_dynamic_quant_gb300 as W
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        self.W, self.torch, self.np = W, torch, np
+        m = S.moe_config(cfg_id, device=str(device))
+        self.m = m
+        self.name = m.name
+        self.n_sets = 1
+        self.w13p = W.w8a8_prepack_weight(m.w13, W.PACK_GATE_UP)
+        self.w2p = W.w8a8_prepack_weight(m.w2)
+        self.gl = torch.from_numpy(m.group_list).to(device)
+        self.s13 = torch.from_numpy(m.s13).to(device)
+        self.s2 = torch.from_numpy(m.s2).to(device)
+        if m.x_scale is None:
+            self.x = torch.from_numpy(m.x.view("int16")).to(device).view(torch.bfloat16)
+            self.xs = None
+        else:
+            self.x = torch.from_numpy(m.x).to(device)
+            self.xs = torch.from_numpy(m.x_scale).to(device)
+        self.ws = W.workspace(W.moe_workspace_bytes(m.R, m.H, m.I, m.E), device)
+        self.y = torch.empty((m.R, m.H), dtype=torch.bfloat16, device=device)
+        self.units_per_step = float(m.T)  # tokens
+        self.unit = "tokens/s"
+        self.kernels = ["moe_layer"]
+        active = int((m.group_list > 0).sum())
+        R, H, I = m.R, m.H, m.I
+        wbytes = active * (2 * I * H + H * I) + 4 * active * (2 * I + H)
+        xbytes = R * H * (1 if m.x_scale is not None else 2 + 1 + 1)  # x read (+ quant write/read)
+        hbytes = R * I * (2 + 2 + 1 + 1)  # h write+read, hq write+read
+        self.alg_bytes = {"moe_layer": wbytes + xbytes + hbytes + 2 * R * H + 8 * R}
+        self.alg_flops = {"moe_layer": 2.0 * R * (2 * I * H + H * I)}
+        self.bound = "hbm" if m.x_scale is not None else "tensor"
+        self.launches_per_step = 3 if m.x_scale is not None else 4
+        self.input_note = f"weights {wbytes / 1e9:.2f} GB active > 129 MB L2 (single set)"
+
+    def launch(self, kernel: str, i: int):
+        m = self.m
+        self.W.moe_w13_swiglu_requant_w2(self.x, self.xs, self.gl, self.w13p, self.s13, self.w2p, self.s2,
+                                         self.ws, self.y)
+
+    def config(self):
+        m = self.m
+        return {"workload": self.name, "T": m.T, "R": m.R, "H": m.H, "I": m.I, "E": m.E, "topk": m.topk,
+                "active_experts": int((m.group_list > 0).sum()), "prequantised_input": m.x_scale is not None,
+                "seed": 0, "inputs": self.input_note}
+
+    def value(self, units, seconds):
+        return units / seconds
+
+    def e2e_setup(self, device):
+        torch = self.torch
+        m = self.m
+        if m.x_scale is None:
+            self.hx = torch.from_numpy(m.x.view("int16")).view(torch.bfloat16).pin_memory()
+            self.hxs = None
+        else:
+            self.hx = torch.from_numpy(m.x).pin_memory()
+            self.hxs = torch.from_numpy(m.x_scale).pin_memory()
+        self.hgl = torch.from_numpy(m.group_list).pin_memory()
+        self.hy = torch.empty((m.R, m.H), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.hx.numel() * self.hx.element_size() + (0 if self.hxs is None else self.hxs.numel() * 4) + \
+            self.hgl.numel() * 8
+        self.d2h = self.hy.numel() * 2
+
+    def e2e_step(self):
+        self.x.copy_(self.hx, non_blocking=True)
+        if self.hxs is not None:
+            self.xs.copy_(self.hxs, non_blocking=True)
+        self.gl.copy_(self.hgl, non_blocking=True)
+        y = self.W.moe_w13_swiglu_requant_w2(self.x, self.xs, self.gl, self.w13p, self.s13, self.w2p, self.s2,
+                                             self.ws, self.y)
+        self.hy.copy_(y, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    # CPU oracle on a subset of routed rows (tokens = rows / topk)
+    def oracle_units(self, rows):
+        return rows / self.m.topk
+
+    def _subset(self, rows):
+        """Host inputs of the compact problem made of `rows` evenly spaced routed rows."""
+        cache = getattr(self, "_subset_cache", {})
+        self._subset_cache = cache
+        if rows not in cache:
+            np = self.np
+            m = self.m
+            sel = np.unique(np.linspace(0, m.R - 1, rows).astype(np.int64))
+            off = np.concatenate([[0], np.cumsum(m.group_list)])
+            eor = np.searchsorted(off, sel, side="right") - 1
+            experts = np.unique(eor)
+            gl = np.array([int(np.sum(eor == e)) for e in experts], np.int64)
+            idx = self.torch.as_tensor(experts, device=m.w13.device)
+            cache[rows] = (m.x[sel], None if m.x_scale is None else m.x_scale[sel], gl,
+                           m.w13.index_select(0, idx).cpu().numpy(), m.s13[experts],
+                           m.w2.index_select(0, idx).cpu().numpy(), m.s2[experts])
+        return cache[rows]
+
+    def oracle_step(self, rows):
+        import oracle
+        oracle.moe_w13_swiglu_requant_w2(*self._subset(rows))
+
+    @property
+    def oracle_full_rows(self):
+        return self.m.R
+
+
+def make_workload(cfg_id, device):
+    from w8a8_dynamic_quant_gb300 import synthetic as S
+    return Dense(cfg_id, device) if S.CONFIGS[cfg_id]["kind"] == "dense" else MoE(cfg_id, device)
+
+
+# -------------------------------------------------------------- the arms --
+
+def time_oracle(wl, budget_s: float, max_rows=None):
+    """Time the CPU oracle on row samples of the workload for about budget_s seconds."""
+    import oracle
+    rows = wl.oracle_full_rows if max_rows is None else min(max_rows, wl.oracle_full_rows)
+    t0 = time.perf_counter()
+    wl.oracle_step(rows)
+    t1 = time.perf_counter() - t0
+    # shrink the sample if one full step is longer than the budget
+    while t1 > budget_s and rows > 1:
+        rows = max(1, rows // 4)
+        t0 = time.perf_counter()
+        wl.oracle_step(rows)
+        t1 = time.perf_counter() - t0
+    reps, total = 1, t1
+    while total < budget_s:
+        t0 = time.perf_counter()
+        wl.oracle_step(rows)
+        total += time.perf_counter() - t0
+        reps += 1
+    units = wl.oracle_units(rows) * reps
+    return {"value": wl.value(units, total), "unit": wl.unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} run(s) of {rows} of {wl.oracle_full_rows} rows, {total:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401
+    import oracle  # noqa: F401
+    from w8a8_dynamic_quant_gb300 import synthetic as S
+    # the oracle arm needs only host data: build the workload's host side on the CPU
+    if S.CONFIGS[args.workload]["kind"] == "dense":
+        wl = _HostDense(args.workload)
+    else:
+        wl = _HostMoE(args.workload)
+    for _ in range(args.warmup):
+        wl.oracle_step(wl.step_rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        wl.oracle_step(wl.step_rows)
+    dt = time.perf_counter() - t0
+    units = wl.oracle_units(wl.step_rows) * args.steps
+    value = wl.value(units, dt)
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": wl.config(),
+            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": cores, "kind": "oracle",
+                             "sample": f"{wl.step_rows} of {wl.oracle_full_rows} rows per step"},
+            "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+class _HostDense(Dense):
+    def __init__(self, cfg_id):
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        self.d = S.dense_config(cfg_id)
+        self.name = self.d.name
+        self.M, self.N, self.K = self.d.M, self.d.N, self.d.K
+        self.unit = "TOPS"
+        self.input_note = "host arrays (CPU oracle)"
+        # about 0.1-0.5 s of CPU per step on 16 cores
+        self.step_rows = max(1, min(self.M, int(2e9 // (2 * self.N * self.K))))
+
+
+class _HostMoE(MoE):
+    def __init__(self, cfg_id):
+        import numpy as np
+        import torch
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        self.np, self.torch = np, torch
+        self.m = S.moe_config(cfg_id, device="cpu")
+        self.name = self.m.name
+        self.unit = "tokens/s"
+        self.input_note = "host arrays (CPU oracle)"
+        self.step_rows = 8
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    import __graft_entry__
+    __graft_entry__.build()
+    peaks = load_peaks()
+    wl = make_workload(args.workload, device)
+    stream = torch.cuda.current_stream(device)
+
+    # one CUDA graph per kernel type over all rotating input sets
+    graphs = {}
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for k in wl.kernels:
+            for i in range(wl.n_sets):
+                wl.launch(k, i)  # warm the launch path before capture
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    for k in wl.kernels:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(wl.n_sets):
+                wl.launch(k, i)
+        graphs[k] = g
+    torch.cuda.synchronize()
+
+    def replay_round(events=None):
+        for j, k in enumerate(wl.kernels):
+            if events is not None:
+                events[j].record(stream)
+            graphs[k].replay()
+        if events is not None:
+            events[-1].record(stream)
+
+    rounds_w = max(1, -(-args.warmup // wl.n_sets))
+    for _ in range(rounds_w):
+        replay_round()
+    rounds = max(1, -(-args.steps // wl.n_sets))
+    steps = rounds * wl.n_sets
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(wl.kernels) + 1)] for _ in range(rounds)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall0 = time.perf_counter()
+        for r in range(rounds):
+            replay_round(ev[r])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        # keep the GPU loaded long enough for the clock sampler to see it
+        extra = 0
+        while not args.quick and time.perf_counter() - t_wall0 < 1.0 and extra < 100000:
+            replay_round()
+            extra += 1
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.summary()
+    per_kernel_ms = {k: sum(ev[r][j].elapsed_time(ev[r][j + 1]) for r in range(rounds)) / steps
+                     for j, k in enumerate(wl.kernels)}
+    step_ms = sum(per_kernel_ms.values())
+    units, seconds = aggregate(wl.units_per_step * steps, step_ms * steps / 1e3)
+    value = wl.value(units, seconds)
+
+    # e2e through the public API with host buffers
+    wl.e2e_setup(device)
+    for _ in range(3):
+        wl.e2e_step()
+    e2e_steps = 3 if args.quick else max(3, min(args.steps, 200))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        wl.e2e_step()
+    e2e_s = time.perf_counter() - t0
+    e_units, e_seconds = aggregate(wl.units_per_step * e2e_steps, e2e_s)
+
+    # dominant kernel roofline
+    dom = max(per_kernel_ms, key=per_kernel_ms.get)
+    dur_s = per_kernel_ms[dom] / 1e3
+    if wl.bound == "hbm":
+        achieved = wl.alg_bytes[dom] / dur_s / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = wl.alg_flops[dom] / dur_s / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    traffic = recorded_traffic(dom, wl.name)
+    roofline = {"bound": wl.bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic, "kernel": dom, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback",
+                "alg_bytes_per_launch": wl.alg_bytes[dom],
+                "per_kernel_us": {k: v * 1e3 for k, v in per_kernel_ms.items()}}
+    if "dynamic_quant" in per_kernel_ms:
+        roofline["quant_gbs"] = wl.alg_bytes["dynamic_quant"] / (per_kernel_ms["dynamic_quant"] / 1e3) / 1e9
+    if dom in wl.alg_flops:
+        roofline["tops_dominant"] = wl.alg_flops[dom] / dur_s / 1e12
+
+    line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,
+            "warmup": rounds_w * wl.n_sets, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": wl.config(),
+            "roofline": roofline, "clocks": clocks, "gpu_launches": steps * wl.launches_per_step,
+            "e2e": {"value": wl.value(e_units, e_seconds), "unit": wl.unit, "h2d_bytes_per_step": wl.h2d,
+                    "d2h_bytes_per_step": wl.d2h},
+            "wall_s_timed_region": t_wall}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(wl, args.cpu_budget)
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="short run for profiler captures: no clock-sampling hold, 3 e2e steps")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
