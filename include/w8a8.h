@@ -189,6 +189,24 @@ W8A8_API w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_sca
 W8A8_API int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int which);
 
 /* ------------------------------------------------------------------------ */
+/* Dense quantised matmul without a caller workspace.  The pages have no     */
+/* counterpart: this exists for callers that cannot allocate device memory   */
+/* (a plugin interface without an allocator, a host that reserved all HBM    */
+/* for its own pools, code where cudaMalloc is not allowed).                 */
+/* ------------------------------------------------------------------------ */
+
+/* Same arguments and result as w8a8_quant_matmul, minus the workspace.  The
+ * scratch lives in a fixed 8 MiB device array inside the library (held by every
+ * GPU that loads it until exit); problems that need more (roughly M*N > 2M)
+ * return W8A8_ERR_WORKSPACE before any launch.  The first call on a device
+ * looks up the array's address and should come before any stream capture.
+ * All calls share the array: calls that overlap on the GPU race.  Allocates
+ * nothing. */
+W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const float* x_scale, int64_t M, int64_t K,
+                                               const void* w_packed, const float* w_scale, int64_t N,
+                                               const uint16_t* bias, uint16_t* y, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Device status                                                             */
 /* ------------------------------------------------------------------------ */
 

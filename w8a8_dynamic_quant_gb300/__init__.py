@@ -23,7 +23,7 @@ __all__ = [
     "w8a8_dynamic_quant", "quant_matmul_workspace_bytes", "w8a8_quant_matmul",
     "w8a8_int8_matmul_acc", "grouped_matmul_workspace_bytes", "w8a8_grouped_matmul",
     "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
-    "moe_w13_swiglu_requant_w2", "read_device_status", "workspace",
+    "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
 ]
 
 
@@ -115,6 +115,29 @@ def w8a8_quant_matmul(q: torch.Tensor, x_scale: torch.Tensor, w_packed: torch.Te
         _capi.check("w8a8_quant_matmul", _capi.lib().w8a8_quant_matmul(
             q.data_ptr(), x_scale.data_ptr(), M, K, w_packed.data_ptr(), w_scale.data_ptr(), N,
             _ptr(bias), y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)))
+    return y
+
+
+def w8a8_quant_matmul_noalloc(q: torch.Tensor, x_scale: torch.Tensor, w_packed: torch.Tensor,
+                              w_scale: torch.Tensor, N: int, bias: Optional[torch.Tensor] = None,
+                              y: Optional[torch.Tensor] = None):
+    """w8a8_quant_matmul for callers that cannot allocate device memory: the
+    library's built-in scratch array replaces the workspace (y must be given by
+    such callers; it is allocated here only for convenience)."""
+    _need(q, "q", torch.int8)
+    M, K = q.shape
+    dev = q.device
+    _need(x_scale, "x_scale", torch.float32, (M,), dev)
+    _need(w_packed, "w_packed", torch.uint8, None, dev)
+    _need(w_scale, "w_scale", torch.float32, (N,), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, (N,), dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if y is None else y
+    _need(y, "y", torch.bfloat16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_quant_matmul_noalloc", _capi.lib().w8a8_quant_matmul_noalloc(
+            q.data_ptr(), x_scale.data_ptr(), M, K, w_packed.data_ptr(), w_scale.data_ptr(), N,
+            _ptr(bias), y.data_ptr(), _stream(dev)))
     return y
 
 

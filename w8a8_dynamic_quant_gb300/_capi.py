@@ -34,6 +34,7 @@ SIGNATURES = {
     "moe_workspace_offset": (_i64, [_i64, _i64, _i64, _i64, _int]),
     "moe_w13_swiglu_requant_w2": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz,
                                          _vp, _vp]),
+    "w8a8_quant_matmul_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp]),
     "w8a8_read_device_status": (_int, [_vp, _vp]),
 }
 
