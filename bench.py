@@ -181,17 +181,20 @@ class Dense:
         self.name = d.name
         M, N, K = d.M, d.N, d.K
         self.M, self.N, self.K = M, N, K
-        set_bytes = 2 * M * K + M * K + N * K + 2 * M * N
+        set_bytes = 2 * M * K + M * K + N * K * (3 if M >= 128 else 1) + 2 * M * N
         self.n_sets = max(1, -(-int(1.2 * L2_BYTES) // set_bytes))
         self.n_sets = min(self.n_sets, 16)
         xd = torch.from_numpy(d.x.view("int16")).to(device).view(torch.bfloat16)
-        wp = W.w8a8_prepack_weight(torch.from_numpy(d.w).to(device))
+        wd = torch.from_numpy(d.w).to(device)
+        # large M runs on the tcgen05 engine, which reads the fp16 copy of the weight
+        self.pack_flags = W.PACK_F16 if M >= 128 else 0
         sw = torch.from_numpy(d.w_scale).to(device)
         bias = None if d.bias is None else torch.from_numpy(d.bias.view("int16")).to(device).view(torch.bfloat16)
         self.sets = []
         for i in range(self.n_sets):
             self.sets.append(dict(
-                x=xd.clone(), wp=wp.clone() if i else wp, sw=sw.clone(), bias=None if bias is None else bias.clone(),
+                x=xd.clone(), wp=W.w8a8_prepack_weight(wd, self.pack_flags), sw=sw.clone(),
+                bias=None if bias is None else bias.clone(),
                 q=torch.empty((M, K), dtype=torch.int8, device=device),
                 s=torch.empty((M,), dtype=torch.float32, device=device),
                 y=torch.empty((M, N), dtype=torch.bfloat16, device=device),
@@ -267,8 +270,9 @@ class MoE:
         self.m = m
         self.name = m.name
         self.n_sets = 1
-        self.w13p = W.w8a8_prepack_weight(m.w13, W.PACK_GATE_UP)
-        self.w2p = W.w8a8_prepack_weight(m.w2)
+        f16 = W.PACK_F16 if m.R >= 64 * m.E else 0  # prefill-sized groups: tcgen05 engine
+        self.w13p = W.w8a8_prepack_weight(m.w13, W.PACK_GATE_UP | f16)
+        self.w2p = W.w8a8_prepack_weight(m.w2, f16)
         self.gl = torch.from_numpy(m.group_list).to(device)
         self.s13 = torch.from_numpy(m.s13).to(device)
         self.s2 = torch.from_numpy(m.s2).to(device)

@@ -1,0 +1,146 @@
+"""GPU parity of the tcgen05 engine (large-M shapes, weights packed with their
+fp16 copy): INT32 accumulators, BF16 outputs and the MoE intermediates must be
+bit-exact against the oracle.  Each test also checks that the engine really
+ran, through the fp16 activation copy it leaves in the workspace."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_dynamic_quant_gb300 as W
+from w8a8_dynamic_quant_gb300 import synthetic as S
+
+from gpu_helpers import dev, dev_bf16, f32_bits, host_bits, moe_subset_oracle, sample_rows
+
+pytestmark = pytest.mark.gpu
+F16 = W.PACK_F16
+
+
+def a16_region(ws, rows, K):
+    """The fp16 activation copy the tcgen05 engine writes: the last 256-aligned block of rows*K*2 bytes."""
+    nbytes = rows * K * 2
+    start = ws.numel() - (nbytes + 255) // 256 * 256
+    return ws[start:start + nbytes].view(torch.float16).view(rows, K)
+
+
+def tc_dense(q, xs, w, wsc, bias=None):
+    M, K = q.shape
+    N = w.shape[0]
+    wp = W.w8a8_prepack_weight(dev(w), F16)
+    ws = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
+    y = W.w8a8_quant_matmul(dev(q), dev(xs), wp, dev(wsc), N, None if bias is None else dev_bf16(bias), ws=ws)
+    ws2 = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
+    acc = W.w8a8_int8_matmul_acc(dev(q), wp, N, ws=ws2)
+    torch.cuda.synchronize()
+    # the tcgen05 engine widens q to fp16 at the end of the workspace
+    assert torch.equal(a16_region(ws, M, K).cpu(), torch.from_numpy(q.astype(np.float16))), \
+        "tcgen05 engine did not run"
+    return host_bits(y), acc.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N,K,bias", [(128, 256, 64, False), (130, 200, 80, True), (300, 512, 1040, True),
+                                        (256, 384, 4096, False), (1000, 768, 2064, True), (129, 2048, 7168, False)])
+def test_tc_dense_exact(M, N, K, bias):
+    d = S.make_dense(M, K, N, n_outlier=min(4, K), outlier_mult=20.0, bias=bias, seed=M * 3 + N + K)
+    q, xs = oracle.dynamic_quant(d.x)
+    y, acc = tc_dense(q, xs, d.w, d.w_scale, d.bias)
+    assert np.array_equal(acc, oracle.int8_gemm_acc(q, d.w))
+    assert np.array_equal(y, oracle.quant_matmul(q, xs, d.w, d.w_scale, d.bias))
+
+
+def test_tc_accumulation_exact_at_extremes():
+    K = 65536
+    M = 128
+    q = np.full((M, K), 127, np.int8)
+    q[1] = -127
+    q[2] = -128
+    q[3, ::2] = -127
+    q[4:] = np.random.default_rng(0).integers(-127, 128, (M - 4, K), dtype=np.int8)
+    w = np.full((256, K), 127, np.int8)
+    w[1] = -128
+    w[2, : K // 2] = 1
+    w[3, ::3] = -127
+    w[4:] = np.random.default_rng(1).integers(-128, 128, (252, K), dtype=np.int8)
+    _, acc = tc_dense(q, np.ones(M, np.float32), w, np.ones(256, np.float32))
+    ref = q.astype(np.int64) @ w.astype(np.int64).T
+    assert np.array_equal(acc.astype(np.int64), ref)
+
+
+def test_tc_dense_prefill_config_sampled_rows():
+    d = S.dense_config(3)
+    q, xs = oracle.dynamic_quant(d.x)
+    wp = W.w8a8_prepack_weight(dev(d.w), F16)
+    qd = dev(q)
+    ws = W.workspace(W.quant_matmul_workspace_bytes(d.M, d.N, d.K))
+    y = W.w8a8_quant_matmul(qd, dev(xs), wp, dev(d.w_scale), d.N, ws=ws)
+    acc = W.w8a8_int8_matmul_acc(qd, wp, d.N)
+    rows = sample_rows(d.M, 40, seed=5)
+    idx = torch.as_tensor(rows, device="cuda")
+    assert np.array_equal(acc[idx].cpu().numpy(), oracle.int8_gemm_acc(q[rows], d.w))
+    assert np.array_equal(host_bits(y[idx]), oracle.quant_matmul(q[rows], xs[rows], d.w, d.w_scale, None))
+    assert torch.equal(a16_region(ws, d.M, d.K).cpu(), torch.from_numpy(q.astype(np.float16)))
+
+
+@pytest.mark.parametrize("gl,K,N", [([300, 0, 129, 77, 0, 200], 512, 256), ([64] * 8, 1024, 512),
+                                    ([0, 0, 1000, 24], 2064, 384)])
+def test_tc_grouped_exact(gl, K, N):
+    rng = np.random.default_rng(sum(gl) + K)
+    R, E = int(sum(gl)), len(gl)
+    x = S.to_bf16_bits(rng.standard_normal((R, K)).astype(np.float32))
+    q, xs = oracle.dynamic_quant(x)
+    w = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
+    wsc = rng.uniform(1e-3, 1e-2, (E, N)).astype(np.float32)
+    glnp = np.asarray(gl, np.int64)
+    wp = W.w8a8_prepack_weight(dev(w), F16)
+    ws = W.workspace(W.grouped_matmul_workspace_bytes(E, R, N, K))
+    y = torch.full((R, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    y = W.w8a8_grouped_matmul(dev(q), dev(xs), dev(glnp), wp, dev(wsc), ws=ws, y=y)
+    acc = W.w8a8_grouped_matmul_acc(dev(q), dev(glnp), wp, N)
+    torch.cuda.synchronize()
+    assert torch.equal(a16_region(ws, R, K).cpu(), torch.from_numpy(q.astype(np.float16))), \
+        "tcgen05 engine did not run"
+    y_ref, acc_ref = oracle.grouped_matmul(q, xs, glnp, w, wsc, want_acc=True)
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert np.array_equal(host_bits(y), y_ref)
+
+
+def tc_moe(m):
+    w13p = W.w8a8_prepack_weight(m.w13.cuda(), W.PACK_GATE_UP | F16)
+    w2p = W.w8a8_prepack_weight(m.w2.cuda(), F16)
+    x, xs = (dev_bf16(m.x), None) if m.x_scale is None else (dev(m.x), dev(m.x_scale))
+    ws = W.workspace(W.moe_workspace_bytes(m.R, m.H, m.I, m.E))
+    y = W.moe_w13_swiglu_requant_w2(x, xs, dev(m.group_list), w13p, dev(m.s13), w2p, dev(m.s2), ws=ws)
+    torch.cuda.synchronize()
+    off16 = W.moe_workspace_offset(m.R, m.H, m.I, m.E, 5)
+    assert off16 > 0
+    xq16 = ws[off16: off16 + m.R * m.H * 2].view(torch.float16)
+    assert bool((xq16 != 0).any()), "tcgen05 engine did not run"
+    return host_bits(y), ws
+
+
+def ws_slice(ws, m, which, dtype, shape):
+    off = W.moe_workspace_offset(m.R, m.H, m.I, m.E, which)
+    n = int(np.prod(shape)) * np.dtype(dtype).itemsize
+    return ws[off:off + n].cpu().numpy().view(dtype).reshape(shape)
+
+
+@pytest.mark.parametrize("prequant", [False, True])
+def test_tc_moe_small_full(prequant):
+    m = S.make_moe(T=256, H=256, I=128, E=4, topk=2, routing="zipf", zipf_s=1.1, n_dead=0,
+                   prequant=prequant, seed=21)
+    y, ws = tc_moe(m)
+    y_ref, it = oracle.moe_w13_swiglu_requant_w2(m.x, m.x_scale, m.group_list, m.w13.numpy(), m.s13,
+                                                 m.w2.numpy(), m.s2, intermediates=True)
+    assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I)), it["h"])
+    assert np.array_equal(ws_slice(ws, m, 3, np.int8, (m.R, m.I)), it["hq"])
+    assert np.array_equal(f32_bits(ws_slice(ws, m, 4, np.float32, (m.R,))), f32_bits(it["hs"]))
+    assert np.array_equal(y, y_ref)
+
+
+def test_tc_moe_prefill_config_sampled_rows():
+    m = S.moe_config(4, device="cuda")
+    y, ws = tc_moe(m)
+    rows = sample_rows(m.R, 24, seed=9)
+    y_ref, it = moe_subset_oracle(m, rows)
+    assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I))[rows], it["h"])
+    assert np.array_equal(y[rows], y_ref)

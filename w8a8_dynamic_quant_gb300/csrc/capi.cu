@@ -48,18 +48,69 @@ w8a8_status device_info(int& sms) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
 inline w8a8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA; }
 
+// Shapes that go to the tcgen05 engine (the tiling choice by M of page
+// "DeepSeek-V4 W8A8 执行链从量化权重到 Ascend INT8 算子" §四: prefill vs decode).
+constexpr int64_t kTcMinM = 128;           // dense rows
+constexpr int64_t kTcMinRowsPerGroup = 64;  // grouped: average rows per expert
+
+bool tc_shape(int64_t E, int64_t R) {
+  return E <= 1 ? R >= kTcMinM : R >= kTcMinRowsPerGroup * E;
+}
+
+// Host record of the packed buffers this process made, so a call can tell
+// (without reading device memory) whether a buffer carries the fp16 copy the
+// tcgen05 engine reads.  Buffers not found here use the warp-level engine.
+struct PackRecord {
+  const void* ptr;
+  int64_t E, N, K;
+  uint32_t flags;
+};
+constexpr int kMaxPackRecords = 4096;
+PackRecord g_packs[kMaxPackRecords];
+int g_npacks = 0;
+int g_pack_next = 0;
+std::mutex g_pack_mu;
+
+void record_pack(const void* ptr, int64_t E, int64_t N, int64_t K, uint32_t flags) {
+  std::lock_guard<std::mutex> lk(g_pack_mu);
+  for (int i = 0; i < g_npacks; ++i)
+    if (g_packs[i].ptr == ptr) {
+      g_packs[i] = PackRecord{ptr, E, N, K, flags};
+      return;
+    }
+  if (g_npacks < kMaxPackRecords) {
+    g_packs[g_npacks++] = PackRecord{ptr, E, N, K, flags};
+  } else {
+    g_packs[g_pack_next] = PackRecord{ptr, E, N, K, flags};
+    g_pack_next = (g_pack_next + 1) % kMaxPackRecords;
+  }
+}
+
+// Device address of the fp16 copy of a packed buffer, or nullptr.
+const void* pack_f16(const void* ptr, int64_t E, int64_t N, int64_t K, uint32_t need_flags) {
+  std::lock_guard<std::mutex> lk(g_pack_mu);
+  for (int i = 0; i < g_npacks; ++i) {
+    const PackRecord& r = g_packs[i];
+    if (r.ptr == ptr && r.E == E && r.N == N && r.K == K && (r.flags & W8A8_PACK_F16) &&
+        (r.flags & W8A8_PACK_GATE_UP) == (need_flags & W8A8_PACK_GATE_UP))
+      return static_cast<const uint8_t*>(ptr) + pack_layout(E, N, K, r.flags).f16_offset;
+  }
+  return nullptr;
+}
+
 w8a8_status check_k(int64_t K) {
   if (K <= 0 || K > W8A8_MAX_K) return W8A8_ERR_SHAPE;
   if (K % 16 != 0) return W8A8_ERR_ALIGN;
   return W8A8_OK;
 }
 
-// Workspace of one contraction: status word, then split-K partials + counters.
+// Workspace of one contraction: status word, split-K partials + counters, and
+// (for shapes the tcgen05 engine takes) the activations as fp16.
 struct GemmWs {
-  size_t status = 0, acc = 0, count = 0, total = 0;
+  size_t status = 0, acc = 0, count = 0, a16 = 0, total = 0;
   int64_t count_len = 0;
 };
-GemmWs gemm_ws_layout(int64_t E, int64_t R, int64_t N, int64_t K) {
+GemmWs gemm_ws_layout(int64_t E, int64_t R, int64_t N, int64_t K, bool with_a16 = true) {
   GemmWs L;
   L.status = 0;
   L.acc = kStatusBytes;
@@ -67,8 +118,8 @@ GemmWs gemm_ws_layout(int64_t E, int64_t R, int64_t N, int64_t K) {
   L.count = L.acc + acc_bytes;
   const int64_t nb = (N + 127) / 128;
   L.count_len = ((R + 7) / 8 + (E > 1 ? E : 0)) * nb;
-  L.total = L.count + align_up(static_cast<uint64_t>(L.count_len) * 4, 256);
-  (void)K;
+  L.a16 = L.count + align_up(static_cast<uint64_t>(L.count_len) * 4, 256);
+  L.total = L.a16 + ((with_a16 && tc_shape(E, R)) ? align_up(static_cast<uint64_t>(R) * K * 2, 256) : 0);
   return L;
 }
 
@@ -81,7 +132,7 @@ void bind_ws(GemmArgs& a, void* ws, const GemmWs& L) {
 }
 
 struct MoeWs {
-  size_t xq, xs, h, hq, hs, gemm, total;
+  size_t xq, xs, h, hq, hs, xq16, hq16, gemm, total;
   GemmWs g;
 };
 MoeWs moe_layout(int64_t R, int64_t H, int64_t I, int64_t E) {
@@ -92,20 +143,33 @@ MoeWs moe_layout(int64_t R, int64_t H, int64_t I, int64_t E) {
   L.h = off;  off = align_up(off + static_cast<uint64_t>(R) * I * 2, 256);
   L.hq = off; off = align_up(off + static_cast<uint64_t>(R) * I, 256);
   L.hs = off; off = align_up(off + static_cast<uint64_t>(R) * 4, 256);
-  // one split-K region serves both contractions (they run one after the other)
-  const GemmWs g13 = gemm_ws_layout(E, R, 2 * I, H);
-  const GemmWs g2 = gemm_ws_layout(E, R, H, I);
+  L.xq16 = L.hq16 = 0;
+  if (tc_shape(E, R)) {  // fp16 copies of the int8 codes for the tcgen05 engine
+    L.xq16 = off; off = align_up(off + static_cast<uint64_t>(R) * H * 2, 256);
+    L.hq16 = off; off = align_up(off + static_cast<uint64_t>(R) * I * 2, 256);
+  }
+  // one split-K region serves both contractions (they run one after the other);
+  // the fp16 activations of the tcgen05 engine live in xq16 / hq16 instead
+  const GemmWs g13 = gemm_ws_layout(E, R, 2 * I, H, false);
+  const GemmWs g2 = gemm_ws_layout(E, R, H, I, false);
   L.g = g13.total >= g2.total ? g13 : g2;
   L.gemm = off;
   L.total = off + L.g.total;
   return L;
 }
 
+// One contraction on the engine its shape calls for: tcgen05 (activations
+// widened to fp16 in the workspace) when the shape is large and the weight
+// carries its fp16 copy, else the warp-level engine.
 w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream, int sms) {
   bind_ws(a, ws, L);
-  // the status word of a contraction inside a bigger workspace is the
-  // workspace's own first word
   a.status = static_cast<DeviceStatus*>(ws);
+  const void* b16 = (L.a16 < L.total) ? pack_f16(a.packed, a.E, a.N, a.K, a.pack_flags) : nullptr;
+  if (b16 != nullptr) {
+    uint16_t* a16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.a16);
+    if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
+    return cuda_status(launch_tc_gemm(a, a16, b16, sms, stream));
+  }
   const GemmPlan p = plan_reg_gemm(a, sms);
   return cuda_status(launch_reg_gemm(a, p, stream));
 }
@@ -147,7 +211,10 @@ w8a8_status w8a8_prepack_weight(const int8_t* w, int64_t E, int64_t N, int64_t K
   if (!aligned16(w) || (reinterpret_cast<uintptr_t>(packed) & 255u)) return W8A8_ERR_ALIGN;
   int sms = 0;
   if (w8a8_status s = device_info(sms)) return s;
-  return cuda_status(launch_prepack(w, E, N, K, flags, packed, reinterpret_cast<cudaStream_t>(stream), sms));
+  const w8a8_status st =
+      cuda_status(launch_prepack(w, E, N, K, flags, packed, reinterpret_cast<cudaStream_t>(stream), sms));
+  if (st == W8A8_OK) record_pack(packed, E, N, K, flags);
+  return st;
 }
 
 w8a8_status w8a8_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
@@ -269,6 +336,8 @@ int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int whi
     case 2: return static_cast<int64_t>(L.h);
     case 3: return static_cast<int64_t>(L.hq);
     case 4: return static_cast<int64_t>(L.hs);
+    case 5: return L.xq16 ? static_cast<int64_t>(L.xq16) : -1;
+    case 6: return L.hq16 ? static_cast<int64_t>(L.hq16) : -1;
     default: return -1;
   }
 }
@@ -297,17 +366,27 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
 
   const int8_t* xq = static_cast<const int8_t*>(x);
   const float* xs = x_scale;
-  if (x_scale == nullptr) {  // BF16 input: quantise once; an INT8 input with its scale is used as is
-    int8_t* q = reinterpret_cast<int8_t*>(b + L.xq);
-    float* s = reinterpret_cast<float*>(b + L.xs);
-    if (w8a8_status e = cuda_status(launch_dynamic_quant(static_cast<const uint16_t*>(x), R, H, q, s, st, sms)))
-      return e;
-    xq = q;
-    xs = s;
-  }
   uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
   int8_t* hq = reinterpret_cast<int8_t*>(b + L.hq);
   float* hs = reinterpret_cast<float*>(b + L.hs);
+  const void* w13_16 = L.xq16 ? pack_f16(w13_packed, E, 2 * I, H, W8A8_PACK_GATE_UP) : nullptr;
+  const void* w2_16 = L.xq16 ? pack_f16(w2_packed, E, H, I, 0u) : nullptr;
+  const bool tc = w13_16 != nullptr && w2_16 != nullptr;
+  uint16_t* xq16 = tc ? reinterpret_cast<uint16_t*>(b + L.xq16) : nullptr;
+  uint16_t* hq16 = tc ? reinterpret_cast<uint16_t*>(b + L.hq16) : nullptr;
+
+  if (x_scale == nullptr) {  // BF16 input: quantise once; an INT8 input with its scale is used as is
+    int8_t* q = reinterpret_cast<int8_t*>(b + L.xq);
+    float* s = reinterpret_cast<float*>(b + L.xs);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    const cudaError_t e = tc ? launch_dynamic_quant_dual(xb, R, H, q, xq16, s, st, sms)
+                             : launch_dynamic_quant(xb, R, H, q, s, st, sms);
+    if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    xq = q;
+    xs = s;
+  } else if (tc) {
+    if (w8a8_status e = cuda_status(launch_s8_to_f16(xq, xq16, R * H, st, sms))) return e;
+  }
 
   GemmArgs a13;
   a13.q = xq;
@@ -324,9 +403,13 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   a13.mode = EPI_SWIGLU;
   bind_ws(a13, gws, L.g);
   a13.status = static_cast<DeviceStatus*>(ws);
-  if (w8a8_status e = cuda_status(launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st))) return e;
+  const cudaError_t e13 = tc ? launch_tc_gemm(a13, xq16, w13_16, sms, st)
+                             : launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st);
+  if (e13 != cudaSuccess) return W8A8_ERR_CUDA;
 
-  if (w8a8_status e = cuda_status(launch_dynamic_quant(h, R, I, hq, hs, st, sms))) return e;
+  const cudaError_t eq = tc ? launch_dynamic_quant_dual(h, R, I, hq, hq16, hs, st, sms)
+                            : launch_dynamic_quant(h, R, I, hq, hs, st, sms);
+  if (eq != cudaSuccess) return W8A8_ERR_CUDA;
 
   GemmArgs a2;
   a2.q = hq;
@@ -343,7 +426,9 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   a2.mode = EPI_BF16;
   bind_ws(a2, gws, L.g);
   a2.status = static_cast<DeviceStatus*>(ws);
-  return cuda_status(launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st));
+  const cudaError_t e2 = tc ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
+                            : launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st);
+  return e2 == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
 }
 
 w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream) {

@@ -1,0 +1,576 @@
+// gemm_tc.cu -- exact INT8 contraction on the 5th-generation tensor cores
+// (tcgen05) for large-M shapes: the dense prefill linear and the grouped
+// expert GEMMs of MoE prefill.
+//
+// Page "DeepSeek-V4 W8A8 执行链从量化权重到 Ascend INT8 算子": §二
+// npu_quant_matmul (INT8 x INT8 -> INT32, then * x_scale * w_scale (+bias) ->
+// BF16), §三 npu_grouped_matmul over group_list and the W13 -> SwiGLU step,
+// §四 (prefill, large M, gets its own tiling).
+//
+// Engine.  sm_103a has no integer tcgen05.mma kind, so the int8 operands are
+// fed as integer-valued FP16 (exact) to tcgen05.mma.kind::f16 with FP32
+// accumulators in tensor memory.  Products |a*b| <= 2^14 are exact and a
+// fresh accumulator is started every 1024 K (|partial| <= 2^24, all partial
+// sums exactly representable), so every accumulator holds an exact integer.
+// Two TMEM accumulators of 128 lanes x 256 columns alternate between
+// consecutive 1024-deep chunks; the epilogue warps drain a finished chunk into
+// int32 registers while the MMA fills the other one.
+//
+// Data movement.  Both operands are K-major FP16 tiles brought in by TMA
+// (cp.async.bulk.tensor, 128-byte swizzle) into a 4-stage ring: A = 128
+// activation rows x 64 K, B = 256 weight rows x 64 K (48 KB per stage).  One
+// elected thread issues tcgen05.mma M=128 N=256 K=16 four times per stage.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer
+//   warp 1     TMEM owner and MMA issuer
+//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and one half
+//              (128 columns) of the tile; each thread owns one output row.
+// Every mbarrier wait is bounded (%globaltimer, 2 s): on expiry the CTA sets
+// W8A8_ERR_DEVICE_TIMEOUT in the status word, lets in-flight copies land,
+// frees its TMEM and returns.
+#include <cuda.h>
+
+#include "kernels.cuh"
+
+namespace w8a8 {
+
+namespace {
+
+constexpr int TC_BM = 128;
+constexpr int TC_BN = 256;
+constexpr int TC_BK = 64;  // fp16 elements = 128 bytes = one swizzle row
+constexpr int TC_STAGES = 4;
+constexpr int TC_KB_PER_CHUNK = kChunkK / TC_BK;  // 16
+constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 2;
+constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 2;
+constexpr uint32_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
+constexpr int TC_THREADS = 320;
+constexpr int TC_EPI_WARPS = 8;
+constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column fp32 accumulators
+constexpr int kMaxE = 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// kind::f16 instruction descriptor: D = F32, A = B = F16, both K-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(TC_BN >> 3) << 17) | (uint32_t(TC_BM >> 4) << 24);
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.  Returns false
+// when the CTA is aborting (this wait gave up, or another one did).
+__device__ __noinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag, DeviceStatus* st,
+                                       uint32_t where) {
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(st, W8A8_ERR_DEVICE_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;    // leading byte offset (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;  // stride byte offset: next 8-row atom
+  d |= static_cast<uint64_t>(1u) << 46;          // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;          // 128-byte swizzle
+  return d;
+}
+
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* s_warp) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) {
+    const int s = s_warp[i];
+    if (i < w) before += s;
+    tot += s;
+  }
+  __syncthreads();
+  total = tot;
+  return before + x - v;
+}
+
+__device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
+
+struct TileInfo {
+  int e, mb, nb, cnt;
+  int64_t row0;  // first global row of the tile (into the [R,K] activation matrix)
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int* tile_prefix, const int* row_off) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  const int local = t - tile_prefix[lo];
+  ti.cnt = row_off[lo + 1] - row_off[lo];
+  const int mblocks = (ti.cnt + TC_BM - 1) / TC_BM;
+  ti.mb = local % mblocks;
+  ti.nb = local / mblocks;
+  (void)NB;
+  ti.row0 = static_cast<int64_t>(row_off[lo]) + static_cast<int64_t>(ti.mb) * TC_BM;
+  return ti;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[TC_STAGES];
+  __shared__ __align__(8) uint64_t bar_empty[TC_STAGES];
+  __shared__ __align__(8) uint64_t bar_accf[2];
+  __shared__ __align__(8) uint64_t bar_acce[2];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+  __shared__ int s_bad;
+  __shared__ int s_tile_prefix[kMaxE + 1];
+  __shared__ int s_row_off[kMaxE + 1];
+  __shared__ int s_warp[TC_THREADS / 32];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = static_cast<int>(a.E);
+  const int64_t N = a.N;
+  const int64_t K = a.K;
+  const int NB = static_cast<int>((N + TC_BN - 1) / TC_BN);
+  const int nkb = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  const int nchunk = (nkb + TC_KB_PER_CHUNK - 1) / TC_KB_PER_CHUNK;
+
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_base = smem_u32(stages);
+
+  if (tid == 0) {
+    s_abort = 0;
+    s_bad = 0;
+    const PackedHeader* h = static_cast<const PackedHeader*>(a.packed);
+    if (h->magic != kPackMagic || h->version != kPackVersion || h->E != a.E || h->N != a.N || h->K != a.K ||
+        ((h->flags ^ a.pack_flags) & W8A8_PACK_GATE_UP) != 0u || (h->flags & W8A8_PACK_F16) == 0u)
+      s_bad = W8A8_ERR_PACKED;
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_accf[b]), 1);
+      mbar_init(smem_u32(&bar_acce[b]), TC_EPI_WARPS);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
+                 "r"(TC_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // ---- per-expert rows and tiles (block scans)
+  constexpr int kPer = (kMaxE + TC_THREADS - 1) / TC_THREADS;
+  int rows_loc = 0, tiles_loc = 0, neg = 0;
+  int cnts[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid * kPer + i;
+    int64_t c = 0;
+    if (e < E) c = a.group_list ? a.group_list[e] : a.R;
+    if (c < 0 || c > a.R) neg = 1;
+    const int ci = (c < 0 || c > a.R) ? 0 : static_cast<int>(c);
+    cnts[i] = ci;
+    rows_loc += ci;
+    tiles_loc += ((ci + TC_BM - 1) / TC_BM) * NB;
+  }
+  int rows_total, tiles_total;
+  int row_before = block_exclusive_scan<TC_THREADS>(rows_loc, rows_total, s_warp);
+  int tile_before = block_exclusive_scan<TC_THREADS>(tiles_loc, tiles_total, s_warp);
+  if (neg) atomicOr(&s_bad, W8A8_ERR_GROUP_LIST << 8);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid * kPer + i;
+    if (e < E) {
+      s_row_off[e] = row_before;
+      s_tile_prefix[e] = tile_before;
+    }
+    row_before += cnts[i];
+    tile_before += ((cnts[i] + TC_BM - 1) / TC_BM) * NB;
+  }
+  if (tid == 0) {
+    s_row_off[E] = rows_total;
+    s_tile_prefix[E] = tiles_total;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  int bad = s_bad;
+  if (rows_total != a.R) bad |= W8A8_ERR_GROUP_LIST << 8;
+  if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, (bad & 0xff) ? (bad & 0xff) : (bad >> 8), 0u);
+  const int my_tiles = bad ? 0 : tiles_total;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < my_tiles && !s_abort; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off);
+        const int ya = static_cast<int>(ti.row0);
+        const int yb = static_cast<int>(static_cast<int64_t>(ti.e) * N + static_cast<int64_t>(ti.nb) * TC_BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
+          const uint32_t full = smem_u32(&bar_full[stage]);
+          mbar_expect_tx(full, TC_STAGE_BYTES);
+          const uint32_t sa = stage_base + stage * TC_STAGE_BYTES;
+          tma_load_2d(sa, &tmA, kb * TC_BK, ya, full);
+          tma_load_2d(sa + TC_A_BYTES, &tmB, kb * TC_BK, yb, full);
+          if (++stage == TC_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_count = 0;
+      for (int t = blockIdx.x; t < my_tiles && !s_abort; t += gridDim.x) {
+        for (int c = 0; c < nchunk && !s_abort; ++c) {
+          const uint32_t b = acc_count & 1u;
+          const uint32_t use = acc_count >> 1;
+          if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * TC_BN;
+          const int kb_end = min(nkb, (c + 1) * TC_KB_PER_CHUNK);
+          bool ok = true;
+          for (int kb = c * TC_KB_PER_CHUNK; kb < kb_end; ++kb) {
+            if (!mbar_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = stage_base + stage * TC_STAGE_BYTES;
+            const uint64_t adesc = smem_desc_sw128(sa);
+            const uint64_t bdesc = smem_desc_sw128(sa + TC_A_BYTES);
+#pragma unroll
+            for (int k = 0; k < TC_BK / 16; ++k) {
+              // +32 bytes per 16-element step along K inside the swizzled row
+              tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k,
+                     (kb > c * TC_KB_PER_CHUNK || k > 0) ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&bar_empty[stage]));
+            if (++stage == TC_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          tc_commit(smem_u32(&bar_accf[b]));
+          ++acc_count;
+          if (!ok) break;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;         // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;  // which 128-column half of the tile
+    const int r_loc = 32 * q + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    uint32_t acc_count = 0;
+    for (int t = blockIdx.x; t < my_tiles && !s_abort; t += gridDim.x) {
+      const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off);
+      int sums[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sums[i] = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunk; ++c) {
+        const uint32_t b = acc_count & 1u;
+        const uint32_t use = acc_count >> 1;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(smem_u32(&bar_accf[b]), use & 1u, &s_abort, a.status, 4u) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col0 = b * TC_BN + half * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + col0 + 32 * j, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sums[32 * j + i] += __float2int_rn(__uint_as_float(v[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_acce[b]));
+        ++acc_count;
+      }
+      if (!ok) break;
+
+      const int rows_valid = min(TC_BM, ti.cnt - ti.mb * TC_BM);
+      const int64_t n_base = static_cast<int64_t>(ti.nb) * TC_BN + half * 128;
+      if (r_loc < rows_valid && n_base < N) {
+        const int64_t gr = ti.row0 + r_loc;
+        if constexpr (MODE == EPI_ACC) {
+          int32_t* dst = static_cast<int32_t*>(a.out) + gr * N + n_base;
+          const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 3) == 0) && (n_base + 128 <= N);
+#pragma unroll
+          for (int c4 = 0; c4 < 32; ++c4) {
+            if (vec) {
+              reinterpret_cast<int4*>(dst)[c4] =
+                  make_int4(sums[4 * c4], sums[4 * c4 + 1], sums[4 * c4 + 2], sums[4 * c4 + 3]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (n_base + 4 * c4 + k < N) dst[4 * c4 + k] = sums[4 * c4 + k];
+            }
+          }
+        } else if constexpr (MODE == EPI_BF16) {
+          const float sx = a.x_scale[gr];
+          const float* sw = a.w_scale + static_cast<int64_t>(ti.e) * N;
+          uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * N + n_base;
+          const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 7) == 0) && (n_base + 128 <= N);
+#pragma unroll
+          for (int c8 = 0; c8 < 16; ++c8) {
+            uint16_t v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int64_t n = n_base + 8 * c8 + k;
+              float f = 0.0f;
+              if (n < N) {
+                f = dequant(sums[8 * c8 + k], sx, sw[n]);
+                if (a.bias) f = __fadd_rn(f, bf16_bits_to_f32(a.bias[n]));
+              }
+              v[k] = f32_to_bf16_bits(f);
+            }
+            if (vec) {
+              reinterpret_cast<uint4*>(dst)[c8] =
+                  make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
+                             v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (n_base + 8 * c8 + k < N) dst[8 * c8 + k] = v[k];
+            }
+          }
+        } else {  // EPI_SWIGLU: columns [0,64) gate j, [64,128) up j, j = n_base/2 + [0,64)
+          const float sx = a.x_scale[gr];
+          const int64_t I = N / 2;
+          const float* sw = a.w_scale + static_cast<int64_t>(ti.e) * N;
+          const int64_t j0 = (n_base / 128) * kGateUpBlock;
+          uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * I + j0;
+          const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((I & 7) == 0);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            uint16_t v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int jj = 8 * c8 + k;
+              const float gte = bf16_round(dequant(sums[jj], sx, sw[j0 + jj]));
+              const float up = bf16_round(dequant(sums[kGateUpBlock + jj], sx, sw[I + j0 + jj]));
+              v[k] = swiglu_bf16(gte, up);
+            }
+            if (vec) {
+              reinterpret_cast<uint4*>(dst)[c8] =
+                  make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
+                             v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) dst[8 * c8 + k] = v[k];
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: on abort, give in-flight copies and MMAs time to land first
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 20000000ull) {
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TC_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+__global__ void __launch_bounds__(256) s8_to_f16_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                                       int64_t n16) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s8x4_to_f16x4(w[k], h[2 * k], h[2 * k + 1]);
+    uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+    d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D fp16 tensor [rows, K] (K contiguous), box = box_rows x 64, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {TC_BK, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_tc_mode(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int grid, size_t smem,
+                           cudaStream_t stream) {
+  auto k = tc_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k<<<grid, TC_THREADS, smem, stream>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t tc_upper_tiles(int64_t E, int64_t R, int64_t N, bool grouped) {
+  return ((R + TC_BM - 1) / TC_BM + (grouped ? E : 0)) * ((N + TC_BN - 1) / TC_BN);
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream) {
+  if (a.R == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, a_f16, a.R, a.K, TC_BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, b_f16, a.E * a.N, a.K, TC_BN)) return cudaErrorInvalidValue;
+  const int64_t ub = tc_upper_tiles(a.E, a.R, a.N, a.group_list != nullptr);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ub, num_sms)));
+  const size_t smem = static_cast<size_t>(TC_STAGES) * TC_STAGE_BYTES + 1024;
+  switch (a.mode) {
+    case EPI_ACC: return launch_tc_mode<EPI_ACC>(ma, mb, a, grid, smem, stream);
+    case EPI_SWIGLU: return launch_tc_mode<EPI_SWIGLU>(ma, mb, a, grid, smem, stream);
+    default: return launch_tc_mode<EPI_BF16>(ma, mb, a, grid, smem, stream);
+  }
+}
+
+cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms) {
+  if (n == 0) return cudaSuccess;
+  const int64_t n16 = n / 16;
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((n16 + 255) / 256, static_cast<int64_t>(num_sms) * 8));
+  s8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, dst, n16);
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8

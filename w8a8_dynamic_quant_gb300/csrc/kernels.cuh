@@ -19,8 +19,9 @@ cudaError_t launch_prepack(const int8_t* w, int64_t E, int64_t N, int64_t K, uin
 
 cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                  cudaStream_t stream, int num_sms);
-cudaError_t launch_dynamic_quant_f16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q_f16, float* scale,
-                                     cudaStream_t stream, int num_sms);
+// int8 codes and the same codes as integer-valued fp16 (operand of the tcgen05 engine)
+cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
+                                      float* scale, cudaStream_t stream, int num_sms);
 
 // Epilogue of the contraction.
 enum EpiMode : int {
@@ -59,5 +60,11 @@ GemmPlan plan_reg_gemm(const GemmArgs& a, int num_sms);
 // Workspace (split-K partials + counters) the plan needs, in bytes.
 size_t reg_gemm_ws_bytes(int64_t E, int64_t R, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_reg_gemm(const GemmArgs& a, const GemmPlan& p, cudaStream_t stream);
+
+// tcgen05 engine (large M): both operands as integer-valued fp16, K-major.
+// a_f16: [R,K] activations; b_f16: [E*N,K] packed weights (fp16 copy).
+int64_t tc_upper_tiles(int64_t E, int64_t R, int64_t N, bool grouped);
+cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream);
+cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
 }  // namespace w8a8

@@ -74,6 +74,13 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   return r;
 }
 
+// OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both.
+__device__ __forceinline__ void store8(const uint4& v, float s, int64_t row, int64_t K, int64_t idx, void* q,
+                                       uint16_t* q16, int out) {
+  if (out != 1) reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v, s);
+  if (out != 0) reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -81,9 +88,9 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).
-template <int CH, bool F16OUT>
+template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
-                                                       int64_t K, void* __restrict__ q,
+                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                        float* __restrict__ scale) {
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = K / 8;
@@ -108,20 +115,16 @@ __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restric
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = lane + 32 * c;
       if (idx < nchunk) {
-        if (F16OUT) {
-          reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + row * K)[idx] = quant8_f16(v[c], s);
-        } else {
-          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v[c], s);
-        }
+        store8(v[c], s, row, K, idx, q, q16, OUT);
       }
     }
   }
 }
 
 // One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).
-template <int CH, bool F16OUT>
+template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
-                                                      int64_t K, void* __restrict__ q,
+                                                      int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                       float* __restrict__ scale) {
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
@@ -149,11 +152,7 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = threadIdx.x + 256 * c;
       if (idx < nchunk) {
-        if (F16OUT) {
-          reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + row * K)[idx] = quant8_f16(v[c], s);
-        } else {
-          reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v[c], s);
-        }
+        store8(v[c], s, row, K, idx, q, q16, OUT);
       }
     }
     __syncthreads();  // red[] is reused by the next row
@@ -161,9 +160,9 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
 }
 
 // Any K: two passes over the row (the second read mostly hits L2).
-template <bool F16OUT>
+template <int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __restrict__ x, int64_t M,
-                                                          int64_t K, void* __restrict__ q,
+                                                          int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                           float* __restrict__ scale) {
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
@@ -180,18 +179,14 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
     const float s = __fdiv_rn(amax, 127.0f);
     if (threadIdx.x == 0) scale[row] = s;
     for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) {
-      if (F16OUT) {
-        reinterpret_cast<uint4*>(static_cast<uint16_t*>(q) + row * K)[idx] = quant8_f16(xr[idx], s);
-      } else {
-        reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(xr[idx], s);
-      }
+      store8(xr[idx], s, row, K, idx, q, q16, OUT);
     }
     __syncthreads();
   }
 }
 
-template <bool F16OUT>
-cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, float* scale,
+template <int OUT>
+cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale,
                            cudaStream_t stream, int num_sms) {
   if (M == 0) return cudaSuccess;
   const int64_t nchunk = K / 8;
@@ -201,18 +196,18 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, flo
     const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
     const int ch = static_cast<int>((nchunk + 31) / 32);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 1) quant_warp_rows<1, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
-    else if (ch <= 2) quant_warp_rows<2, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
-    else if (ch <= 4) quant_warp_rows<4, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
-    else quant_warp_rows<8, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    if (ch <= 1) quant_warp_rows<1, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    else if (ch <= 2) quant_warp_rows<2, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    else if (ch <= 4) quant_warp_rows<4, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    else quant_warp_rows<8, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
   } else {
     const int64_t blocks = std::min<int64_t>(M, max_grid);
     const int ch = static_cast<int>((nchunk + 255) / 256);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 2) quant_cta_rows<2, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
-    else if (ch <= 4) quant_cta_rows<4, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
-    else if (ch <= 8) quant_cta_rows<8, F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
-    else quant_cta_rows_any<F16OUT><<<g, b, 0, stream>>>(x, M, K, q, scale);
+    if (ch <= 2) quant_cta_rows<2, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    else if (ch <= 4) quant_cta_rows<4, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    else if (ch <= 8) quant_cta_rows<8, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    else quant_cta_rows_any<OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
   }
   return cudaGetLastError();
 }
@@ -221,12 +216,12 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, flo
 
 cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                  cudaStream_t stream, int num_sms) {
-  return launch_quant_t<false>(x, M, K, q, scale, stream, num_sms);
+  return launch_quant_t<0>(x, M, K, q, nullptr, scale, stream, num_sms);
 }
 
-cudaError_t launch_dynamic_quant_f16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q_f16,
-                                     float* scale, cudaStream_t stream, int num_sms) {
-  return launch_quant_t<true>(x, M, K, q_f16, scale, stream, num_sms);
+cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
+                                      float* scale, cudaStream_t stream, int num_sms) {
+  return launch_quant_t<2>(x, M, K, q, q_f16, scale, stream, num_sms);
 }
 
 }  // namespace w8a8
