@@ -41,6 +41,7 @@ constexpr int TC_BM = 128;
 constexpr int TC_BN = 256;
 constexpr int TC_BK = 64;  // fp16 elements = 128 bytes = one swizzle row
 constexpr int TC_STAGES = 4;
+constexpr int TC_GROUP_N = 16;  // n-blocks per rasterisation group
 constexpr int TC_KB_PER_CHUNK = kChunkK / TC_BK;  // 16
 constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 2;
 constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 2;
@@ -187,9 +188,15 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int*
   const int local = t - tile_prefix[lo];
   ti.cnt = row_off[lo + 1] - row_off[lo];
   const int mblocks = (ti.cnt + TC_BM - 1) / TC_BM;
-  ti.mb = local % mblocks;
-  ti.nb = local / mblocks;
-  (void)NB;
+  // Rasterise in groups of up to TC_GROUP_N n-blocks: inside a group the
+  // n-block varies fastest, then the m-block, so the CTAs in flight share one
+  // activation block and the group's weight blocks stay resident in L2 while
+  // all m-blocks sweep past them.
+  const int g = local / (mblocks * TC_GROUP_N);
+  const int rem = local - g * mblocks * TC_GROUP_N;
+  const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
+  ti.mb = rem / gn;
+  ti.nb = g * TC_GROUP_N + rem % gn;
   ti.row0 = static_cast<int64_t>(row_off[lo]) + static_cast<int64_t>(ti.mb) * TC_BM;
   return ti;
 }
