@@ -479,7 +479,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
 
-  // ---- teardown: on abort, give in-flight copies and MMAs time to land first
+  // ---- teardown: on abort, give in-flight copies and MMAs time to land first.
+  // Lanes 1-31 of warps 0 and 1 skipped the single-lane role loops; reconverge
+  // every warp before the block-wide (aligned) barrier, so TMEM is not freed
+  // while epilogue warps still read it.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (s_abort) {
