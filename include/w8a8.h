@@ -32,8 +32,10 @@
  *     wait) are written to the status word at the start of the caller's
  *     workspace; read them with w8a8_read_device_status().
  *   - Workspaces must be zero-filled once before their first use; every call
- *     leaves its workspace zeroed again (except for the status word after an
- *     error, which w8a8_read_device_status() clears).
+ *     leaves the parts that must start at zero (arrival counters, split-K
+ *     sums) zeroed again, and the status word too unless an error was
+ *     recorded (w8a8_read_device_status() clears it).  One workspace serves
+ *     one stream at a time.
  *   - K (the reduction depth) must be a multiple of 16 and at most
  *     W8A8_MAX_K; M, N and group sizes are arbitrary (>= 0 / >= 1).
  *   - Integer results (INT8 payloads, INT32 accumulators) and FP32 scales are

@@ -1,0 +1,80 @@
+"""GPU parity of the decode engine (dense, M <= 64 tokens): int8 weights
+widened into tensor memory, K split over co-resident CTAs whose exact int32
+partials are summed through the workspace.  Bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_dynamic_quant_gb300 as W
+from w8a8_dynamic_quant_gb300 import synthetic as S
+
+from gpu_helpers import dev, dev_bf16, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def dec_region(ws, N):
+    """(partials, counters) of the decode engine: the last block of the workspace."""
+    nblk = (N + 127) // 128
+    part = (nblk * 16 * 64 * 128 * 4 + 255) // 256 * 256
+    cnt = (nblk * 8 + 255) // 256 * 256
+    tail = ws[ws.numel() - part - cnt:]
+    return tail[:part], tail[part:part + nblk * 8]
+
+
+def run(q, xs, w, wsc, bias=None):
+    M, K = q.shape
+    N = w.shape[0]
+    wp = W.w8a8_prepack_weight(dev(w))
+    ws = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
+    y = W.w8a8_quant_matmul(dev(q), dev(xs), wp, dev(wsc), N, None if bias is None else dev_bf16(bias), ws=ws)
+    ws2 = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
+    acc = W.w8a8_int8_matmul_acc(dev(q), wp, N, ws=ws2)
+    torch.cuda.synchronize()
+    part, cnt = dec_region(ws, N)
+    assert bool((part != 0).any()), "decode engine did not run"
+    assert int(cnt.count_nonzero()) == 0, "arrival counters not reset"
+    assert W.read_device_status(ws) == 0
+    return host_bits(y), acc.cpu().numpy()
+
+
+@pytest.mark.parametrize("M", [1, 7, 33, 64])
+@pytest.mark.parametrize("N,K", [(128, 16), (200, 80), (2048, 1024), (384, 4096), (256, 7168), (130, 8192),
+                                 (2048, 7168)])
+def test_dec_shapes_exact(M, N, K):
+    d = S.make_dense(M, K, N, n_outlier=min(5, K), outlier_mult=25.0, bias=(N % 2 == 0), seed=M * 7 + N + K)
+    q, xs = oracle.dynamic_quant(d.x)
+    y, acc = run(q, xs, d.w, d.w_scale, d.bias)
+    assert np.array_equal(acc, oracle.int8_gemm_acc(q, d.w))
+    assert np.array_equal(y, oracle.quant_matmul(q, xs, d.w, d.w_scale, d.bias))
+
+
+def test_dec_partial_sums_at_the_fp32_integer_limit():
+    """A CTA covers at most 1024 of K: with every product 128*128 its fp32
+    partial is exactly 2^24, the largest value the chunking allows."""
+    M, N, K = 64, 256, 8192
+    q = np.full((M, K), -128, np.int8)
+    q[1] = 127
+    q[2, ::2] = -127
+    q[3:] = np.random.default_rng(3).integers(-128, 128, (M - 3, K), dtype=np.int8)
+    w = np.full((N, K), -128, np.int8)
+    w[1] = 127
+    w[2, : K // 2] = 1
+    w[3:] = np.random.default_rng(4).integers(-128, 128, (N - 3, K), dtype=np.int8)
+    _, acc = run(q, np.ones(M, np.float32), w, np.ones(N, np.float32))
+    ref = q.astype(np.int64) @ w.astype(np.int64).T
+    assert ref[0, 0] == K * 16384
+    assert np.array_equal(acc.astype(np.int64), ref)
+
+
+def test_dec_repeated_calls_reuse_the_workspace():
+    d = S.dense_config(2)
+    q, xs = oracle.dynamic_quant(d.x)
+    wp = W.w8a8_prepack_weight(dev(d.w))
+    ws = W.workspace(W.quant_matmul_workspace_bytes(d.M, d.N, d.K))
+    ref = oracle.quant_matmul(q, xs, d.w, d.w_scale, None)
+    for _ in range(5):
+        y = W.w8a8_quant_matmul(dev(q), dev(xs), wp, dev(d.w_scale), d.N, ws=ws)
+        assert np.array_equal(host_bits(y), ref)
+    assert W.read_device_status(ws) == 0

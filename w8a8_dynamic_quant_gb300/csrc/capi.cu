@@ -107,7 +107,7 @@ w8a8_status check_k(int64_t K) {
 // Workspace of one contraction: status word, split-K partials + counters, and
 // (for shapes the tcgen05 engine takes) the activations as fp16.
 struct GemmWs {
-  size_t status = 0, acc = 0, count = 0, a16 = 0, total = 0;
+  size_t status = 0, acc = 0, count = 0, a16 = 0, dec = 0, total = 0;
   int64_t count_len = 0;
 };
 GemmWs gemm_ws_layout(int64_t E, int64_t R, int64_t N, int64_t K, bool with_a16 = true) {
@@ -119,7 +119,9 @@ GemmWs gemm_ws_layout(int64_t E, int64_t R, int64_t N, int64_t K, bool with_a16 
   const int64_t nb = (N + 127) / 128;
   L.count_len = ((R + 7) / 8 + (E > 1 ? E : 0)) * nb;
   L.a16 = L.count + align_up(static_cast<uint64_t>(L.count_len) * 4, 256);
-  L.total = L.a16 + ((with_a16 && tc_shape(E, R)) ? align_up(static_cast<uint64_t>(R) * K * 2, 256) : 0);
+  L.dec = L.a16 + ((with_a16 && tc_shape(E, R)) ? align_up(static_cast<uint64_t>(R) * K * 2, 256) : 0);
+  // decode engine (dense, at most 64 rows): split-K partial tiles + counters
+  L.total = L.dec + ((with_a16 && E <= 1 && R <= 64) ? dec_ws_bytes(N) : 0);
   return L;
 }
 
@@ -169,6 +171,10 @@ w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream,
     uint16_t* a16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.a16);
     if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
     return cuda_status(launch_tc_gemm(a, a16, b16, sms, stream));
+  }
+  if (a.group_list == nullptr && a.mode != EPI_SWIGLU && L.dec < L.total) {
+    const int ks = dec_plan_ksplit(a.R, a.N, a.K, sms);  // dense decode: int8 weights widened in TMEM
+    if (ks > 0) return cuda_status(launch_dec_gemm(a, ks, static_cast<uint8_t*>(ws) + L.dec, stream));
   }
   const GemmPlan p = plan_reg_gemm(a, sms);
   return cuda_status(launch_reg_gemm(a, p, stream));

@@ -67,4 +67,11 @@ int64_t tc_upper_tiles(int64_t E, int64_t R, int64_t N, bool grouped);
 cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream);
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
+// tcgen05 decode engine (dense, M <= 64): int8 weights widened into TMEM, K
+// split over co-resident CTAs reduced through the workspace.
+// dec_plan_ksplit returns 0 when the shape does not suit it.
+size_t dec_ws_bytes(int64_t N);
+int dec_plan_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_dec_gemm(const GemmArgs& a, int ksplit, void* dec_ws, cudaStream_t stream);
+
 }  // namespace w8a8
