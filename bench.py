@@ -63,8 +63,9 @@ def weight_read_bound_ms(active_params: float, bytes_per_param: float, n_gpus: i
 # only while these files are unchanged)
 KERNEL_SOURCES = {
     "dynamic_quant": ["quant.cu", "common.cuh", "kernels.cuh"],
-    "quant_matmul": ["gemm_reg.cu", "common.cuh", "kernels.cuh"],
-    "moe_layer": ["gemm_reg.cu", "quant.cu", "capi.cu", "common.cuh", "kernels.cuh"],
+    "quant_matmul": ["gemm_reg.cu", "gemm_dec.cu", "gemm_tc.cu", "tc_common.cuh", "capi.cu", "common.cuh",
+                     "kernels.cuh"],
+    "moe_layer": ["gemm_reg.cu", "gemm_tc.cu", "tc_common.cuh", "quant.cu", "capi.cu", "common.cuh", "kernels.cuh"],
 }
 
 

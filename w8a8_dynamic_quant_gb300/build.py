@@ -19,8 +19,11 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw8a8.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Warnings are errors: a shadowed or uninitialised index in device code is a
+# wild address on the GPU, so the build refuses to produce such a library.
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
+              "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-Wall", "-Werror", "all-warnings",
+              "-I", os.path.join(ROOT, "include")]
 
 
 def nvcc() -> str:
