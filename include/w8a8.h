@@ -217,6 +217,21 @@ W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const float* x_s
  * passed to the calls above. */
 W8A8_API w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream);
 
+/* Engines a contraction can run on. */
+enum {
+  W8A8_ENGINE_NONE = 0,    /* no contraction launched yet on this thread (or M == 0) */
+  W8A8_ENGINE_WARP = 1,    /* warp-level mma.sync engine (any shape) */
+  W8A8_ENGINE_DECODE = 2,  /* tcgen05 decode engine: dense, M <= 64, int8 weights widened in tensor memory */
+  W8A8_ENGINE_TC = 3       /* tcgen05 engine for large M: both operands as fp16 (weights packed with W8A8_PACK_F16) */
+};
+
+/* The engine the last contraction launched by the calling host thread ran on
+ * (w8a8_quant_matmul, w8a8_int8_matmul_acc, w8a8_grouped_matmul,
+ * w8a8_grouped_matmul_acc, and the W2 contraction of
+ * moe_w13_swiglu_requant_w2).  A host-side record: no device access, never
+ * fails. */
+W8A8_API int w8a8_last_engine(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,6 +24,7 @@ __all__ = [
     "w8a8_int8_matmul_acc", "grouped_matmul_workspace_bytes", "w8a8_grouped_matmul",
     "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
+    "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
 ]
 
 
@@ -237,3 +238,11 @@ def read_device_status(ws: torch.Tensor) -> int:
     """Synchronise the current stream and return (and clear) the device status word of `ws`."""
     with torch.cuda.device(ws.device):
         return int(_capi.lib().w8a8_read_device_status(ws.data_ptr(), _stream(ws.device)))
+
+
+ENGINE_NONE, ENGINE_WARP, ENGINE_DECODE, ENGINE_TC = 0, 1, 2, 3
+
+
+def last_engine() -> int:
+    """Engine the calling thread's last contraction ran on (ENGINE_WARP / ENGINE_DECODE / ENGINE_TC)."""
+    return int(_capi.lib().w8a8_last_engine())

@@ -36,6 +36,7 @@ SIGNATURES = {
                                          _vp, _vp]),
     "w8a8_quant_matmul_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp]),
     "w8a8_read_device_status": (_int, [_vp, _vp]),
+    "w8a8_last_engine": (_int, []),
 }
 
 STATUS = {0: "W8A8_OK", 1: "W8A8_ERR_NULL", 2: "W8A8_ERR_SHAPE", 3: "W8A8_ERR_ALIGN",

@@ -98,6 +98,18 @@ const void* pack_f16(const void* ptr, int64_t E, int64_t N, int64_t K, uint32_t 
   return nullptr;
 }
 
+// True when this process packed `ptr` itself with these sizes and gate/up order.
+bool pack_recorded(const void* ptr, int64_t E, int64_t N, int64_t K, uint32_t need_flags) {
+  std::lock_guard<std::mutex> lk(g_pack_mu);
+  for (int i = 0; i < g_npacks; ++i) {
+    const PackRecord& r = g_packs[i];
+    if (r.ptr == ptr && r.E == E && r.N == N && r.K == K &&
+        (r.flags & W8A8_PACK_GATE_UP) == (need_flags & W8A8_PACK_GATE_UP))
+      return true;
+  }
+  return false;
+}
+
 w8a8_status check_k(int64_t K) {
   if (K <= 0 || K > W8A8_MAX_K) return W8A8_ERR_SHAPE;
   if (K % 16 != 0) return W8A8_ERR_ALIGN;
@@ -163,6 +175,8 @@ MoeWs moe_layout(int64_t R, int64_t H, int64_t I, int64_t E) {
 // One contraction on the engine its shape calls for: tcgen05 (activations
 // widened to fp16 in the workspace) when the shape is large and the weight
 // carries its fp16 copy, else the warp-level engine.
+thread_local int t_last_engine = W8A8_ENGINE_NONE;
+
 w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream, int sms) {
   bind_ws(a, ws, L);
   a.status = static_cast<DeviceStatus*>(ws);
@@ -170,12 +184,18 @@ w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream,
   if (b16 != nullptr) {
     uint16_t* a16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.a16);
     if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
+    t_last_engine = W8A8_ENGINE_TC;
     return cuda_status(launch_tc_gemm(a, a16, b16, sms, stream));
   }
   if (a.group_list == nullptr && a.mode != EPI_SWIGLU && L.dec < L.total) {
     const int ks = dec_plan_ksplit(a.R, a.N, a.K, sms);  // dense decode: int8 weights widened in TMEM
-    if (ks > 0) return cuda_status(launch_dec_gemm(a, ks, static_cast<uint8_t*>(ws) + L.dec, stream));
+    if (ks > 0) {
+      a.pack_known = pack_recorded(a.packed, a.E, a.N, a.K, a.pack_flags) ? 1 : 0;
+      t_last_engine = W8A8_ENGINE_DECODE;
+      return cuda_status(launch_dec_gemm(a, ks, static_cast<uint8_t*>(ws) + L.dec, stream));
+    }
   }
+  t_last_engine = W8A8_ENGINE_WARP;
   const GemmPlan p = plan_reg_gemm(a, sms);
   return cuda_status(launch_reg_gemm(a, p, stream));
 }
@@ -434,6 +454,7 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   a2.status = static_cast<DeviceStatus*>(ws);
   const cudaError_t e2 = tc ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
                             : launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st);
+  t_last_engine = tc ? W8A8_ENGINE_TC : W8A8_ENGINE_WARP;
   return e2 == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
 }
 
@@ -448,5 +469,7 @@ w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream) {
   }
   return static_cast<w8a8_status>(s.code);
 }
+
+int w8a8_last_engine(void) { return t_last_engine; }
 
 }  // extern "C"

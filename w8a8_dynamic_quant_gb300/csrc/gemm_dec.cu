@@ -6,30 +6,36 @@
 // BF16) and §四 (decode, small M, gets its own tiling).
 //
 // The weights stay INT8 in HBM (one byte per element, row-major, K
-// contiguous).  Eight converter warps stream them with 16-byte loads straight
-// into registers -- lane r of a warp reads its own row r, 64 contiguous bytes
-// (a full DRAM burst) per half stage -- keep three 128-deep K stages of loads
-// in flight, widen each row to integer-valued FP16 and store it into tensor
-// memory, where tcgen05.mma reads its A operand.
-// No copy engine and no shared-memory staging touch the large operand (the
-// tensor-copy engine's per-row request rate caps a weight stream far below the
-// HBM share of one SM).  The 64-token activation slice of each stage is widened
-// into two 128-byte-swizzled K-major FP16 tiles in shared memory (the B
-// operand).  The MMA is M = 128 weight rows x N = 64 tokens x K = 16 into an
-// FP32 TMEM accumulator; each CTA covers at most 1024 of K, so the accumulator
-// holds an exact integer (|partial| <= 1024 * 2^14 = 2^24).
+// contiguous).  A CTA owns 128 weight rows and a K slice of at most 7 stages
+// of 128.  With one CTA per SM, an SM streams at the HBM rate only with about
+// 100 KB of reads in flight, so one thread issues tensor-copy (TMA) loads of
+// the CTA's WHOLE slice at once: per stage a 128-row x 128-byte weight tile
+// and the 64-token x 128-byte INT8 activation tile of the same K range, both
+// 128-byte swizzled, each stage on its own mbarrier.  When the host made the
+// packed buffer itself (it keeps a record of the packs it wrote), the loads
+// are issued before the header check instead of after it.
+// Eight converter warps take the stages in order: lane r reads weight row r
+// (conflict-free thanks to the swizzle), widens it to integer-valued FP16 and
+// stores it into tensor memory, where tcgen05.mma reads its A operand; the
+// activation tile is widened into two 128-byte-swizzled K-major FP16 tiles in
+// shared memory (the B operand).  The MMA is M = 128 weight rows x N = 64
+// tokens x K = 16 into an FP32 TMEM accumulator; the CTA's K slice is at most
+// 896, so the accumulator holds an exact integer (|partial| <= 896 * 127^2
+// < 2^24).
 //
-// K is split over `ksplit` CTAs per 128-row block.  The launch is cooperative
-// (every CTA resident at once), so the split-K reduction needs no second
-// kernel: each CTA stores its exact int32 partial tile token-major into the
-// workspace with coalesced stores, bumps an arrival counter for its row block
-// and waits (bounded) until all `ksplit` partials are in; then every CTA sums
-// its share of the rows over the partials with 16-byte loads issued together,
-// applies the dequant epilogue and writes BF16 (or the INT32 sums).  A second
-// counter tells the last reader to zero both counters.
+// Split-K reduction in two steps, neither of which waits on another CTA's
+// progress beyond the cluster barrier: the K splits of a row block form
+// clusters of up to four CTAs; after a cluster barrier each CTA sums, for its
+// quarter of the tokens, the cluster's partial tiles straight out of the other
+// CTAs' shared memory (distributed shared memory).  With more than four
+// splits, each CTA then stores its quarter in its own workspace slot and bumps
+// the arrival counter of that quarter (release); the CTA that arrives last
+// adds the other clusters' slots.  The CTA holding the complete sums applies
+// the dequant epilogue and writes BF16 (or the INT32 sums) and resets the
+// counter.  Integer addition is exact in any order.
 //
-// Warps: 0 TMEM owner + MMA issuer; 1-8 converters, then epilogue (warp w
-// owns TMEM lanes 32*(w%4).. and K half / token half (w-1)/4).  All waits are
+// Warps: 0 TMEM owner + TMA producer + MMA issuer; 1-8 converters (warp w owns
+// TMEM lanes 32*(w%4).. and K part / token part (w-1)/4).  All waits are
 // bounded.
 #include <mutex>
 
@@ -45,27 +51,66 @@ using namespace tc;
 constexpr int DC_ROWS = 128;  // weight rows per CTA (MMA M)
 constexpr int DC_TOK = 64;    // token columns (MMA N)
 constexpr int DC_BK = 128;    // K per stage
-constexpr int DC_SF = 3;      // fp16 / TMEM stages
-constexpr int DC_PF = 3;      // stages of loads in flight per converter thread
+constexpr int DC_SF = 3;      // fp16 B tiles in shared memory / A stages in TMEM
 constexpr uint32_t DC_B_SUB = DC_TOK * 128;    // one 64-K fp16 sub-tile (8 KB)
 constexpr uint32_t DC_B_BYTES = 2 * DC_B_SUB;  // 128 K of fp16 activations
 constexpr uint32_t DC_RING_BYTES = DC_SF * DC_B_BYTES;
+#ifndef DC_CONV_WARPS_OVERRIDE
 constexpr int DC_CONV_WARPS = 8;
+#else
+constexpr int DC_CONV_WARPS = DC_CONV_WARPS_OVERRIDE;
+#endif
 constexpr int DC_THREADS = 32 * (1 + DC_CONV_WARPS);
+constexpr int DC_NPART = DC_CONV_WARPS / 4;          // converter warps per TMEM lane quadrant
+constexpr int DC_WCH = 8 / DC_NPART;                 // 16-byte weight chunks per lane per stage
+constexpr int DC_XCH = 512 / (32 * DC_CONV_WARPS);   // 16-byte activation chunks per thread per stage
+constexpr int DC_TPW = DC_TOK / DC_NPART;            // accumulator columns (tokens) drained per warp
+static_assert(DC_CONV_WARPS == 8 || DC_CONV_WARPS == 16, "8 or 16 converter warps");
 constexpr uint32_t DC_TMEM_COLS = 256;
 constexpr uint32_t DC_A_COLS = DC_BK / 2;         // 64 columns of fp16 pairs per A stage
 constexpr uint32_t DC_D_COL = DC_SF * DC_A_COLS;  // accumulator columns [192, 256)
-constexpr int DC_MAX_KB = kChunkK / DC_BK;        // 8 stages = 1024 of K per CTA
+constexpr int DC_MAX_KB = 7;                      // stages per CTA: 896 of K
+constexpr uint32_t DC_W_STAGE = DC_ROWS * DC_BK;  // int8 weight tile (16 KB)
+constexpr uint32_t DC_X_STAGE = DC_TOK * DC_BK;   // int8 activation tile (8 KB)
+constexpr uint32_t DC_TILE_I32 = DC_TOK * DC_ROWS * 4;  // int32 partial tile (32 KB)
 constexpr int DC_MAX_KSPLIT = 16;
+constexpr int DC_CLUSTER = 4;                            // CTAs per cluster (consecutive K splits)
+constexpr int DC_SLOT_I32 = DC_TOK / DC_CLUSTER * DC_ROWS;  // int32 per workspace slot
 constexpr uint32_t kIdescDec = (1u << 4) | (uint32_t(DC_TOK >> 3) << 17) | (uint32_t(DC_ROWS >> 4) << 24);
-static_assert(DC_B_BYTES % 1024 == 0, "1024-byte aligned stages");
+static_assert(DC_B_BYTES % 1024 == 0 && DC_W_STAGE % 1024 == 0 && DC_X_STAGE % 1024 == 0, "1024-byte aligned tiles");
 static_assert(DC_D_COL + DC_TOK <= DC_TMEM_COLS, "tensor memory budget");
+static_assert(DC_MAX_KB * DC_BK * 127 * 127 < (1 << 24), "exact fp32 accumulator");
+static_assert(DC_MAX_KB * DC_W_STAGE >= DC_TILE_I32, "the partial tile reuses the weight tiles");
 
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
+// 32 lanes x N consecutive 32-bit TMEM columns (N = 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 32) {
+    tmem_st32(taddr, v);
+  } else {
+    static_assert(N == 16, "16 or 32 columns");
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+  }
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
+  if constexpr (N == 32) {
+    tmem_ld32(taddr, v);
+  } else {
+    static_assert(N == 16, "16 or 32 columns");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+  }
 }
 
 // 16 int8 (one 16-byte chunk) -> 8 words of fp16 pairs.
@@ -76,39 +121,63 @@ __device__ __forceinline__ void widen16(const uint4& x, uint32_t* h) {
   s8x4_to_f16x4(x.w, h[6], h[7]);
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// TMA loads of a CTA's whole K slice (stages [kb0, kb0 + my) of row block rb), one mbarrier per stage.
+__device__ __forceinline__ void issue_slice(const CUtensorMap* wmap, const CUtensorMap* xmap, uint64_t* bar_full,
+                                            uint8_t* wtiles, uint8_t* xtiles, int kb0, int my, int rb) {
+  for (int s = 0; s < my; ++s) {
+    const uint32_t fb = smem_u32(&bar_full[s]);
+    mbar_expect_tx(fb, DC_W_STAGE + DC_X_STAGE);
+    tma_load_2d(smem_u32(wtiles + s * DC_W_STAGE), wmap, (kb0 + s) * DC_BK, rb * DC_ROWS, fb);
+    tma_load_2d(smem_u32(xtiles + s * DC_X_STAGE), xmap, (kb0 + s) * DC_BK, 0, fb);
+  }
+}
+
+// Workspace of the decode engine: per row block and K split a slot for the
+// cluster-summed int32 piece [tokens of the CTA][DC_ROWS], and per row block
+// four arrival counters (one per cluster rank), zero between calls.
+struct DecWs {
+  int32_t* slots;
+  uint32_t* cnt;
+};
+
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ int4 ld_dsmem_v4(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
   return v;
 }
 
-// Workspace of the decode engine: partial tiles [nblk][ksplit][DC_TOK][DC_ROWS]
-// int32 (token-major), then two arrival counters per row block.
-struct DecWs {
-  int32_t* part;
-  uint32_t* cnt_in;
-  uint32_t* cnt_out;
-};
-
 template <int MODE>
 __global__ void __launch_bounds__(DC_THREADS, 1)
-dec_gemm_kernel(const GemmArgs a, const DecWs ws) {
+dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtensorMap wmap,
+                const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[DC_MAX_KB];
   __shared__ __align__(8) uint64_t bar_ready[DC_SF];
   __shared__ __align__(8) uint64_t bar_emptyf[DC_SF];
   __shared__ __align__(8) uint64_t bar_accf;
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
-  __shared__ int s_bad;
+  __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int ct = tid - 32;      // converter thread index (warps 1..DC_CONV_WARPS)
   const int rank = blockIdx.x;  // split of K
   const int ksplit = gridDim.x;
   const int rb = blockIdx.y;    // 128-row weight block
   const int64_t M = a.R, N = a.N, K = a.K;
-  const int64_t KC = K / 16;
   const int nkb = static_cast<int>((K + DC_BK - 1) / DC_BK);
   const int kb0 = static_cast<int>(static_cast<int64_t>(nkb) * rank / ksplit);
   const int kb1 = static_cast<int>(static_cast<int64_t>(nkb) * (rank + 1) / ksplit);
@@ -116,22 +185,28 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws) {
 
   uint8_t* ringb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t ringb_base = smem_u32(ringb);
-  int32_t* my_part = ws.part + (static_cast<int64_t>(rb) * ksplit + rank) * (DC_TOK * DC_ROWS);
+  uint8_t* wtiles = ringb + DC_RING_BYTES;           // int8 weights [DC_MAX_KB][DC_ROWS][DC_BK], swizzled
+  uint8_t* xtiles = wtiles + DC_MAX_KB * DC_W_STAGE;  // int8 activations [DC_MAX_KB][DC_TOK][DC_BK], swizzled
+  int32_t* ptile = reinterpret_cast<int32_t*>(wtiles);  // int32 partial [DC_TOK][DC_ROWS], after the main loop
 
   if (tid == 0) {
+    tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&xmap);
     s_abort = 0;
-    s_bad = 0;
-    const PackedHeader* h = static_cast<const PackedHeader*>(a.packed);
-    if (h->magic != kPackMagic || h->version != kPackVersion || h->E != 1 || h->N != N || h->K != K ||
-        (h->flags & W8A8_PACK_GATE_UP) != 0u)
-      s_bad = W8A8_ERR_PACKED;
+    s_last = 0;
+    for (int s = 0; s < DC_MAX_KB; ++s) mbar_init(smem_u32(&bar_full[s]), 1);
     for (int f = 0; f < DC_SF; ++f) {
       mbar_init(smem_u32(&bar_ready[f]), DC_CONV_WARPS);
       mbar_init(smem_u32(&bar_emptyf[f]), 1);
     }
     mbar_init(smem_u32(&bar_accf), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (a.pack_known) issue_slice(&wmap, &xmap, bar_full, wtiles, xtiles, kb0, my, rb);
   }
+  const PackedHeader* hdr = static_cast<const PackedHeader*>(a.packed);
+  const bool run = hdr->magic == kPackMagic && hdr->version == kPackVersion && hdr->E == 1 && hdr->N == N &&
+                   hdr->K == K && (hdr->flags & W8A8_PACK_GATE_UP) == 0u;
+  if (tid == 0 && run && !a.pack_known) issue_slice(&wmap, &xmap, bar_full, wtiles, xtiles, kb0, my, rb);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
                  "r"(DC_TMEM_COLS)
@@ -142,8 +217,7 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
-  const bool run = (s_bad == 0);
-  if (!run && tid == 0 && rank == 0 && rb == 0) set_status(a.status, static_cast<uint32_t>(s_bad), 0u);
+  if (!run && tid == 0 && rank == 0 && rb == 0) set_status(a.status, W8A8_ERR_PACKED, 0u);
 
   if (run && warp == 0) {
     // ------------------------------------------------------------- MMA issuer
@@ -165,84 +239,54 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws) {
       tc_commit(smem_u32(&bar_accf));
     }
   } else if (run) {
-    // ------------------------------------------------ converters, then epilogue
+    // ------------------------------------------------ converters, then the partial tile
     const int q = warp & 3;           // TMEM lane quadrant
-    const int half = (warp - 1) >> 2;  // K half of each stage (chunks 4*half..4*half+3)
-    const int row = 32 * q + lane;     // weight row inside the block == TMEM lane
-    const int ct = tid - 32;           // 0..255
-    // this lane's weight row (row-major int8 payload, K contiguous); rows past N read as zero
-    const int64_t grow = static_cast<int64_t>(rb) * DC_ROWS + row;
-    const bool row_ok = grow < N;
-    const uint8_t* wrow = reinterpret_cast<const uint8_t*>(a.packed) +
-                          static_cast<const PackedHeader*>(a.packed)->i8_offset + (row_ok ? grow : 0) * K;
-    const uint8_t* xq = reinterpret_cast<const uint8_t*>(a.q);
-    uint4 wr[DC_PF][4];
-    uint4 xr[DC_PF][2];
-    // loads of stage i into register buffer B (B is a compile-time constant at every use)
-#define DC_LOAD(B, I)                                                                                  \
-    do {                                                                                               \
-      const int ld_i = (I);                                                                              \
-      if (ld_i < my) {                                                                                   \
-        const int64_t kc0 = static_cast<int64_t>(kb0 + ld_i) * (DC_BK / 16) + 4 * half;                 \
-        _Pragma("unroll") for (int c = 0; c < 4; ++c) {                                                \
-          wr[B][c] = (row_ok && kc0 + c < KC) ? ldg_nc(wrow + (kc0 + c) * 16) : make_uint4(0, 0, 0, 0);     \
-        }                                                                                              \
-        _Pragma("unroll") for (int j = 0; j < 2; ++j) {                                                \
-          const int p = ct + 256 * j;                                                                  \
-          const int t = p >> 3, c = p & 7;                                                             \
-          const int64_t k = static_cast<int64_t>(kb0 + ld_i) * DC_BK + 16 * c;                           \
-          xr[B][j] = (t < M && k < K) ? ldg_nc(xq + t * K + k) : make_uint4(0, 0, 0, 0);               \
-        }                                                                                              \
-      }                                                                                                \
-    } while (0)
-    // widen stage i from register buffer B into TMEM A / smem B stage i % DC_SF, refill B with stage i + DC_PF
-#define DC_STEP(B, I)                                                                                  \
-    if ((I) < my && ok) {                                                                              \
-      const int st_i = (I);                                                                              \
-      const int f = st_i % DC_SF;                                                                        \
-      const uint32_t phf = static_cast<uint32_t>(st_i / DC_SF) & 1u;                                    \
-      int got = 0;                                                                                     \
-      if (lane == 0) got = mbar_wait(smem_u32(&bar_emptyf[f]), phf ^ 1u, &s_abort, a.status, 15u) ? 1 : 0; \
-      got = __shfl_sync(0xffffffffu, got, 0);                                                          \
-      if (!got) {                                                                                      \
-        ok = false;                                                                                    \
-      } else {                                                                                         \
-        uint32_t v[32];                                                                                \
-        _Pragma("unroll") for (int c = 0; c < 4; ++c) widen16(wr[B][c], &v[8 * c]);                   \
-        uint8_t* bt = ringb + f * DC_B_BYTES;                                                          \
-        _Pragma("unroll") for (int j = 0; j < 2; ++j) {                                                \
-          const int p = ct + 256 * j;                                                                  \
-          const int t = p >> 3, c = p & 7;                                                             \
-          uint32_t hh[8];                                                                              \
-          widen16(xr[B][j], hh);                                                                       \
-          uint8_t* brow = bt + (c >> 2) * DC_B_SUB + t * 128;                                          \
-          const int cc = (c & 3) * 2;                                                                  \
-          *reinterpret_cast<uint4*>(brow + ((cc ^ (t & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]); \
-          *reinterpret_cast<uint4*>(brow + (((cc + 1) ^ (t & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]); \
-        }                                                                                              \
-        DC_LOAD(B, st_i + DC_PF);                                                                        \
-        tmem_st32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + f * DC_A_COLS + 32u * half, v);   \
-        tmem_wait_st();                                                                                \
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");                                   \
-        tc_fence_before();                                                                             \
-        __syncwarp();                                                                                  \
-        if (lane == 0) mbar_arrive(smem_u32(&bar_ready[f]));                                          \
-      }                                                                                                \
-    }
-    static_assert(DC_PF == 3, "the pipeline below is written for three register buffers");
+    const int part = (warp - 1) >> 2;  // K part of each stage (chunks DC_WCH*part..) / token part
+    const int row = 32 * q + lane;    // weight row inside the block == TMEM lane
     bool ok = true;
-    DC_LOAD(0, 0);
-    DC_LOAD(1, 1);
-    DC_LOAD(2, 2);
-    for (int i = 0; i < my && ok; i += DC_PF) {
-      DC_STEP(0, i)
-      DC_STEP(1, i + 1)
-      DC_STEP(2, i + 2)
+    for (int i = 0; i < my && ok; ++i) {
+      const int f = i % DC_SF;
+      const uint32_t phf = static_cast<uint32_t>(i / DC_SF) & 1u;
+      int got = 0;
+      if (lane == 0) got = mbar_wait(smem_u32(&bar_emptyf[f]), phf ^ 1u, &s_abort, a.status, 15u) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      // every lane observes the completed load of stage i itself
+      if (got) got = mbar_wait(smem_u32(&bar_full[i]), 0u, &s_abort, a.status, 13u) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      // weights first: their tensor-memory store runs while the activations are widened
+      uint32_t v[8 * DC_WCH];
+      const uint8_t* wst = wtiles + i * DC_W_STAGE + row * DC_BK;
+#pragma unroll
+      for (int c = 0; c < DC_WCH; ++c)
+        widen16(*reinterpret_cast<const uint4*>(wst + (((DC_WCH * part + c) ^ (row & 7)) << 4)), &v[8 * c]);
+      tmem_st_cols<8 * DC_WCH>(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + f * DC_A_COLS +
+                                   static_cast<uint32_t>(8 * DC_WCH * part),
+                               v);
+      uint8_t* bt = ringb + f * DC_B_BYTES;
+      const uint8_t* xst = xtiles + i * DC_X_STAGE;
+#pragma unroll
+      for (int jj = 0; jj < DC_XCH; ++jj) {
+        const int p = ct + 32 * DC_CONV_WARPS * jj;
+        const int t = p >> 3, c = p & 7;
+        uint32_t hh[8];
+        widen16(*reinterpret_cast<const uint4*>(xst + t * DC_BK + ((c ^ (t & 7)) << 4)), hh);
+        uint8_t* brow = bt + (c >> 2) * DC_B_SUB + t * 128;
+        const int cc = (c & 3) * 2;
+        *reinterpret_cast<uint4*>(brow + ((cc ^ (t & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        *reinterpret_cast<uint4*>(brow + (((cc + 1) ^ (t & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+      }
+      tmem_wait_st();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_ready[f]));
     }
-#undef DC_STEP
-#undef DC_LOAD
-    // exact partial -> workspace, token-major (lanes store consecutive rows);
-    // this warp drains tokens [32*half, 32*half + 32)
+    // exact partial -> shared memory, token-major; this warp drains tokens
+    // [DC_TPW*part, DC_TPW*(part+1)).  Once the last MMA has completed every converter warp is past its
+    // last stage, so the weight tiles are free to hold the partial.
     int got = 1;
     if (my > 0) {
       if (lane == 0) got = mbar_wait(smem_u32(&bar_accf), 0u, &s_abort, a.status, 14u) ? 1 : 0;
@@ -250,84 +294,117 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws) {
     }
     if (my > 0 && got && ok) {
       tc_fence_after();
-      uint32_t d[32];
-      tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + DC_D_COL + 32u * half, d);
+      uint32_t d[DC_TPW];
+      tmem_ld_cols<DC_TPW>(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + DC_D_COL +
+                               static_cast<uint32_t>(DC_TPW * part),
+                           d);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 32; ++c) my_part[(32 * half + c) * DC_ROWS + row] = __float2int_rn(__uint_as_float(d[c]));
+      for (int c = 0; c < DC_TPW; ++c)
+        ptile[(DC_TPW * part + c) * DC_ROWS + row] = __float2int_rn(__uint_as_float(d[c]));
     } else {
 #pragma unroll 8
-      for (int c = 0; c < 32; ++c) my_part[(32 * half + c) * DC_ROWS + row] = 0;
+      for (int c = 0; c < DC_TPW; ++c) ptile[(DC_TPW * part + c) * DC_ROWS + row] = 0;
     }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
   }
   __syncwarp();
-  __threadfence();
   __syncthreads();
 
-  // ---- all partials of this row block in: bounded wait on the arrival counter
-  __shared__ int s_ready;
-  if (tid == 0) {
-    atomicAdd(&ws.cnt_in[rb], 1u);
-    int ok = 1;
-    if (ld_acquire_u32(&ws.cnt_in[rb]) < static_cast<uint32_t>(ksplit)) {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_u32(&ws.cnt_in[rb]) < static_cast<uint32_t>(ksplit)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          set_status(a.status, W8A8_ERR_DEVICE_TIMEOUT, 16u);
-          ok = 0;
-          break;
+  // ---- split-K, step 1: the CTAs of a cluster (consecutive K splits of the row block) sum their partial
+  // tiles through distributed shared memory; CTA cr of the cluster takes tokens [cr*tq, (cr+1)*tq)
+  uint32_t csize, cr;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(cr));
+  const int tq = DC_TOK / static_cast<int>(csize);
+  const int ntask = tq * (DC_ROWS / 4);  // (token, 4 rows) pieces of this CTA
+  constexpr int kPer = (DC_TOK * DC_ROWS / 4 + DC_THREADS - 1) / DC_THREADS;
+  cluster_sync();  // every partial tile of the cluster is in place
+  int4 sums[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    sums[u] = make_int4(0, 0, 0, 0);
+    const int task = tid + DC_THREADS * u;
+    if (task >= ntask) continue;
+    const uint32_t off = static_cast<uint32_t>(((static_cast<int>(cr) * tq + (task >> 5)) * DC_ROWS + (task & 31) * 4) * 4);
+    for (uint32_t c = 0; c < csize; ++c) {
+      const int4 v = ld_dsmem_v4(mapa_shared(smem_u32(ptile), c) + off);
+      sums[u].x += v.x;
+      sums[u].y += v.y;
+      sums[u].z += v.z;
+      sums[u].w += v.w;
+    }
+  }
+  cluster_sync();  // no CTA reuses or releases its tile while the others still read it
+
+  // ---- step 2: the clusters of the row block meet through the workspace; each CTA stores its sums in its
+  // own slot and arrives (release); the last to arrive for these tokens adds the others' slots
+  const int ncl = ksplit / static_cast<int>(csize);
+  const int cg = rank / static_cast<int>(csize);
+  if (ncl > 1) {
+    int4* my_slot = reinterpret_cast<int4*>(ws.slots) + (static_cast<int64_t>(rb) * ksplit + rank) * (DC_SLOT_I32 / 4);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int task = tid + DC_THREADS * u;
+      if (task < ntask) __stcg(my_slot + task, sums[u]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      const uint32_t prev = atomicAdd(&ws.cnt[rb * 4 + cr], 1u);
+      if (prev == static_cast<uint32_t>(ncl - 1)) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        s_last = 1;
+        ws.cnt[rb * 4 + cr] = 0u;  // for the next call
+      }
+    }
+    __syncthreads();
+    if (s_last) {
+      for (int g = 0; g < ncl; ++g) {
+        if (g == cg) continue;
+        const int4* slot = reinterpret_cast<const int4*>(ws.slots) +
+                           (static_cast<int64_t>(rb) * ksplit + g * static_cast<int>(csize) + cr) * (DC_SLOT_I32 / 4);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int task = tid + DC_THREADS * u;
+          if (task >= ntask) continue;
+          const int4 v = __ldcg(slot + task);
+          sums[u].x += v.x;
+          sums[u].y += v.y;
+          sums[u].z += v.z;
+          sums[u].w += v.w;
         }
       }
     }
-    s_ready = ok;
+  } else if (tid == 0) {
+    s_last = 1;
   }
   __syncthreads();
 
-  // ---- split-K reduction and epilogue: this CTA owns row chunks [c0, c1) of 8 rows
-  if (run && s_ready && !s_abort) {
-    const int c0 = (DC_ROWS / 8) * rank / ksplit;
-    const int c1 = (DC_ROWS / 8) * (rank + 1) / ksplit;
-    const int nch = c1 - c0;
-    const int32_t* blk = ws.part + static_cast<int64_t>(rb) * ksplit * (DC_TOK * DC_ROWS);
-    for (int task = tid; task < DC_TOK * nch; task += DC_THREADS) {
-      const int t = task / nch;
-      const int r0 = (c0 + task % nch) * 8;
-      if (t >= M) continue;
-      int sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      // all partial loads of a batch are issued before any is consumed
-      for (int j0 = 0; j0 < ksplit; j0 += 8) {
-        int4 lo[8], hi[8];
+  // ---- epilogue of this CTA's tokens over the complete sums
+  if (s_last && run && !s_abort) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j0 + j < ksplit) {
-            const int4* src = reinterpret_cast<const int4*>(blk + static_cast<int64_t>(j0 + j) * (DC_TOK * DC_ROWS) +
-                                                            t * DC_ROWS + r0);
-            lo[j] = __ldcg(src);
-            hi[j] = __ldcg(src + 1);
-          } else {
-            lo[j] = make_int4(0, 0, 0, 0);
-            hi[j] = make_int4(0, 0, 0, 0);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sum[0] += lo[j].x; sum[1] += lo[j].y; sum[2] += lo[j].z; sum[3] += lo[j].w;
-          sum[4] += hi[j].x; sum[5] += hi[j].y; sum[6] += hi[j].z; sum[7] += hi[j].w;
-        }
-      }
-      const int64_t n0 = static_cast<int64_t>(rb) * DC_ROWS + r0;
-      if (n0 >= N) continue;
+    for (int u = 0; u < kPer; ++u) {
+      const int task = tid + DC_THREADS * u;
+      const int t = static_cast<int>(cr) * tq + (task >> 5);
+      const int64_t n0 = static_cast<int64_t>(rb) * DC_ROWS + (task & 31) * 4;
+      if (task >= ntask || t >= M || n0 >= N) continue;
+      const int sum[4] = {sums[u].x, sums[u].y, sums[u].z, sums[u].w};
       if constexpr (MODE == EPI_ACC) {
         int32_t* dst = static_cast<int32_t*>(a.out) + t * N + n0;
+        if (((reinterpret_cast<uintptr_t>(dst) & 15u) == 0u) && n0 + 4 <= N) {
+          *reinterpret_cast<int4*>(dst) = sums[u];
+        } else {
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-          if (n0 + r < N) dst[r] = sum[r];
+          for (int r = 0; r < 4; ++r)
+            if (n0 + r < N) dst[r] = sum[r];
+        }
       } else {
         const float sx = a.x_scale[t];
-        uint16_t o[8];
+        uint16_t o[4];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < 4; ++r) {
           float fv = 0.0f;
           if (n0 + r < N) {
             fv = dequant(sum[r], sx, a.w_scale[n0 + r]);
@@ -336,120 +413,142 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws) {
           o[r] = f32_to_bf16_bits(fv);
         }
         uint16_t* dst = static_cast<uint16_t*>(a.out) + t * N + n0;
-        if (((reinterpret_cast<uintptr_t>(dst) & 15u) == 0u) && n0 + 8 <= N) {
-          *reinterpret_cast<uint4*>(dst) = make_uint4(o[0] | (uint32_t(o[1]) << 16), o[2] | (uint32_t(o[3]) << 16),
-                                                      o[4] | (uint32_t(o[5]) << 16), o[6] | (uint32_t(o[7]) << 16));
+        if (((reinterpret_cast<uintptr_t>(dst) & 7u) == 0u) && n0 + 4 <= N) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(o[0] | (uint32_t(o[1]) << 16), o[2] | (uint32_t(o[3]) << 16));
         } else {
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+          for (int r = 0; r < 4; ++r)
             if (n0 + r < N) dst[r] = o[r];
         }
       }
     }
   }
-  __syncthreads();
-  // the last CTA of the row block to finish reading zeroes both counters
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(&ws.cnt_out[rb], 1u);
-    if (prev == static_cast<uint32_t>(ksplit - 1)) {
-      atomicExch(&ws.cnt_in[rb], 0u);
-      atomicExch(&ws.cnt_out[rb], 0u);
-    }
-  }
 
-  if (s_abort) {
+  if (tid == 0 && ((!run && a.pack_known) || s_abort)) {
+    // loads issued for a buffer that failed the header check, or an aborted CTA: let the copies land
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 20000000ull) {
     }
   }
+  __syncthreads();
   if (warp == 0) {
-    __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(DC_TMEM_COLS)
                  : "memory");
   }
 }
 
-constexpr size_t kDecSmem = DC_RING_BYTES + 1024;
+constexpr size_t kDecSmem = DC_RING_BYTES + static_cast<size_t>(DC_MAX_KB) * (DC_W_STAGE + DC_X_STAGE) + 1024;
+static_assert(kDecSmem <= 227 * 1024, "shared memory budget");
 
-// CTAs of the decode kernel that can be resident at once on the current device.
-int dec_resident_ctas() {
+void dec_set_attributes() {
+  for (auto k : {dec_gemm_kernel<EPI_BF16>, dec_gemm_kernel<EPI_ACC>}) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDecSmem));
+  }
+}
+
+// Clusters of `cs` decode CTAs that can be resident at once on the current device.
+int dec_resident_clusters(int cs) {
   static std::mutex mu;
-  static int cache[64] = {};
+  static int cache[64][DC_CLUSTER + 1] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cs < 1 || cs > DC_CLUSTER || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
-  if (cache[dev] == 0) {
-    int per_sm = 0, sms = 0;
-    cudaFuncSetAttribute(dec_gemm_kernel<EPI_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kDecSmem));
-    cudaFuncSetAttribute(dec_gemm_kernel<EPI_ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kDecSmem));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dec_gemm_kernel<EPI_BF16>, DC_THREADS, kDecSmem) !=
-            cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+  if (cache[dev][cs] == 0) {
+    dec_set_attributes();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+    cfg.blockDim = dim3(DC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = kDecSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dec_gemm_kernel<EPI_BF16>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
-    cache[dev] = per_sm * sms;
+    cache[dev][cs] = n;
   }
-  return cache[dev];
+  return cache[dev][cs];
 }
 
 template <int MODE>
-cudaError_t launch_dec_mode(const GemmArgs& a, const DecWs& ws, int ksplit, int nblk, cudaStream_t stream) {
-  auto k = dec_gemm_kernel<MODE>;
+cudaError_t launch_dec_mode(const GemmArgs& a, const DecWs& ws, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                            int ksplit, int nblk, cudaStream_t stream) {
+  dec_set_attributes();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ksplit), static_cast<unsigned>(nblk), 1);
   cfg.blockDim = dim3(DC_THREADS, 1, 1);
   cfg.dynamicSmemBytes = kDecSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit < DC_CLUSTER ? ksplit : DC_CLUSTER);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, ws);
+  return cudaLaunchKernelEx(&cfg, dec_gemm_kernel<MODE>, a, ws, wmap, xmap);
 }
 
 }  // namespace
 
 size_t dec_ws_bytes(int64_t N) {
   const int64_t nblk = (N + DC_ROWS - 1) / DC_ROWS;
-  return align_up(static_cast<uint64_t>(nblk) * DC_MAX_KSPLIT * DC_TOK * DC_ROWS * 4, 256) +
-         align_up(static_cast<uint64_t>(nblk) * 2 * 4, 256);
+  return align_up(static_cast<uint64_t>(nblk) * DC_MAX_KSPLIT * DC_SLOT_I32 * 4, 256) +
+         align_up(static_cast<uint64_t>(nblk) * DC_CLUSTER * 4, 256);
 }
 
-// K split for the decode engine: every CTA covers at most 1024 of K (one
-// exact fp32 chunk) and all nblk * ksplit CTAs must be resident at once; among
-// those, the largest split (most CTAs streaming weights).  0 = shape unsuited.
+// K split for the decode engine: 1, 2, 4 (one cluster per row block) or a
+// multiple of 4 up to 16 (clusters of 4); every CTA covers at most DC_MAX_KB
+// stages of K and all clusters fit in one wave.  Among those, the split with
+// the fewest stages per CTA, and of equal ones the smallest.  0 = shape
+// unsuited.
 int dec_plan_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
   (void)num_sms;
-  if (M < 1 || M > DC_TOK || K > static_cast<int64_t>(DC_MAX_KSPLIT) * kChunkK) return 0;
+  if (M < 1 || M > DC_TOK) return 0;
   const int64_t nkb = (K + DC_BK - 1) / DC_BK;
   const int64_t nblk = (N + DC_ROWS - 1) / DC_ROWS;
-  const int resident = dec_resident_ctas();
+  static const int kSplits[] = {1, 2, 4, 8, 12, 16};
   int best = 0;
-  for (int ks = 1; ks <= DC_MAX_KSPLIT; ++ks) {
-    if (ks > nkb || nblk * ks > resident) break;
-    if ((nkb + ks - 1) / ks <= DC_MAX_KB) best = ks;
+  int64_t best_stages = DC_MAX_KB + 1;
+  for (int ks : kSplits) {
+    if (ks > nkb) break;
+    const int cs = ks < DC_CLUSTER ? ks : DC_CLUSTER;
+    if (nblk * (ks / cs) > dec_resident_clusters(cs)) break;
+    const int64_t stages = (nkb + ks - 1) / ks;
+    if (stages < best_stages) {
+      best_stages = stages;
+      best = ks;
+    }
   }
-  return best;
+  return best_stages <= DC_MAX_KB ? best : 0;
 }
 
 cudaError_t launch_dec_gemm(const GemmArgs& a, int ksplit, void* dec_ws, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
+  if (ksplit < 1 || ksplit > DC_MAX_KSPLIT || (ksplit > DC_CLUSTER && ksplit % DC_CLUSTER != 0) || ksplit == 3)
+    return cudaErrorInvalidValue;
   const int nblk = static_cast<int>((a.N + DC_ROWS - 1) / DC_ROWS);
   DecWs ws;
   uint8_t* b = static_cast<uint8_t*>(dec_ws);
-  ws.part = reinterpret_cast<int32_t*>(b);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(
-      b + align_up(static_cast<uint64_t>(nblk) * DC_MAX_KSPLIT * DC_TOK * DC_ROWS * 4, 256));
-  ws.cnt_in = cnt;
-  ws.cnt_out = cnt + nblk;
-  if (a.mode == EPI_ACC) return launch_dec_mode<EPI_ACC>(a, ws, ksplit, nblk, stream);
-  return launch_dec_mode<EPI_BF16>(a, ws, ksplit, nblk, stream);
+  ws.slots = reinterpret_cast<int32_t*>(b);
+  ws.cnt = reinterpret_cast<uint32_t*>(b + align_up(static_cast<uint64_t>(nblk) * DC_MAX_KSPLIT * DC_SLOT_I32 * 4, 256));
+  // tensor maps of the int8 weight payload [N, K] and the int8 activations [R, K]; rows past the ends read as zero
+  CUtensorMap wmap, xmap;
+  const uint8_t* w_i8 = static_cast<const uint8_t*>(a.packed) + pack_layout(1, a.N, a.K, 0).i8_offset;
+  if (!encode_map_2d(&wmap, w_i8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.N, a.K, DC_BK, DC_ROWS,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_2d(&xmap, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.R, a.K, DC_BK, DC_TOK,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (a.mode == EPI_ACC) return launch_dec_mode<EPI_ACC>(a, ws, wmap, xmap, ksplit, nblk, stream);
+  return launch_dec_mode<EPI_BF16>(a, ws, wmap, xmap, ksplit, nblk, stream);
 }
 
 }  // namespace w8a8

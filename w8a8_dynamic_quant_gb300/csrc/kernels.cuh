@@ -38,6 +38,7 @@ struct GemmArgs {
   int64_t E = 1, R = 0, K = 0, N = 0; // N = rows per expert of the packed weight
   const void* packed = nullptr;       // packed weight buffer (header first)
   uint32_t pack_flags = 0;            // flags the call expects in the header
+  int pack_known = 0;                 // 1: this process packed the buffer with these E, N, K (host record)
   const float* w_scale = nullptr;     // [E,N] in ORIGINAL channel order
   const uint16_t* bias = nullptr;     // [N] bf16 or nullptr (dense only)
   void* out = nullptr;                // bf16 [R,N] | int32 [R,N] | bf16 h [R,N/2]
@@ -68,7 +69,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
 // tcgen05 decode engine (dense, M <= 64): int8 weights widened into TMEM, K
-// split over co-resident CTAs reduced through the workspace.
+// split over CTAs whose partials are bulk-added into the workspace.
 // dec_plan_ksplit returns 0 when the shape does not suit it.
 size_t dec_ws_bytes(int64_t N);
 int dec_plan_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);

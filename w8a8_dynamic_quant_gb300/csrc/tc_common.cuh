@@ -38,10 +38,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
-// when the CTA is aborting (this wait gave up, or another one did).
-static __device__ __noinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag, DeviceStatus* st,
-                                       uint32_t where) {
-  if (mbar_try_wait(a, parity)) return true;
+// when the CTA is aborting (this wait gave up, or another one did).  The
+// first probe is inline; only a phase still open calls the polling loop.
+static __device__ __noinline__ bool mbar_wait_poll(uint32_t a, uint32_t parity, volatile int* abort_flag,
+                                                   DeviceStatus* st, uint32_t where) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
@@ -52,6 +52,10 @@ static __device__ __noinline__ bool mbar_wait(uint32_t a, uint32_t parity, volat
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag, DeviceStatus* st,
+                                          uint32_t where) {
+  return mbar_try_wait(a, parity) || mbar_wait_poll(a, parity, abort_flag, st, where);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
