@@ -8,10 +8,14 @@ the five workloads (1 tiny dense, 2 dense decode, 3 dense prefill, 4 MoE
 prefill, 5 MoE decode with pre-quantised input).
 
 Timing: W warm-up steps, then exactly K steps between a barrier +
-synchronize on both sides.  Each kernel type is captured into a CUDA graph
-over rotating input sets whose total size exceeds the 129 MB L2 (or a single
-set when one set already exceeds it), and timed with CUDA events on the
-stream it runs on; the step time is the sum of the per-kernel times.  The
+synchronize on both sides.  The step (every kernel of the path, in order, on
+one input set) is captured into a CUDA graph over rotating input sets whose
+total size exceeds the 129 MB L2 (or a single set when one set already
+exceeds it) and timed with CUDA events on the stream it runs on; kernels of a
+step may overlap where the library lets them (the decode contraction starts
+its weight stream while the quantisation still runs).  Each kernel type is
+also captured on its own over the same sets for the per-kernel breakdown and
+the roofline of the dominant kernel.  The
 `e2e` leg runs the same step through the public Python API with the inputs
 copied from pinned host memory and the result copied back every step.
 `cpu_baseline` times the CPU oracle on the host cores on a bounded sample.
@@ -488,43 +492,51 @@ def run_gpu(args):
             for i in range(wl.n_sets):
                 wl.launch(k, i)
         graphs[k] = g
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph):
+        for i in range(wl.n_sets):
+            for k in wl.kernels:
+                wl.launch(k, i)
     torch.cuda.synchronize()
-
-    def replay_round(events=None):
-        for j, k in enumerate(wl.kernels):
-            if events is not None:
-                events[j].record(stream)
-            graphs[k].replay()
-        if events is not None:
-            events[-1].record(stream)
 
     rounds_w = max(1, -(-args.warmup // wl.n_sets))
     for _ in range(rounds_w):
-        replay_round()
+        step_graph.replay()
     rounds = max(1, -(-args.steps // wl.n_sets))
     steps = rounds * wl.n_sets
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(wl.kernels) + 1)] for _ in range(rounds)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(rounds + 1)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         t_wall0 = time.perf_counter()
+        ev[0].record(stream)
         for r in range(rounds):
-            replay_round(ev[r])
+            step_graph.replay()
+            ev[r + 1].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
         # keep the GPU loaded long enough for the clock sampler to see it
         extra = 0
         while not args.quick and time.perf_counter() - t_wall0 < 1.0 and extra < 100000:
-            replay_round()
+            step_graph.replay()
             extra += 1
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = clk.summary()
-    per_kernel_ms = {k: sum(ev[r][j].elapsed_time(ev[r][j + 1]) for r in range(rounds)) / steps
+    step_ms = sum(ev[r].elapsed_time(ev[r + 1]) for r in range(rounds)) / steps
+
+    # per-kernel breakdown: each kernel type alone over the same sets (outside the timed region)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(wl.kernels) + 1)] for _ in range(rounds)]
+    for r in range(rounds):
+        for j, k in enumerate(wl.kernels):
+            kev[r][j].record(stream)
+            graphs[k].replay()
+        kev[r][-1].record(stream)
+    torch.cuda.synchronize()
+    per_kernel_ms = {k: sum(kev[r][j].elapsed_time(kev[r][j + 1]) for r in range(rounds)) / steps
                      for j, k in enumerate(wl.kernels)}
-    step_ms = sum(per_kernel_ms.values())
     units, seconds = aggregate(wl.units_per_step * steps, step_ms * steps / 1e3)
     value = wl.value(units, seconds)
 
@@ -553,7 +565,8 @@ def run_gpu(args):
                 "traffic": traffic, "kernel": dom, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback",
                 "alg_bytes_per_launch": wl.alg_bytes[dom],
-                "per_kernel_us": {k: v * 1e3 for k, v in per_kernel_ms.items()}}
+                "per_kernel_us": {k: v * 1e3 for k, v in per_kernel_ms.items()},
+                "sum_of_kernels_us": sum(per_kernel_ms.values()) * 1e3}
     if "dynamic_quant" in per_kernel_ms:
         roofline["quant_gbs"] = wl.alg_bytes["dynamic_quant"] / (per_kernel_ms["dynamic_quant"] / 1e3) / 1e9
     if dom in wl.alg_flops:

@@ -121,16 +121,25 @@ __device__ __forceinline__ void widen16(const uint4& x, uint32_t* h) {
   s8x4_to_f16x4(x.w, h[6], h[7]);
 }
 
-// TMA loads of a CTA's whole K slice (stages [kb0, kb0 + my) of row block rb), one mbarrier per stage.
-__device__ __forceinline__ void issue_slice(const CUtensorMap* wmap, const CUtensorMap* xmap, uint64_t* bar_full,
-                                            uint8_t* wtiles, uint8_t* xtiles, int kb0, int my, int rb) {
+// TMA loads of a CTA's whole K slice of weights (stages [kb0, kb0 + my) of row block rb), one
+// mbarrier per stage that also expects the stage's activation tile.
+__device__ __forceinline__ void issue_weights(const CUtensorMap* wmap, uint64_t* bar_full, uint8_t* wtiles, int kb0,
+                                              int my, int rb) {
   for (int s = 0; s < my; ++s) {
     const uint32_t fb = smem_u32(&bar_full[s]);
     mbar_expect_tx(fb, DC_W_STAGE + DC_X_STAGE);
     tma_load_2d(smem_u32(wtiles + s * DC_W_STAGE), wmap, (kb0 + s) * DC_BK, rb * DC_ROWS, fb);
-    tma_load_2d(smem_u32(xtiles + s * DC_X_STAGE), xmap, (kb0 + s) * DC_BK, 0, fb);
   }
 }
+__device__ __forceinline__ void issue_activations(const CUtensorMap* xmap, uint64_t* bar_full, uint8_t* xtiles,
+                                                  int kb0, int my) {
+  for (int s = 0; s < my; ++s)
+    tma_load_2d(smem_u32(xtiles + s * DC_X_STAGE), xmap, (kb0 + s) * DC_BK, 0, smem_u32(&bar_full[s]));
+}
+// With programmatic stream serialization this kernel may start while the
+// kernel before it (the activation quantisation) still runs: everything that
+// kernel writes -- the int8 codes and the scales -- is read only after this.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Workspace of the decode engine: per row block and K split a slot for the
 // cluster-summed int32 piece [tokens of the CTA][DC_ROWS], and per row block
@@ -201,12 +210,16 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     }
     mbar_init(smem_u32(&bar_accf), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (a.pack_known) issue_slice(&wmap, &xmap, bar_full, wtiles, xtiles, kb0, my, rb);
+    if (a.pack_known) issue_weights(&wmap, bar_full, wtiles, kb0, my, rb);
   }
   const PackedHeader* hdr = static_cast<const PackedHeader*>(a.packed);
   const bool run = hdr->magic == kPackMagic && hdr->version == kPackVersion && hdr->E == 1 && hdr->N == N &&
                    hdr->K == K && (hdr->flags & W8A8_PACK_GATE_UP) == 0u;
-  if (tid == 0 && run && !a.pack_known) issue_slice(&wmap, &xmap, bar_full, wtiles, xtiles, kb0, my, rb);
+  if (tid == 0 && run) {
+    if (!a.pack_known) issue_weights(&wmap, bar_full, wtiles, kb0, my, rb);
+    wait_prior_grid();
+    issue_activations(&xmap, bar_full, xtiles, kb0, my);
+  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
                  "r"(DC_TMEM_COLS)
@@ -328,12 +341,17 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     const int task = tid + DC_THREADS * u;
     if (task >= ntask) continue;
     const uint32_t off = static_cast<uint32_t>(((static_cast<int>(cr) * tq + (task >> 5)) * DC_ROWS + (task & 31) * 4) * 4);
-    for (uint32_t c = 0; c < csize; ++c) {
-      const int4 v = ld_dsmem_v4(mapa_shared(smem_u32(ptile), c) + off);
-      sums[u].x += v.x;
-      sums[u].y += v.y;
-      sums[u].z += v.z;
-      sums[u].w += v.w;
+    int4 v[DC_CLUSTER];  // all remote loads in flight together
+#pragma unroll
+    for (int c = 0; c < DC_CLUSTER; ++c)
+      v[c] = c < static_cast<int>(csize) ? ld_dsmem_v4(mapa_shared(smem_u32(ptile), static_cast<uint32_t>(c)) + off)
+                                         : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int c = 0; c < DC_CLUSTER; ++c) {
+      sums[u].x += v[c].x;
+      sums[u].y += v[c].y;
+      sums[u].z += v[c].z;
+      sums[u].w += v[c].w;
     }
   }
   cluster_sync();  // no CTA reuses or releases its tile while the others still read it
@@ -359,28 +377,45 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
         ws.cnt[rb * 4 + cr] = 0u;  // for the next call
       }
     }
-    __syncthreads();
-    if (s_last) {
-      for (int g = 0; g < ncl; ++g) {
-        if (g == cg) continue;
-        const int4* slot = reinterpret_cast<const int4*>(ws.slots) +
-                           (static_cast<int64_t>(rb) * ksplit + g * static_cast<int>(csize) + cr) * (DC_SLOT_I32 / 4);
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int task = tid + DC_THREADS * u;
-          if (task >= ntask) continue;
-          const int4 v = __ldcg(slot + task);
-          sums[u].x += v.x;
-          sums[u].y += v.y;
-          sums[u].z += v.z;
-          sums[u].w += v.w;
-        }
-      }
-    }
   } else if (tid == 0) {
     s_last = 1;
   }
   __syncthreads();
+
+  // ---- the CTA holding the complete sums: epilogue inputs and the other clusters' slots, all loads
+  // issued before any is consumed (the scales were written by the kernel before this one)
+  wait_prior_grid();
+  float e_sx[kPer], e_sw[kPer][4], e_b[kPer][4];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int task = tid + DC_THREADS * u;
+    const int t = static_cast<int>(cr) * tq + (task >> 5);
+    const int64_t n0 = static_cast<int64_t>(rb) * DC_ROWS + (task & 31) * 4;
+    const bool live = MODE != EPI_ACC && s_last && run && task < ntask && t < M;
+    e_sx[u] = live ? a.x_scale[t] : 0.0f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      e_sw[u][r] = live && n0 + r < N ? a.w_scale[n0 + r] : 0.0f;
+      e_b[u][r] = live && a.bias != nullptr && n0 + r < N ? bf16_bits_to_f32(a.bias[n0 + r]) : 0.0f;
+    }
+  }
+  if (ncl > 1 && s_last) {
+    for (int g = 0; g < ncl; ++g) {
+      if (g == cg) continue;
+      const int4* slot = reinterpret_cast<const int4*>(ws.slots) +
+                         (static_cast<int64_t>(rb) * ksplit + g * static_cast<int>(csize) + cr) * (DC_SLOT_I32 / 4);
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int task = tid + DC_THREADS * u;
+        if (task >= ntask) continue;
+        const int4 v = __ldcg(slot + task);
+        sums[u].x += v.x;
+        sums[u].y += v.y;
+        sums[u].z += v.z;
+        sums[u].w += v.w;
+      }
+    }
+  }
 
   // ---- epilogue of this CTA's tokens over the complete sums
   if (s_last && run && !s_abort) {
@@ -401,15 +436,11 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
             if (n0 + r < N) dst[r] = sum[r];
         }
       } else {
-        const float sx = a.x_scale[t];
         uint16_t o[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          float fv = 0.0f;
-          if (n0 + r < N) {
-            fv = dequant(sum[r], sx, a.w_scale[n0 + r]);
-            if (a.bias) fv = __fadd_rn(fv, bf16_bits_to_f32(a.bias[n0 + r]));
-          }
+          float fv = dequant(sum[r], e_sx[u], e_sw[u][r]);
+          if (a.bias) fv = __fadd_rn(fv, e_b[u][r]);
           o[r] = f32_to_bf16_bits(fv);
         }
         uint16_t* dst = static_cast<uint16_t*>(a.out) + t * N + n0;
@@ -486,13 +517,17 @@ cudaError_t launch_dec_mode(const GemmArgs& a, const DecWs& ws, const CUtensorMa
   cfg.blockDim = dim3(DC_THREADS, 1, 1);
   cfg.dynamicSmemBytes = kDecSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit < DC_CLUSTER ? ksplit : DC_CLUSTER);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start before the previous kernel on the stream ends, if that kernel allows it (only the
+  // activation quantisation does); the kernel waits for it before reading what it wrote
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, dec_gemm_kernel<MODE>, a, ws, wmap, xmap);
 }
 

@@ -81,6 +81,12 @@ __device__ __forceinline__ void store8(const uint4& v, float s, int64_t row, int
   if (out != 0) reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s);
 }
 
+// Lets a kernel launched after this one with programmatic stream serialization
+// (the decode contraction) start its prologue -- and its weight stream, which
+// reads nothing this kernel writes -- while this kernel still runs; that kernel
+// waits (griddepcontrol.wait) before it reads the codes or scales written here.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -92,6 +98,7 @@ template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
                                                        int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                        float* __restrict__ scale) {
+  allow_dependent_launch();
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = K / 8;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
@@ -126,6 +133,7 @@ template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                       float* __restrict__ scale) {
+  allow_dependent_launch();
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
@@ -164,6 +172,7 @@ template <int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __restrict__ x, int64_t M,
                                                           int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                           float* __restrict__ scale) {
+  allow_dependent_launch();
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
