@@ -178,6 +178,10 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
   __shared__ int s_last;
+  // epilogue inputs of this row block, loaded by the converter warps before their first stage
+  __shared__ float s_sw[DC_ROWS];
+  __shared__ float s_bias[DC_ROWS];
+  __shared__ float s_sx[DC_TOK];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -215,8 +219,8 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   const PackedHeader* hdr = static_cast<const PackedHeader*>(a.packed);
   const bool run = hdr->magic == kPackMagic && hdr->version == kPackVersion && hdr->E == 1 && hdr->N == N &&
                    hdr->K == K && (hdr->flags & W8A8_PACK_GATE_UP) == 0u;
-  if (tid == 0 && run) {
-    if (!a.pack_known) issue_weights(&wmap, bar_full, wtiles, kb0, my, rb);
+  if (tid == 0 && run && !a.pack_known) issue_weights(&wmap, bar_full, wtiles, kb0, my, rb);
+  if (tid == 32 && run) {  // a second issuing thread, so the weight stream never waits for the previous grid
     wait_prior_grid();
     issue_activations(&xmap, bar_full, xtiles, kb0, my);
   }
@@ -256,13 +260,27 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     const int q = warp & 3;           // TMEM lane quadrant
     const int part = (warp - 1) >> 2;  // K part of each stage (chunks DC_WCH*part..) / token part
     const int row = 32 * q + lane;    // weight row inside the block == TMEM lane
+    if (MODE != EPI_ACC) {
+      // epilogue inputs into shared memory while the first stage is still in flight; the token
+      // scales come from the previous grid
+      if (ct < DC_ROWS) {
+        const int64_t n = static_cast<int64_t>(rb) * DC_ROWS + ct;
+        s_sw[ct] = n < N ? a.w_scale[n] : 0.0f;
+        s_bias[ct] = (a.bias != nullptr && n < N) ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
+      } else if (ct < DC_ROWS + DC_TOK) {
+        wait_prior_grid();
+        s_sx[ct - DC_ROWS] = ct - DC_ROWS < M ? a.x_scale[ct - DC_ROWS] : 0.0f;
+      }
+    }
     bool ok = true;
     for (int i = 0; i < my && ok; ++i) {
       const int f = i % DC_SF;
       const uint32_t phf = static_cast<uint32_t>(i / DC_SF) & 1u;
-      int got = 0;
-      if (lane == 0) got = mbar_wait(smem_u32(&bar_emptyf[f]), phf ^ 1u, &s_abort, a.status, 15u) ? 1 : 0;
-      got = __shfl_sync(0xffffffffu, got, 0);
+      int got = 1;
+      if (i >= DC_SF) {  // a fresh slot needs no wait
+        if (lane == 0) got = mbar_wait(smem_u32(&bar_emptyf[f]), phf ^ 1u, &s_abort, a.status, 15u) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+      }
       // every lane observes the completed load of stage i itself
       if (got) got = mbar_wait(smem_u32(&bar_full[i]), 0u, &s_abort, a.status, 13u) ? 1 : 0;
       if (!__all_sync(0xffffffffu, got)) {
@@ -382,23 +400,7 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   }
   __syncthreads();
 
-  // ---- the CTA holding the complete sums: epilogue inputs and the other clusters' slots, all loads
-  // issued before any is consumed (the scales were written by the kernel before this one)
-  wait_prior_grid();
-  float e_sx[kPer], e_sw[kPer][4], e_b[kPer][4];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int task = tid + DC_THREADS * u;
-    const int t = static_cast<int>(cr) * tq + (task >> 5);
-    const int64_t n0 = static_cast<int64_t>(rb) * DC_ROWS + (task & 31) * 4;
-    const bool live = MODE != EPI_ACC && s_last && run && task < ntask && t < M;
-    e_sx[u] = live ? a.x_scale[t] : 0.0f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      e_sw[u][r] = live && n0 + r < N ? a.w_scale[n0 + r] : 0.0f;
-      e_b[u][r] = live && a.bias != nullptr && n0 + r < N ? bf16_bits_to_f32(a.bias[n0 + r]) : 0.0f;
-    }
-  }
+  // ---- the CTA holding the complete sums adds the other clusters' slots
   if (ncl > 1 && s_last) {
     for (int g = 0; g < ncl; ++g) {
       if (g == cg) continue;
@@ -436,11 +438,13 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
             if (n0 + r < N) dst[r] = sum[r];
         }
       } else {
+        const int r0 = (task & 31) * 4;
+        const float sx = s_sx[t];
         uint16_t o[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          float fv = dequant(sum[r], e_sx[u], e_sw[u][r]);
-          if (a.bias) fv = __fadd_rn(fv, e_b[u][r]);
+          float fv = dequant(sum[r], sx, s_sw[r0 + r]);
+          if (a.bias) fv = __fadd_rn(fv, s_bias[r0 + r]);
           o[r] = f32_to_bf16_bits(fv);
         }
         uint16_t* dst = static_cast<uint16_t*>(a.out) + t * N + n0;
