@@ -33,7 +33,15 @@ namespace w8a8 {
 namespace {
 
 constexpr int BK = 64;       // K bytes per pipeline stage
-constexpr int STAGES = 4;
+// Ring depth and CTAs per SM of the 8-token tile (MoE decode); measured on GB300 at 8 x 2, against
+// 4 x 2 (70 % of HBM on the MoE decode layer) and 6..20 stages with 1..4 CTAs per SM.
+#ifndef REG_STAGES_V8
+#define REG_STAGES_V8 8
+#endif
+#ifndef REG_GRID_V8
+#define REG_GRID_V8 2
+#endif
+constexpr int STAGES = 4;  // pipeline depth of the 32- and 64-token tiles
 constexpr int kMaxE = 1024;
 
 template <int WM, int WN, int WARPS_W, int WARPS_T>
@@ -44,7 +52,9 @@ struct Tile {
   static constexpr int kStageW = BNW * BK;
   static constexpr int kStageT = BMT * BK;
   static constexpr int kStageBytes = kStageW + kStageT;
-  static constexpr int kPipeBytes = STAGES * kStageBytes;
+  // the 8-token tile streams weights for decode-sized groups: a deeper ring keeps more bytes in flight
+  static constexpr int kStages = (WM == 1 && WN == 1) ? REG_STAGES_V8 : STAGES;
+  static constexpr int kPipeBytes = kStages * kStageBytes;
   static constexpr int kEpiStride = BNW + 4;     // int32 words per staged token row
   static constexpr int kEpiBytes = BMT * kEpiStride * 4;
   static constexpr int kSmem = kPipeBytes > kEpiBytes ? kPipeBytes : kEpiBytes;
@@ -228,20 +238,20 @@ reg_gemm_kernel(const GemmArgs a, const int ksplit) {
     };
 
 #pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s) {
+    for (int s = 0; s < T::kStages - 1; ++s) {
       if (s < nkb) load_stage(s, kb0 + s);
       cp_async_commit();
     }
     int since_drain = 0;
     for (int i = 0; i < nkb; ++i) {
-      cp_async_wait<STAGES - 2>();
+      cp_async_wait<T::kStages - 2>();
       __syncthreads();
       {
-        const int nxt = i + STAGES - 1;
-        if (nxt < nkb) load_stage(nxt % STAGES, kb0 + nxt);
+        const int nxt = i + T::kStages - 1;
+        if (nxt < nkb) load_stage(nxt % T::kStages, kb0 + nxt);
         cp_async_commit();
       }
-      const uint8_t* sW = smem + (i % STAGES) * T::kStageBytes;
+      const uint8_t* sW = smem + (i % T::kStages) * T::kStageBytes;
       const uint8_t* sT = sW + T::kStageW;
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
@@ -478,7 +488,8 @@ GemmPlan plan_reg_gemm(const GemmArgs& a, int num_sms) {
   }
   p.ksplit = ks;
   const int64_t ub = upper_tiles(a.E, a.R, a.N, grouped, bmt) * ks;
-  p.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ub, static_cast<int64_t>(num_sms) * 2)));
+  const int per_sm = p.variant == 8 ? REG_GRID_V8 : 2;
+  p.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ub, static_cast<int64_t>(num_sms) * per_sm)));
   p.smem = smem_of(p.variant);
   return p;
 }
