@@ -74,11 +74,29 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   return r;
 }
 
-// OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both.
+// OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both (each code computed once).
 __device__ __forceinline__ void store8(const uint4& v, float s, int64_t row, int64_t K, int64_t idx, void* q,
                                        uint16_t* q16, int out) {
-  if (out != 1) reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v, s);
-  if (out != 0) reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s);
+  if (out == 0) {
+    reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v, s);
+  } else if (out == 1) {
+    reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s);
+  } else {
+    uint32_t b[4] = {0u, 0u, 0u, 0u}, h[4] = {0u, 0u, 0u, 0u};  // byte pairs / fp16 pairs of v.x .. v.w
+    if (s > 0.0f) {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int lo = q1(__uint_as_float(w[i] << 16), s);
+        const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s);
+        b[i] = (static_cast<uint32_t>(lo) & 0xffu) | ((static_cast<uint32_t>(hi) & 0xffu) << 8);
+        h[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
+               (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
+      }
+    }
+    reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+    reinterpret_cast<uint4*>(q16 + row * K)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
 }
 
 // Lets a kernel launched after this one with programmatic stream serialization
@@ -106,15 +124,14 @@ __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restric
        row += warps_total) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
     uint4 v[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {  // every load of the row in flight before any is used
+      const int64_t idx = lane + 32 * c;
+      v[c] = idx < nchunk ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int64_t idx = lane + 32 * c;
-      if (idx < nchunk) {
-        v[c] = ldg_stream(xr + idx);
-        amax = fmaxf(amax, absmax8(v[c]));
-      }
-    }
+    for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
     amax = warp_max(amax);
     const float s = __fdiv_rn(amax, 127.0f);
     if (lane == 0) scale[row] = s;
@@ -139,15 +156,14 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
     uint4 v[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {  // every load of the row in flight before any is used
+      const int64_t idx = threadIdx.x + 256 * c;
+      v[c] = idx < nchunk ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int64_t idx = threadIdx.x + 256 * c;
-      if (idx < nchunk) {
-        v[c] = ldg_stream(xr + idx);
-        amax = fmaxf(amax, absmax8(v[c]));
-      }
-    }
+    for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
     amax = warp_max(amax);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
     __syncthreads();
