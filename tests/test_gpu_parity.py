@@ -70,6 +70,36 @@ def test_quant_edge_rows():
     assert_quant_equal(S.to_bf16_bits(np.stack(rows)))
 
 
+def test_quant_quotients_at_and_near_half_integers():
+    """Rows whose quotients x / s sit exactly on, or within a few binary32 ulps
+    of, the half-integers where rounding changes: the kernels take their
+    exact-division path there and must still agree bit for bit."""
+    K = 256
+    ks = np.arange(-127, 127, dtype=np.float32)
+    rows = []
+    for e in (-20, -3, 0, 5, 40):  # s = 2^e exactly when the row's absmax is 127 * 2^e
+        base = np.float32(2.0 ** e)
+        ties = (ks + np.float32(0.5)) * base
+        row = np.resize(ties, K)
+        row[0] = np.float32(127) * base
+        rows.append(row)
+    # absmax not a multiple of 127: s is inexact and the quotients land near, not on, the ties
+    rng = np.random.default_rng(5)
+    for amax in (np.float32(126.9), np.float32(100.25), np.float32(3.0e-3), np.float32(7.77e20)):
+        s = np.float32(amax / np.float32(127))
+        near = (rng.integers(-127, 127, K).astype(np.float32) + np.float32(0.5)) * s
+        near = near * (np.float32(1) + rng.integers(-4, 5, K).astype(np.float32) * np.float32(2.0 ** -20))
+        near[0] = amax
+        rows.append(near)
+    x = np.stack(rows).astype(np.float32)
+    assert_quant_equal(S.to_bf16_bits(x))
+    # the rows do hold many exact ties after rounding to bf16
+    xb = S.bf16_bits_to_f32(S.to_bf16_bits(x))
+    q, s = oracle.dynamic_quant(S.to_bf16_bits(x))
+    quot = xb / s[:, None]
+    assert np.count_nonzero(np.abs(quot - np.rint(quot)) == 0.5) > 500
+
+
 def test_quant_empty_is_noop():
     x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     q, s = W.w8a8_dynamic_quant(x)

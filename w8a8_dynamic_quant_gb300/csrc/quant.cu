@@ -29,21 +29,27 @@ __device__ __forceinline__ float absmax8(const uint4& v) {
   return m;
 }
 
-__device__ __forceinline__ int q1(float xf, float s) {
-  // s > 0 here; binary32 divide, round half to even, clamp to +-127
-  int r = __float2int_rn(__fdiv_rn(xf, s));
+// rint(x / s) with the quotient rounded to binary32 first (round half to even), clamped to +-127;
+// s > 0, rs = the binary32 reciprocal of s.  y = x * rs is within |x / s| * 2^-23 + 2^-18 <= 2^-15 of
+// the correctly rounded quotient (|x / s| <= 128), so when y is more than 2^-14 from the nearest
+// half-integer both lie strictly inside the same rounding interval and round to the same integer;
+// otherwise (rare), and for non-finite y, the quotient itself is computed.
+__device__ __forceinline__ int q1(float xf, float s, float rs) {
+  const float y = __fmul_rn(xf, rs);
+  const float frac = __fsub_rn(y, floorf(y));  // exact for |y| < 2^23
+  const int r = fabsf(frac - 0.5f) > 0x1p-14f ? __float2int_rn(y) : __float2int_rn(__fdiv_rn(xf, s));
   return max(-127, min(127, r));
 }
 
 // 8 bf16 -> 8 int8 packed in a uint2.
-__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s, float rs) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t out[2] = {0u, 0u};
   if (s > 0.0f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int lo = q1(__uint_as_float(w[i] << 16), s);
-      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s);
+      const int lo = q1(__uint_as_float(w[i] << 16), s, rs);
+      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s, rs);
       const uint32_t pair = (static_cast<uint32_t>(lo) & 0xffu) | ((static_cast<uint32_t>(hi) & 0xffu) << 8);
       out[i >> 1] |= pair << ((i & 1) * 16);
     }
@@ -52,14 +58,14 @@ __device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
 }
 
 // 8 bf16 -> 8 integer-valued fp16 (same codes as quant8) packed in a uint4.
-__device__ __forceinline__ uint4 quant8_f16(const uint4& v, float s) {
+__device__ __forceinline__ uint4 quant8_f16(const uint4& v, float s, float rs) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t out[4] = {0u, 0u, 0u, 0u};
   if (s > 0.0f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int lo = q1(__uint_as_float(w[i] << 16), s);
-      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s);
+      const int lo = q1(__uint_as_float(w[i] << 16), s, rs);
+      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s, rs);
       out[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
                (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
     }
@@ -75,20 +81,20 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
 }
 
 // OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both (each code computed once).
-__device__ __forceinline__ void store8(const uint4& v, float s, int64_t row, int64_t K, int64_t idx, void* q,
-                                       uint16_t* q16, int out) {
+__device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_t row, int64_t K, int64_t idx,
+                                       void* q, uint16_t* q16, int out) {
   if (out == 0) {
-    reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v, s);
+    reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v, s, rs);
   } else if (out == 1) {
-    reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s);
+    reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s, rs);
   } else {
     uint32_t b[4] = {0u, 0u, 0u, 0u}, h[4] = {0u, 0u, 0u, 0u};  // byte pairs / fp16 pairs of v.x .. v.w
     if (s > 0.0f) {
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int lo = q1(__uint_as_float(w[i] << 16), s);
-        const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s);
+        const int lo = q1(__uint_as_float(w[i] << 16), s, rs);
+        const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s, rs);
         b[i] = (static_cast<uint32_t>(lo) & 0xffu) | ((static_cast<uint32_t>(hi) & 0xffu) << 8);
         h[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
                (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
@@ -134,12 +140,13 @@ __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restric
     for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
     amax = warp_max(amax);
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
     if (lane == 0) scale[row] = s;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = lane + 32 * c;
       if (idx < nchunk) {
-        store8(v[c], s, row, K, idx, q, q16, OUT);
+        store8(v[c], s, rs, row, K, idx, q, q16, OUT);
       }
     }
   }
@@ -171,12 +178,13 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
     if (threadIdx.x == 0) scale[row] = s;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = threadIdx.x + 256 * c;
       if (idx < nchunk) {
-        store8(v[c], s, row, K, idx, q, q16, OUT);
+        store8(v[c], s, rs, row, K, idx, q, q16, OUT);
       }
     }
     __syncthreads();  // red[] is reused by the next row
@@ -202,9 +210,10 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
     if (threadIdx.x == 0) scale[row] = s;
     for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) {
-      store8(xr[idx], s, row, K, idx, q, q16, OUT);
+      store8(xr[idx], s, rs, row, K, idx, q, q16, OUT);
     }
     __syncthreads();
   }
