@@ -39,7 +39,8 @@ def tc_dense(q, xs, w, wsc, bias=None):
 
 
 @pytest.mark.parametrize("M,N,K,bias", [(128, 256, 64, False), (130, 200, 80, True), (300, 512, 1040, True),
-                                        (256, 384, 4096, False), (1000, 768, 2064, True), (129, 2048, 7168, False)])
+                                        (256, 384, 4096, False), (1000, 768, 2064, True), (129, 2048, 7168, False),
+                                        (600, 1280, 576, True)])
 def test_tc_dense_exact(M, N, K, bias):
     d = S.make_dense(M, K, N, n_outlier=min(4, K), outlier_mult=20.0, bias=bias, seed=M * 3 + N + K)
     q, xs = oracle.dynamic_quant(d.x)
@@ -82,7 +83,7 @@ def test_tc_dense_prefill_config_sampled_rows():
 
 
 @pytest.mark.parametrize("gl,K,N", [([300, 0, 129, 77, 0, 200], 512, 256), ([64] * 8, 1024, 512),
-                                    ([0, 0, 1000, 24], 2064, 384)])
+                                    ([0, 0, 1000, 24], 2064, 384), ([385, 0, 129, 1], 576, 768)])
 def test_tc_grouped_exact(gl, K, N):
     rng = np.random.default_rng(sum(gl) + K)
     R, E = int(sum(gl)), len(gl)

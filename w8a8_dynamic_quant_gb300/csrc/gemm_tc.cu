@@ -21,6 +21,17 @@
 // activation rows x 64 K, B = 256 weight rows x 64 K (48 KB per stage).  One
 // elected thread issues tcgen05.mma M=128 N=256 K=16 four times per stage.
 //
+// Clusters of two CTAs.  The CTAs of a cluster work on neighbouring tiles
+// that share one operand and fetch that operand once for both: each loads
+// half of it and multicasts the half into the same stage of both CTAs.  For
+// m-blocks 2p and 2p+1 of an expert at one n-block the shared operand is the
+// 256-row weight block; an expert with an odd number of m-blocks leaves its
+// last m-block, and for it the pair takes n-blocks 2j and 2j+1 and shares
+// the 128-row activation block.  Either way each SM requests 256 rows of 128
+// bytes per stage instead of 384.  A stage is free again only when both
+// CTAs' MMAs are done with it, so each MMA commit arrives on the empty
+// barrier of both CTAs (count 2).
+//
 // Warp roles (320 threads, one CTA per SM, persistent over output tiles):
 //   warp 0     TMA producer
 //   warp 1     TMEM owner and MMA issuer
@@ -48,6 +59,8 @@ constexpr uint32_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
 constexpr int TC_THREADS = 320;
 constexpr int TC_EPI_WARPS = 8;
 constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column fp32 accumulators
+constexpr int TC_CLUSTER = 2;
+constexpr uint16_t TC_PAIR_MASK = 0x3;
 constexpr int kMaxE = 1024;
 
 // kind::f16 instruction descriptor: D = F32, A = B = F16, both K-major, N = 256, M = 128.
@@ -59,10 +72,21 @@ __device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f
 
 struct TileInfo {
   int e, mb, nb, cnt;
+  int share_a;   // 0: the pair shares the weight block, 1: it shares the activation block
   int64_t row0;  // first global row of the tile (into the [R,K] activation matrix)
 };
 
-__device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int* tile_prefix, const int* row_off) {
+// Work units (tile pairs) of an expert with `cnt` rows: pairs of m-blocks at
+// every n-block, then pairs of n-blocks for a leftover odd m-block.
+__host__ __device__ __forceinline__ int pair_units(int cnt, int NB) {
+  const int mblocks = (cnt + TC_BM - 1) / TC_BM;
+  return (mblocks >> 1) * NB + (mblocks & 1) * ((NB + 1) >> 1);
+}
+
+// Tile of CTA `rank` (0 or 1) of the cluster for work unit t.  The second tile
+// of a unit may lie past the expert's n-blocks: it is computed and not stored.
+__device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int* tile_prefix, const int* row_off,
+                                                int rank) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -73,21 +97,105 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int*
   const int local = t - tile_prefix[lo];
   ti.cnt = row_off[lo + 1] - row_off[lo];
   const int mblocks = (ti.cnt + TC_BM - 1) / TC_BM;
-  // Rasterise in groups of up to TC_GROUP_N n-blocks: inside a group the
-  // n-block varies fastest, then the m-block, so the CTAs in flight share one
-  // activation block and the group's weight blocks stay resident in L2 while
-  // all m-blocks sweep past them.
-  const int g = local / (mblocks * TC_GROUP_N);
-  const int rem = local - g * mblocks * TC_GROUP_N;
-  const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
-  ti.mb = rem / gn;
-  ti.nb = g * TC_GROUP_N + rem % gn;
+  const int mpairs = mblocks >> 1;
+  if (local < mpairs * NB) {
+    // Rasterise in groups of up to TC_GROUP_N n-blocks: inside a group the
+    // n-block varies fastest, then the m-block pair, so the clusters in
+    // flight share activation blocks and the group's weight blocks stay
+    // resident in L2 while all m-blocks sweep past them.
+    const int g = local / (mpairs * TC_GROUP_N);
+    const int rem = local - g * mpairs * TC_GROUP_N;
+    const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
+    ti.share_a = 0;
+    ti.mb = 2 * (rem / gn) + rank;
+    ti.nb = g * TC_GROUP_N + rem % gn;
+  } else {
+    ti.share_a = 1;
+    ti.mb = mblocks - 1;
+    ti.nb = 2 * (local - mpairs * NB) + rank;
+  }
   ti.row0 = static_cast<int64_t>(row_off[lo]) + static_cast<int64_t>(ti.mb) * TC_BM;
   return ti;
 }
 
+// Stores one output row segment of a finished tile: global row gr, 128
+// columns from n_base (expert e's weight rows), from the exact int32 sums.
 template <int MODE>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__device__ __forceinline__ void store_row(const GemmArgs& a, int e, int64_t gr, int64_t n_base, const int (&sums)[128]) {
+  const int64_t N = a.N;
+  if constexpr (MODE == EPI_ACC) {
+    int32_t* dst = static_cast<int32_t*>(a.out) + gr * N + n_base;
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 3) == 0) && (n_base + 128 <= N);
+#pragma unroll
+    for (int c4 = 0; c4 < 32; ++c4) {
+      if (vec) {
+        reinterpret_cast<int4*>(dst)[c4] =
+            make_int4(sums[4 * c4], sums[4 * c4 + 1], sums[4 * c4 + 2], sums[4 * c4 + 3]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (n_base + 4 * c4 + k < N) dst[4 * c4 + k] = sums[4 * c4 + k];
+      }
+    }
+  } else if constexpr (MODE == EPI_BF16) {
+    const float sx = a.x_scale[gr];
+    const float* sw = a.w_scale + static_cast<int64_t>(e) * N;
+    uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * N + n_base;
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 7) == 0) && (n_base + 128 <= N);
+#pragma unroll
+    for (int c8 = 0; c8 < 16; ++c8) {
+      uint16_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t n = n_base + 8 * c8 + k;
+        float f = 0.0f;
+        if (n < N) {
+          f = dequant(sums[8 * c8 + k], sx, sw[n]);
+          if (a.bias) f = __fadd_rn(f, bf16_bits_to_f32(a.bias[n]));
+        }
+        v[k] = f32_to_bf16_bits(f);
+      }
+      if (vec) {
+        reinterpret_cast<uint4*>(dst)[c8] =
+            make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
+                       v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (n_base + 8 * c8 + k < N) dst[8 * c8 + k] = v[k];
+      }
+    }
+  } else {  // EPI_SWIGLU: columns [0,64) gate j, [64,128) up j, j = n_base/2 + [0,64)
+    const float sx = a.x_scale[gr];
+    const int64_t I = N / 2;
+    const float* sw = a.w_scale + static_cast<int64_t>(e) * N;
+    const int64_t j0 = (n_base / 128) * kGateUpBlock;
+    uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * I + j0;
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((I & 7) == 0);
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      uint16_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int jj = 8 * c8 + k;
+        const float gte = bf16_round(dequant(sums[jj], sx, sw[j0 + jj]));
+        const float up = bf16_round(dequant(sums[kGateUpBlock + jj], sx, sw[I + j0 + jj]));
+        v[k] = swiglu_bf16(gte, up);
+      }
+      if (vec) {
+        reinterpret_cast<uint4*>(dst)[c8] =
+            make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
+                       v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[8 * c8 + k] = v[k];
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(TC_CLUSTER, 1, 1) __launch_bounds__(TC_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[TC_STAGES];
@@ -113,6 +221,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_base = smem_u32(stages);
+  uint32_t rank, cluster_id, nclusters;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cluster_id));
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(nclusters));
 
   if (tid == 0) {
     s_abort = 0;
@@ -123,7 +235,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       s_bad = W8A8_ERR_PACKED;
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), TC_CLUSTER);  // one commit from each CTA's MMA
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_accf[b]), 1);
@@ -153,7 +265,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int ci = (c < 0 || c > a.R) ? 0 : static_cast<int>(c);
     cnts[i] = ci;
     rows_loc += ci;
-    tiles_loc += ((ci + TC_BM - 1) / TC_BM) * NB;
+    tiles_loc += pair_units(ci, NB);
   }
   int rows_total, tiles_total;
   int row_before = block_exclusive_scan<TC_THREADS>(rows_loc, rows_total, s_warp);
@@ -167,14 +279,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       s_tile_prefix[e] = tile_before;
     }
     row_before += cnts[i];
-    tile_before += ((cnts[i] + TC_BM - 1) / TC_BM) * NB;
+    tile_before += pair_units(cnts[i], NB);
   }
   if (tid == 0) {
     s_row_off[E] = rows_total;
     s_tile_prefix[E] = tiles_total;
   }
+  // Both CTAs' barriers are initialised before either sends the other a copy or an arrival.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   int bad = s_bad;
@@ -187,21 +300,40 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < my_tiles && !s_abort; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off);
+      for (int t = static_cast<int>(cluster_id); t < my_tiles && !s_abort; t += static_cast<int>(nclusters)) {
+        const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off, static_cast<int>(rank));
         const int ya = static_cast<int>(ti.row0);
         const int yb = static_cast<int>(static_cast<int64_t>(ti.e) * N + static_cast<int64_t>(ti.nb) * TC_BN);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
           const uint32_t full = smem_u32(&bar_full[stage]);
-          mbar_expect_tx(full, TC_STAGE_BYTES);
+          mbar_expect_tx(full, TC_STAGE_BYTES);  // own loads plus the peer's multicast half
           const uint32_t sa = stage_base + stage * TC_STAGE_BYTES;
-          tma_load_2d(sa, &tmA, kb * TC_BK, ya, full);
-          tma_load_2d(sa + TC_A_BYTES, &tmB, kb * TC_BK, yb, full);
+          const int x = kb * TC_BK;
+          if (ti.share_a) {
+            tma_load_2d_mc(sa + rank * (TC_A_BYTES / 2), &tmA, x, ya + static_cast<int>(rank) * (TC_BM / 2), full,
+                           TC_PAIR_MASK);
+            tma_load_2d(sa + TC_A_BYTES, &tmB, x, yb, full);
+            tma_load_2d(sa + TC_A_BYTES + TC_B_BYTES / 2, &tmB, x, yb + TC_BN / 2, full);
+          } else {
+            tma_load_2d(sa, &tmA, x, ya, full);
+            tma_load_2d(sa + TC_A_BYTES / 2, &tmA, x, ya + TC_BM / 2, full);
+            tma_load_2d_mc(sa + TC_A_BYTES + rank * (TC_B_BYTES / 2), &tmB, x, yb + static_cast<int>(rank) * (TC_BN / 2),
+                           full, TC_PAIR_MASK);
+          }
           if (++stage == TC_STAGES) {
             stage = 0;
             phase ^= 1u;
           }
+        }
+      }
+      // Drain: every stage's last fill has been consumed by both CTAs, so no copy into either CTA and no
+      // arrival on this CTA's barriers is still in flight when the cluster leaves.
+      for (int i = 0; i < TC_STAGES && !s_abort; ++i) {
+        if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 5u)) break;
+        if (++stage == TC_STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
@@ -211,7 +343,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_count = 0;
-      for (int t = blockIdx.x; t < my_tiles && !s_abort; t += gridDim.x) {
+      for (int t = static_cast<int>(cluster_id); t < my_tiles && !s_abort; t += static_cast<int>(nclusters)) {
         for (int c = 0; c < nchunk && !s_abort; ++c) {
           const uint32_t b = acc_count & 1u;
           const uint32_t use = acc_count >> 1;
@@ -235,7 +367,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc,
                      (kb > c * TC_KB_PER_CHUNK || k > 0) ? 1u : 0u);
             }
-            tc_commit(smem_u32(&bar_empty[stage]));
+            tc_commit_mc(smem_u32(&bar_empty[stage]), TC_PAIR_MASK);  // frees the stage in both CTAs
             if (++stage == TC_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -254,8 +386,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int r_loc = 32 * q + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     uint32_t acc_count = 0;
-    for (int t = blockIdx.x; t < my_tiles && !s_abort; t += gridDim.x) {
-      const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off);
+    for (int t = static_cast<int>(cluster_id); t < my_tiles && !s_abort; t += static_cast<int>(nclusters)) {
+      const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off, static_cast<int>(rank));
       int sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
@@ -290,76 +422,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int rows_valid = min(TC_BM, ti.cnt - ti.mb * TC_BM);
       const int64_t n_base = static_cast<int64_t>(ti.nb) * TC_BN + half * 128;
       if (r_loc < rows_valid && n_base < N) {
-        const int64_t gr = ti.row0 + r_loc;
-        if constexpr (MODE == EPI_ACC) {
-          int32_t* dst = static_cast<int32_t*>(a.out) + gr * N + n_base;
-          const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 3) == 0) && (n_base + 128 <= N);
-#pragma unroll
-          for (int c4 = 0; c4 < 32; ++c4) {
-            if (vec) {
-              reinterpret_cast<int4*>(dst)[c4] =
-                  make_int4(sums[4 * c4], sums[4 * c4 + 1], sums[4 * c4 + 2], sums[4 * c4 + 3]);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                if (n_base + 4 * c4 + k < N) dst[4 * c4 + k] = sums[4 * c4 + k];
-            }
-          }
-        } else if constexpr (MODE == EPI_BF16) {
-          const float sx = a.x_scale[gr];
-          const float* sw = a.w_scale + static_cast<int64_t>(ti.e) * N;
-          uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * N + n_base;
-          const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 7) == 0) && (n_base + 128 <= N);
-#pragma unroll
-          for (int c8 = 0; c8 < 16; ++c8) {
-            uint16_t v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int64_t n = n_base + 8 * c8 + k;
-              float f = 0.0f;
-              if (n < N) {
-                f = dequant(sums[8 * c8 + k], sx, sw[n]);
-                if (a.bias) f = __fadd_rn(f, bf16_bits_to_f32(a.bias[n]));
-              }
-              v[k] = f32_to_bf16_bits(f);
-            }
-            if (vec) {
-              reinterpret_cast<uint4*>(dst)[c8] =
-                  make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
-                             v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
-            } else {
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (n_base + 8 * c8 + k < N) dst[8 * c8 + k] = v[k];
-            }
-          }
-        } else {  // EPI_SWIGLU: columns [0,64) gate j, [64,128) up j, j = n_base/2 + [0,64)
-          const float sx = a.x_scale[gr];
-          const int64_t I = N / 2;
-          const float* sw = a.w_scale + static_cast<int64_t>(ti.e) * N;
-          const int64_t j0 = (n_base / 128) * kGateUpBlock;
-          uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * I + j0;
-          const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((I & 7) == 0);
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            uint16_t v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int jj = 8 * c8 + k;
-              const float gte = bf16_round(dequant(sums[jj], sx, sw[j0 + jj]));
-              const float up = bf16_round(dequant(sums[kGateUpBlock + jj], sx, sw[I + j0 + jj]));
-              v[k] = swiglu_bf16(gte, up);
-            }
-            if (vec) {
-              reinterpret_cast<uint4*>(dst)[c8] =
-                  make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
-                             v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
-            } else {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) dst[8 * c8 + k] = v[k];
-            }
-          }
-        }
+        store_row<MODE>(a, ti.e, ti.row0 + r_loc, n_base, sums);
       }
     }
   }
@@ -376,10 +439,240 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     while (globaltimer_ns() - t0 < 20000000ull) {
     }
   }
+  cluster_sync_all();  // neither CTA leaves while the other may still write into it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TC_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dense contraction on CTA pairs (tcgen05 cta_group::2).  One tile is 256
+// rows x 256 columns; the even CTA of the cluster holds rows [0,128) of A and
+// weight rows [0,128) of B, the odd CTA rows [128,256) and weight rows
+// [128,256), so a stage is 32 KB per CTA and six stages fit (more copies in
+// flight than the four 48 KB stages of the single-CTA tile).  One thread of
+// the even CTA issues tcgen05.mma M=256 N=256 K=16 over both CTAs' shared
+// memory; each CTA's tensor memory receives its 128 rows of the accumulator.
+// Both CTAs' copies complete on the even CTA's full barrier; the MMA commit
+// frees the stage in both CTAs; both CTAs' epilogues release an accumulator
+// on the even CTA's barrier.
+constexpr int P_BM = 256;       // rows per pair tile
+constexpr int P_HALF = 128;     // rows of A and of B held by each CTA
+constexpr int P_STAGES = 6;
+constexpr uint32_t P_HALF_BYTES = P_HALF * TC_BK * 2;  // 16 KB
+constexpr uint32_t P_STAGE_BYTES = 2 * P_HALF_BYTES;   // this CTA's A rows and B rows
+constexpr uint32_t kIdescPair = (1u << 4) | (uint32_t(TC_BN >> 3) << 17) | (uint32_t(P_BM >> 4) << 24);
+
+template <int MODE>
+__global__ void __cluster_dims__(TC_CLUSTER, 1, 1) __launch_bounds__(TC_THREADS, 1)
+tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[P_STAGES];   // even CTA: both CTAs' copies of the stage landed
+  __shared__ __align__(8) uint64_t bar_empty[P_STAGES];  // the pair MMAs reading the stage are done
+  __shared__ __align__(8) uint64_t bar_accf[2];
+  __shared__ __align__(8) uint64_t bar_acce[2];          // even CTA: both CTAs drained the accumulator
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+  __shared__ int s_bad;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t M = a.R;
+  const int64_t N = a.N;
+  const int64_t K = a.K;
+  const int NB = static_cast<int>((N + TC_BN - 1) / TC_BN);
+  const int MB = static_cast<int>((M + P_BM - 1) / P_BM);
+  const int nkb = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  const int nchunk = (nkb + TC_KB_PER_CHUNK - 1) / TC_KB_PER_CHUNK;
+
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_base = smem_u32(stages);
+  uint32_t rank, cluster_id, nclusters;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cluster_id));
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(nclusters));
+
+  if (tid == 0) {
+    s_abort = 0;
+    s_bad = 0;
+    const PackedHeader* h = static_cast<const PackedHeader*>(a.packed);
+    if (h->magic != kPackMagic || h->version != kPackVersion || h->E != a.E || h->N != a.N || h->K != a.K ||
+        ((h->flags ^ a.pack_flags) & W8A8_PACK_GATE_UP) != 0u || (h->flags & W8A8_PACK_F16) == 0u)
+      s_bad = W8A8_ERR_PACKED;
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_accf[b]), 1);
+      mbar_init(smem_u32(&bar_acce[b]), TC_CLUSTER * TC_EPI_WARPS);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
+                 "r"(TC_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers and tensor memory exist before either touches the other's
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  const int bad = s_bad;
+  if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, static_cast<uint32_t>(bad), 0u);
+  const int units = bad ? 0 : MB * NB;
+
+  // Rasterised like the single-CTA kernel: groups of TC_GROUP_N n-blocks, m-block slower.
+  auto tile_of = [&](int t, int& mb, int& nb) {
+    const int g = t / (MB * TC_GROUP_N);
+    const int rem = t - g * MB * TC_GROUP_N;
+    const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
+    mb = rem / gn;
+    nb = g * TC_GROUP_N + rem % gn;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = static_cast<int>(cluster_id); t < units && !s_abort; t += static_cast<int>(nclusters)) {
+        int mb, nb;
+        tile_of(t, mb, nb);
+        const int ya = mb * P_BM + static_cast<int>(rank) * P_HALF;
+        const int yb = nb * TC_BN + static_cast<int>(rank) * P_HALF;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
+          const uint32_t full = smem_u32(&bar_full[stage]);
+          if (rank == 0) mbar_expect_tx(full, TC_CLUSTER * P_STAGE_BYTES);
+          const uint32_t full_even = smem_cluster_addr(full, 0);
+          const uint32_t sa = stage_base + stage * P_STAGE_BYTES;
+          tma_load_2d_pair(sa, &tmA, kb * TC_BK, ya, full_even);
+          tma_load_2d_pair(sa + P_HALF_BYTES, &tmB, kb * TC_BK, yb, full_even);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: the last fill of every stage has been consumed, so no copy into this CTA and no MMA
+      // arrival on its barriers is still in flight when the cluster leaves.
+      for (int i = 0; i < P_STAGES && !s_abort; ++i) {
+        if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 5u)) break;
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_count = 0;
+      for (int t = static_cast<int>(cluster_id); t < units && !s_abort; t += static_cast<int>(nclusters)) {
+        for (int c = 0; c < nchunk && !s_abort; ++c) {
+          const uint32_t b = acc_count & 1u;
+          const uint32_t use = acc_count >> 1;
+          if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * TC_BN;
+          const int kb_end = min(nkb, (c + 1) * TC_KB_PER_CHUNK);
+          bool ok = true;
+          for (int kb = c * TC_KB_PER_CHUNK; kb < kb_end; ++kb) {
+            if (!mbar_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = stage_base + stage * P_STAGE_BYTES;
+            const uint64_t adesc = smem_desc_sw128(sa);
+            const uint64_t bdesc = smem_desc_sw128(sa + P_HALF_BYTES);
+#pragma unroll
+            for (int k = 0; k < TC_BK / 16; ++k)
+              tc_mma_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdescPair,
+                          (kb > c * TC_KB_PER_CHUNK || k > 0) ? 1u : 0u);
+            tc_commit_pair_mc(smem_u32(&bar_empty[stage]), TC_PAIR_MASK);  // frees the stage in both CTAs
+            if (++stage == P_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          tc_commit_pair_mc(smem_u32(&bar_accf[b]), TC_PAIR_MASK);
+          ++acc_count;
+          if (!ok) break;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r_loc = 32 * q + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    uint32_t acc_count = 0;
+    for (int t = static_cast<int>(cluster_id); t < units && !s_abort; t += static_cast<int>(nclusters)) {
+      int mb, nb;
+      tile_of(t, mb, nb);
+      int sums[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sums[i] = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunk; ++c) {
+        const uint32_t b = acc_count & 1u;
+        const uint32_t use = acc_count >> 1;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(smem_u32(&bar_accf[b]), use & 1u, &s_abort, a.status, 4u) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col0 = b * TC_BN + half * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + col0 + 32 * j, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sums[32 * j + i] += __float2int_rn(__uint_as_float(v[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(smem_cluster_addr(smem_u32(&bar_acce[b]), 0));
+        ++acc_count;
+      }
+      if (!ok) break;
+      const int64_t m0 = static_cast<int64_t>(mb) * P_BM + static_cast<int64_t>(rank) * P_HALF;
+      const int64_t n_base = static_cast<int64_t>(nb) * TC_BN + half * 128;
+      if (m0 + r_loc < M && n_base < N) store_row<MODE>(a, 0, m0 + r_loc, n_base, sums);
+    }
+  }
+
+  // ---- teardown (as in the single-CTA kernel), then the pair leaves together.
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 20000000ull) {
+    }
+  }
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TC_TMEM_COLS)
                  : "memory");
   }
 }
@@ -405,10 +698,12 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 cudaError_t launch_tc_mode(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int grid, size_t smem,
                            cudaStream_t stream) {
-  auto k = tc_gemm_kernel<MODE>;
+  void (*k)(CUtensorMap, CUtensorMap, GemmArgs);
+  if constexpr (PAIR) k = tc_pair_gemm_kernel<MODE>;
+  else k = tc_gemm_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   k<<<grid, TC_THREADS, smem, stream>>>(ma, mb, a);
@@ -417,22 +712,38 @@ cudaError_t launch_tc_mode(const CUtensorMap& ma, const CUtensorMap& mb, const G
 
 }  // namespace
 
-int64_t tc_upper_tiles(int64_t E, int64_t R, int64_t N, bool grouped) {
-  return ((R + TC_BM - 1) / TC_BM + (grouped ? E : 0)) * ((N + TC_BN - 1) / TC_BN);
+// Upper bound on the kernel's work units (tile pairs): every unit holds at
+// least one tile with rows, except the second n-block of a pair past an odd NB.
+static int64_t tc_upper_units(int64_t E, int64_t R, int64_t N, bool grouped) {
+  const int64_t nb = (N + TC_BN - 1) / TC_BN;
+  return ((R + TC_BM - 1) / TC_BM + (grouped ? E : 0)) * ((nb + 1) / 2 + 1);
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, a_f16, a.R, a.K, TC_BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b_f16, a.E * a.N, a.K, TC_BN)) return cudaErrorInvalidValue;
-  const int64_t ub = tc_upper_tiles(a.E, a.R, a.N, a.group_list != nullptr);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ub, num_sms)));
+  if (a.group_list == nullptr && a.E == 1 && a.mode != EPI_SWIGLU) {
+    // Dense: 256-row tiles on CTA pairs.
+    if (!make_map(&ma, a_f16, a.R, a.K, P_HALF)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, b_f16, a.N, a.K, P_HALF)) return cudaErrorInvalidValue;
+    const int64_t units = ((a.R + P_BM - 1) / P_BM) * ((a.N + TC_BN - 1) / TC_BN);
+    const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / TC_CLUSTER));
+    const int grid = static_cast<int>(clusters * TC_CLUSTER);
+    const size_t smem = static_cast<size_t>(P_STAGES) * P_STAGE_BYTES + 1024;
+    if (a.mode == EPI_ACC) return launch_tc_mode<EPI_ACC, true>(ma, mb, a, grid, smem, stream);
+    return launch_tc_mode<EPI_BF16, true>(ma, mb, a, grid, smem, stream);
+  }
+  // Half-tile boxes: one operand of a tile pair is fetched as two halves, one by each CTA.
+  if (!make_map(&ma, a_f16, a.R, a.K, TC_BM / 2)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, b_f16, a.E * a.N, a.K, TC_BN / 2)) return cudaErrorInvalidValue;
+  const int64_t units = tc_upper_units(a.E, a.R, a.N, a.group_list != nullptr);
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / TC_CLUSTER));
+  const int grid = static_cast<int>(clusters * TC_CLUSTER);
   const size_t smem = static_cast<size_t>(TC_STAGES) * TC_STAGE_BYTES + 1024;
   switch (a.mode) {
-    case EPI_ACC: return launch_tc_mode<EPI_ACC>(ma, mb, a, grid, smem, stream);
-    case EPI_SWIGLU: return launch_tc_mode<EPI_SWIGLU>(ma, mb, a, grid, smem, stream);
-    default: return launch_tc_mode<EPI_BF16>(ma, mb, a, grid, smem, stream);
+    case EPI_ACC: return launch_tc_mode<EPI_ACC, false>(ma, mb, a, grid, smem, stream);
+    case EPI_SWIGLU: return launch_tc_mode<EPI_SWIGLU, false>(ma, mb, a, grid, smem, stream);
+    default: return launch_tc_mode<EPI_BF16, false>(ma, mb, a, grid, smem, stream);
   }
 }
 

@@ -64,7 +64,6 @@ cudaError_t launch_reg_gemm(const GemmArgs& a, const GemmPlan& p, cudaStream_t s
 
 // tcgen05 engine (large M): both operands as integer-valued fp16, K-major.
 // a_f16: [R,K] activations; b_f16: [E*N,K] packed weights (fp16 copy).
-int64_t tc_upper_tiles(int64_t E, int64_t R, int64_t N, bool grouped);
 cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream);
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
