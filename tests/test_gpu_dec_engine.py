@@ -74,3 +74,33 @@ def test_dec_repeated_calls_reuse_the_workspace():
         y = W.w8a8_quant_matmul(dev(q), dev(xs), wp, dev(d.w_scale), d.N, ws=ws)
         assert np.array_equal(host_bits(y), ref)
     assert W.read_device_status(ws) == 0
+
+
+def test_dec_chained_calls_share_buffers():
+    """Quantisation and decode contraction enqueued back to back, every call
+    reusing one code buffer, one scale buffer and one workspace: the launches
+    overlap (each may start while the previous one still runs), yet no kernel
+    touches those buffers before the kernel it depends on has finished, so
+    every output matches the oracle."""
+    M, N, K = 64, 1024, 3584
+    rng = np.random.default_rng(11)
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    wsc = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    xs = [S.to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32) * (1.0 + i)) for i in range(6)]
+    wp = W.w8a8_prepack_weight(dev(w))
+    wsc_d = dev(wsc)
+    xd = [dev_bf16(x) for x in xs]
+    q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    s = torch.empty(M, dtype=torch.float32, device="cuda")
+    ws = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in xs]
+    torch.cuda.synchronize()
+    for x, y in zip(xd, ys):
+        W.w8a8_dynamic_quant(x, q=q, scale=s)
+        W.w8a8_quant_matmul(q, s, wp, wsc_d, N, ws=ws, y=y)
+        assert W.last_engine() == W.ENGINE_DECODE
+    torch.cuda.synchronize()
+    assert W.read_device_status(ws) == 0
+    for x, y in zip(xs, ys):
+        qo, so = oracle.dynamic_quant(x)
+        assert np.array_equal(host_bits(y), oracle.quant_matmul(qo, so, w, wsc, None))

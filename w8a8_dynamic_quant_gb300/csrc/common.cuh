@@ -132,6 +132,15 @@ __device__ __forceinline__ float dequant(int32_t acc, float sx, float sw) {
 
 // ------------------------------------------------------------- PTX helpers --
 
+// Programmatic dependent launch.  pdl_trigger: a kernel launched after this
+// one with programmatic stream serialization may be scheduled from now on (it
+// still waits for this grid before it touches anything this grid reads or
+// writes).  pdl_wait: blocks the calling thread until the grids this one
+// depends on have completed and their writes are visible; returns at once for
+// a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -9,19 +9,26 @@
 // contiguous).  A CTA owns 128 weight rows and a K slice of at most 7 stages
 // of 128.  With one CTA per SM, an SM streams at the HBM rate only with about
 // 100 KB of reads in flight, so one thread issues tensor-copy (TMA) loads of
-// the CTA's WHOLE slice at once: per stage a 128-row x 128-byte weight tile
-// and the 64-token x 128-byte INT8 activation tile of the same K range, both
-// 128-byte swizzled, each stage on its own mbarrier.  When the host made the
-// packed buffer itself (it keeps a record of the packs it wrote), the loads
-// are issued before the header check instead of after it.
-// Eight converter warps take the stages in order: lane r reads weight row r
+// the CTA's WHOLE weight slice at once: per stage a 128-row x 128-byte tile,
+// 128-byte swizzled, on its own mbarrier.  When the host made the packed
+// buffer itself (it keeps a record of the packs it wrote), the loads are
+// issued before the header check instead of after it.
+//
+// Tensor memory (512 columns) holds every weight stage of the slice at once
+// (7 x 64 columns) beside the accumulator (64 columns).  So eight converter
+// warps widen each weight stage as it lands -- lane r reads weight row r
 // (conflict-free thanks to the swizzle), widens it to integer-valued FP16 and
-// stores it into tensor memory, where tcgen05.mma reads its A operand; the
-// activation tile is widened into two 128-byte-swizzled K-major FP16 tiles in
-// shared memory (the B operand).  The MMA is M = 128 weight rows x N = 64
-// tokens x K = 16 into an FP32 TMEM accumulator; the CTA's K slice is at most
-// 896, so the accumulator holds an exact integer (|partial| <= 896 * 127^2
-// < 2^24).
+// stores it into the stage's own A columns -- without waiting for the
+// activations, which the kernel before (the quantisation) may still be
+// writing.  Once that kernel has finished, the MMA thread requests the
+// slice's activation tiles (64 tokens x 128 bytes per stage, TMA, 128-byte
+// swizzled, one mbarrier per stage); the converters widen each into a
+// 128-byte-swizzled K-major FP16 tile in the bytes the int8 weight tiles
+// occupied (the B operand), and each stage's MMAs follow as soon as its tile
+// is ready.  After the activations arrive, only their widening, the MMAs and the
+// reduction remain.  The MMA is M = 128 weight rows x N = 64 tokens x K = 16
+// into an FP32 TMEM accumulator; the CTA's K slice is at most 896, so the
+// accumulator holds an exact integer (|partial| <= 896 * 128^2 < 2^24).
 //
 // Split-K reduction in two steps, neither of which waits on another CTA's
 // progress beyond the cluster barrier: the K splits of a row block form
@@ -34,7 +41,7 @@
 // the dequant epilogue and writes BF16 (or the INT32 sums) and resets the
 // counter.  Integer addition is exact in any order.
 //
-// Warps: 0 TMEM owner + TMA producer + MMA issuer; 1-8 converters (warp w owns
+// Warps: 0 TMEM owner, TMA producer and MMA issuer (lane 0); 1-8 converters (warp w owns
 // TMEM lanes 32*(w%4).. and K part / token part (w-1)/4).  All waits are
 // bounded.
 #include <mutex>
@@ -51,10 +58,8 @@ using namespace tc;
 constexpr int DC_ROWS = 128;  // weight rows per CTA (MMA M)
 constexpr int DC_TOK = 64;    // token columns (MMA N)
 constexpr int DC_BK = 128;    // K per stage
-constexpr int DC_SF = 3;      // fp16 B tiles in shared memory / A stages in TMEM
 constexpr uint32_t DC_B_SUB = DC_TOK * 128;    // one 64-K fp16 sub-tile (8 KB)
 constexpr uint32_t DC_B_BYTES = 2 * DC_B_SUB;  // 128 K of fp16 activations
-constexpr uint32_t DC_RING_BYTES = DC_SF * DC_B_BYTES;
 #ifndef DC_CONV_WARPS_OVERRIDE
 constexpr int DC_CONV_WARPS = 8;
 #else
@@ -66,10 +71,10 @@ constexpr int DC_WCH = 8 / DC_NPART;                 // 16-byte weight chunks pe
 constexpr int DC_XCH = 512 / (32 * DC_CONV_WARPS);   // 16-byte activation chunks per thread per stage
 constexpr int DC_TPW = DC_TOK / DC_NPART;            // accumulator columns (tokens) drained per warp
 static_assert(DC_CONV_WARPS == 8 || DC_CONV_WARPS == 16, "8 or 16 converter warps");
-constexpr uint32_t DC_TMEM_COLS = 256;
-constexpr uint32_t DC_A_COLS = DC_BK / 2;         // 64 columns of fp16 pairs per A stage
-constexpr uint32_t DC_D_COL = DC_SF * DC_A_COLS;  // accumulator columns [192, 256)
-constexpr int DC_MAX_KB = 7;                      // stages per CTA: 896 of K
+constexpr uint32_t DC_TMEM_COLS = 512;
+constexpr uint32_t DC_A_COLS = DC_BK / 2;  // 64 columns of fp16 pairs per A stage
+constexpr int DC_MAX_KB = 7;               // stages per CTA: 896 of K
+constexpr uint32_t DC_D_COL = DC_MAX_KB * DC_A_COLS;  // every A stage resident; accumulator at [448, 512)
 constexpr uint32_t DC_W_STAGE = DC_ROWS * DC_BK;  // int8 weight tile (16 KB)
 constexpr uint32_t DC_X_STAGE = DC_TOK * DC_BK;   // int8 activation tile (8 KB)
 constexpr uint32_t DC_TILE_I32 = DC_TOK * DC_ROWS * 4;  // int32 partial tile (32 KB)
@@ -81,6 +86,7 @@ static_assert(DC_B_BYTES % 1024 == 0 && DC_W_STAGE % 1024 == 0 && DC_X_STAGE % 1
 static_assert(DC_D_COL + DC_TOK <= DC_TMEM_COLS, "tensor memory budget");
 static_assert(DC_MAX_KB * DC_BK * 127 * 127 < (1 << 24), "exact fp32 accumulator");
 static_assert(DC_MAX_KB * DC_W_STAGE >= DC_TILE_I32, "the partial tile reuses the weight tiles");
+static_assert(DC_B_BYTES == DC_W_STAGE, "a stage's fp16 activation tile replaces its int8 weight tile");
 
 // 32 lanes x N consecutive 32-bit TMEM columns (N = 16 or 32).
 template <int N>
@@ -121,25 +127,29 @@ __device__ __forceinline__ void widen16(const uint4& x, uint32_t* h) {
   s8x4_to_f16x4(x.w, h[6], h[7]);
 }
 
-// TMA loads of a CTA's whole K slice of weights (stages [kb0, kb0 + my) of row block rb), one
-// mbarrier per stage that also expects the stage's activation tile.
-__device__ __forceinline__ void issue_weights(const CUtensorMap* wmap, uint64_t* bar_full, uint8_t* wtiles, int kb0,
+// TMA loads of a CTA's whole K slice of weights (stages [kb0, kb0 + my) of row block rb) and of the
+// matching activation tiles, one mbarrier per stage and operand.
+__device__ __forceinline__ void issue_weights(const CUtensorMap* wmap, uint64_t* bar_w, uint8_t* wtiles, int kb0,
                                               int my, int rb) {
   for (int s = 0; s < my; ++s) {
-    const uint32_t fb = smem_u32(&bar_full[s]);
-    mbar_expect_tx(fb, DC_W_STAGE + DC_X_STAGE);
+    const uint32_t fb = smem_u32(&bar_w[s]);
+    mbar_expect_tx(fb, DC_W_STAGE);
     tma_load_2d(smem_u32(wtiles + s * DC_W_STAGE), wmap, (kb0 + s) * DC_BK, rb * DC_ROWS, fb);
   }
 }
-__device__ __forceinline__ void issue_activations(const CUtensorMap* xmap, uint64_t* bar_full, uint8_t* xtiles,
+__device__ __forceinline__ void issue_activations(const CUtensorMap* xmap, uint64_t* bar_x, uint8_t* xtiles,
                                                   int kb0, int my) {
-  for (int s = 0; s < my; ++s)
-    tma_load_2d(smem_u32(xtiles + s * DC_X_STAGE), xmap, (kb0 + s) * DC_BK, 0, smem_u32(&bar_full[s]));
+  for (int s = 0; s < my; ++s) {
+    const uint32_t fb = smem_u32(&bar_x[s]);
+    mbar_expect_tx(fb, DC_X_STAGE);
+    tma_load_2d(smem_u32(xtiles + s * DC_X_STAGE), xmap, (kb0 + s) * DC_BK, 0, fb);
+  }
 }
 // With programmatic stream serialization this kernel may start while the
 // kernel before it (the activation quantisation) still runs: everything that
-// kernel writes -- the int8 codes and the scales -- is read only after this.
-__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// kernel writes -- the int8 codes and the scales -- is read only after
+// pdl_wait, and every global write of this kernel follows that wait (through
+// the activation tiles the whole computation waits for).
 
 // Workspace of the decode engine: per row block and K split a slot for the
 // cluster-summed int32 piece [tokens of the CTA][DC_ROWS], and per row block
@@ -171,9 +181,9 @@ __global__ void __launch_bounds__(DC_THREADS, 1)
 dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtensorMap wmap,
                 const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[DC_MAX_KB];
-  __shared__ __align__(8) uint64_t bar_ready[DC_SF];
-  __shared__ __align__(8) uint64_t bar_emptyf[DC_SF];
+  __shared__ __align__(8) uint64_t bar_w[DC_MAX_KB];      // weight tile of the stage landed
+  __shared__ __align__(8) uint64_t bar_x[DC_MAX_KB];      // activation tile of the stage landed
+  __shared__ __align__(8) uint64_t bar_ready[DC_MAX_KB];  // both operands of the stage widened
   __shared__ __align__(8) uint64_t bar_accf;
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
@@ -196,9 +206,10 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   const int kb1 = static_cast<int>(static_cast<int64_t>(nkb) * (rank + 1) / ksplit);
   const int my = kb1 - kb0;
 
-  uint8_t* ringb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t ringb_base = smem_u32(ringb);
-  uint8_t* wtiles = ringb + DC_RING_BYTES;           // int8 weights [DC_MAX_KB][DC_ROWS][DC_BK], swizzled
+  // int8 weights [DC_MAX_KB][DC_ROWS][DC_BK], swizzled; once every weight stage sits in tensor memory the
+  // same bytes hold the fp16 activation tiles [DC_MAX_KB][2][DC_TOK][64] (the MMA's B operand)
+  uint8_t* wtiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t btiles_base = smem_u32(wtiles);
   uint8_t* xtiles = wtiles + DC_MAX_KB * DC_W_STAGE;  // int8 activations [DC_MAX_KB][DC_TOK][DC_BK], swizzled
   int32_t* ptile = reinterpret_cast<int32_t*>(wtiles);  // int32 partial [DC_TOK][DC_ROWS], after the main loop
 
@@ -207,23 +218,22 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     tma_prefetch_desc(&xmap);
     s_abort = 0;
     s_last = 0;
-    for (int s = 0; s < DC_MAX_KB; ++s) mbar_init(smem_u32(&bar_full[s]), 1);
-    for (int f = 0; f < DC_SF; ++f) {
-      mbar_init(smem_u32(&bar_ready[f]), DC_CONV_WARPS);
-      mbar_init(smem_u32(&bar_emptyf[f]), 1);
+    for (int s = 0; s < DC_MAX_KB; ++s) {
+      mbar_init(smem_u32(&bar_w[s]), 1);
+      mbar_init(smem_u32(&bar_x[s]), 1);
+      mbar_init(smem_u32(&bar_ready[s]), DC_CONV_WARPS);
     }
     mbar_init(smem_u32(&bar_accf), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (a.pack_known) issue_weights(&wmap, bar_full, wtiles, kb0, my, rb);
+    if (a.pack_known) issue_weights(&wmap, bar_w, wtiles, kb0, my, rb);
   }
+  // The next kernel on the stream may be scheduled now: it waits for this grid before it touches memory
+  // this grid uses, and its own prologue (a following contraction's weight stream) overlaps this one's tail.
+  pdl_trigger();
   const PackedHeader* hdr = static_cast<const PackedHeader*>(a.packed);
   const bool run = hdr->magic == kPackMagic && hdr->version == kPackVersion && hdr->E == 1 && hdr->N == N &&
                    hdr->K == K && (hdr->flags & W8A8_PACK_GATE_UP) == 0u;
-  if (tid == 0 && run && !a.pack_known) issue_weights(&wmap, bar_full, wtiles, kb0, my, rb);
-  if (tid == 32 && run) {  // a second issuing thread, so the weight stream never waits for the previous grid
-    wait_prior_grid();
-    issue_activations(&xmap, bar_full, xtiles, kb0, my);
-  }
+  if (tid == 0 && run && !a.pack_known) issue_weights(&wmap, bar_w, wtiles, kb0, my, rb);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
                  "r"(DC_TMEM_COLS)
@@ -237,21 +247,22 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   if (!run && tid == 0 && rank == 0 && rb == 0) set_status(a.status, W8A8_ERR_PACKED, 0u);
 
   if (run && warp == 0) {
-    // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // activations: the previous grid writes them, so they are requested only after it has finished (the
+      // MMAs need them first of all, so their issuer requests them)
+      pdl_wait();
+      issue_activations(&xmap, bar_x, xtiles, kb0, my);
+      // ----------------------------------------------------------- MMA issuer
       for (int i = 0; i < my && !s_abort; ++i) {
-        const int f = i % DC_SF;
-        const uint32_t ph = static_cast<uint32_t>(i / DC_SF) & 1u;
-        if (!mbar_wait(smem_u32(&bar_ready[f]), ph, &s_abort, a.status, 12u)) break;
+        if (!mbar_wait(smem_u32(&bar_ready[i]), 0u, &s_abort, a.status, 12u)) break;
         tc_fence_after();
-        const uint32_t bsub0 = ringb_base + f * DC_B_BYTES;
+        const uint32_t bsub0 = btiles_base + i * DC_B_BYTES;
 #pragma unroll
         for (int kk = 0; kk < DC_BK / 16; ++kk) {
           const uint64_t bdesc = smem_desc_sw128(bsub0 + (kk >> 2) * DC_B_SUB) + 2u * (kk & 3);
-          tc_mma_tmem_a(tmem_base + DC_D_COL, tmem_base + f * DC_A_COLS + 8u * kk, bdesc, kIdescDec,
+          tc_mma_tmem_a(tmem_base + DC_D_COL, tmem_base + i * DC_A_COLS + 8u * kk, bdesc, kIdescDec,
                         (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&bar_emptyf[f]));
       }
       tc_commit(smem_u32(&bar_accf));
     }
@@ -260,43 +271,45 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     const int q = warp & 3;           // TMEM lane quadrant
     const int part = (warp - 1) >> 2;  // K part of each stage (chunks DC_WCH*part..) / token part
     const int row = 32 * q + lane;    // weight row inside the block == TMEM lane
-    if (MODE != EPI_ACC) {
-      // epilogue inputs into shared memory while the first stage is still in flight; the token
-      // scales come from the previous grid
-      if (ct < DC_ROWS) {
-        const int64_t n = static_cast<int64_t>(rb) * DC_ROWS + ct;
-        s_sw[ct] = n < N ? a.w_scale[n] : 0.0f;
-        s_bias[ct] = (a.bias != nullptr && n < N) ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
-      } else if (ct < DC_ROWS + DC_TOK) {
-        wait_prior_grid();
-        s_sx[ct - DC_ROWS] = ct - DC_ROWS < M ? a.x_scale[ct - DC_ROWS] : 0.0f;
-      }
+    if (MODE != EPI_ACC && ct < DC_ROWS) {  // epilogue inputs of the row block, while the weights stream
+      const int64_t n = static_cast<int64_t>(rb) * DC_ROWS + ct;
+      s_sw[ct] = n < N ? a.w_scale[n] : 0.0f;
+      s_bias[ct] = (a.bias != nullptr && n < N) ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
     }
+    // Weights: every stage of the slice is widened into its own tensor-memory A stage as it lands,
+    // independent of the activations (which the previous grid may still be writing).
     bool ok = true;
     for (int i = 0; i < my && ok; ++i) {
-      const int f = i % DC_SF;
-      const uint32_t phf = static_cast<uint32_t>(i / DC_SF) & 1u;
-      int got = 1;
-      if (i >= DC_SF) {  // a fresh slot needs no wait
-        if (lane == 0) got = mbar_wait(smem_u32(&bar_emptyf[f]), phf ^ 1u, &s_abort, a.status, 15u) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-      }
       // every lane observes the completed load of stage i itself
-      if (got) got = mbar_wait(smem_u32(&bar_full[i]), 0u, &s_abort, a.status, 13u) ? 1 : 0;
+      const int got = mbar_wait(smem_u32(&bar_w[i]), 0u, &s_abort, a.status, 13u) ? 1 : 0;
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
-      // weights first: their tensor-memory store runs while the activations are widened
       uint32_t v[8 * DC_WCH];
       const uint8_t* wst = wtiles + i * DC_W_STAGE + row * DC_BK;
 #pragma unroll
       for (int c = 0; c < DC_WCH; ++c)
         widen16(*reinterpret_cast<const uint4*>(wst + (((DC_WCH * part + c) ^ (row & 7)) << 4)), &v[8 * c]);
-      tmem_st_cols<8 * DC_WCH>(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + f * DC_A_COLS +
+      tmem_st_cols<8 * DC_WCH>(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + i * DC_A_COLS +
                                    static_cast<uint32_t>(8 * DC_WCH * part),
                                v);
-      uint8_t* bt = ringb + f * DC_B_BYTES;
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    // every converter is done reading the int8 weight tiles: their bytes now take the fp16 activations
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * DC_CONV_WARPS) : "memory");
+    if (MODE != EPI_ACC && ct >= DC_ROWS && ct < DC_ROWS + DC_TOK) {  // token scales: the previous grid's output
+      pdl_wait();
+      s_sx[ct - DC_ROWS] = ct - DC_ROWS < M ? a.x_scale[ct - DC_ROWS] : 0.0f;
+    }
+    for (int i = 0; i < my && ok; ++i) {
+      const int got = mbar_wait(smem_u32(&bar_x[i]), 0u, &s_abort, a.status, 16u) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      uint8_t* bt = wtiles + i * DC_B_BYTES;
       const uint8_t* xst = xtiles + i * DC_X_STAGE;
 #pragma unroll
       for (int jj = 0; jj < DC_XCH; ++jj) {
@@ -309,15 +322,13 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
         *reinterpret_cast<uint4*>(brow + ((cc ^ (t & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
         *reinterpret_cast<uint4*>(brow + (((cc + 1) ^ (t & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
       }
-      tmem_wait_st();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_ready[f]));
+      if (lane == 0) mbar_arrive(smem_u32(&bar_ready[i]));
     }
     // exact partial -> shared memory, token-major; this warp drains tokens
-    // [DC_TPW*part, DC_TPW*(part+1)).  Once the last MMA has completed every converter warp is past its
-    // last stage, so the weight tiles are free to hold the partial.
+    // [DC_TPW*part, DC_TPW*(part+1)).  Once the last MMA has completed, the activation tiles (in the
+    // weight tiles' bytes) are free to hold the partial.
     int got = 1;
     if (my > 0) {
       if (lane == 0) got = mbar_wait(smem_u32(&bar_accf), 0u, &s_abort, a.status, 14u) ? 1 : 0;
@@ -473,8 +484,10 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   }
 }
 
-constexpr size_t kDecSmem = DC_RING_BYTES + static_cast<size_t>(DC_MAX_KB) * (DC_W_STAGE + DC_X_STAGE) + 1024;
-static_assert(kDecSmem <= 227 * 1024, "shared memory budget");
+// Weight and activation tiles: more than half of the SM's shared memory, which keeps a CTA (it holds all
+// 512 tensor-memory columns) alone on its SM (a second one would stall in its allocation).
+constexpr size_t kDecSmem = static_cast<size_t>(DC_MAX_KB) * (DC_W_STAGE + DC_X_STAGE) + 1024;
+static_assert(kDecSmem > 114 * 1024 && kDecSmem <= 227 * 1024, "shared memory budget");
 
 void dec_set_attributes() {
   for (auto k : {dec_gemm_kernel<EPI_BF16>, dec_gemm_kernel<EPI_ACC>}) {
@@ -526,8 +539,8 @@ cudaError_t launch_dec_mode(const GemmArgs& a, const DecWs& ws, const CUtensorMa
   attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit < DC_CLUSTER ? ksplit : DC_CLUSTER);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // may start before the previous kernel on the stream ends, if that kernel allows it (only the
-  // activation quantisation does); the kernel waits for it before reading what it wrote
+  // may start before the previous kernel on the stream ends, if that kernel allows it (the activation
+  // quantisation and this kernel do); the kernel waits for it before reading what it wrote
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;

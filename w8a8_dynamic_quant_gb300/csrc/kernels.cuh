@@ -68,7 +68,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
 // tcgen05 decode engine (dense, M <= 64): int8 weights widened into TMEM, K
-// split over CTAs whose partials are bulk-added into the workspace.
+// split over clusters of CTAs whose partials meet in distributed shared memory
+// and, across clusters, in workspace slots.
 // dec_plan_ksplit returns 0 when the shape does not suit it.
 size_t dec_ws_bytes(int64_t N);
 int dec_plan_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);

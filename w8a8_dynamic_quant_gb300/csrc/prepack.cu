@@ -60,6 +60,11 @@ __global__ void __launch_bounds__(256) prepack_kernel(const int8_t* __restrict__
     hd.f16_offset = f16_off;
     *reinterpret_cast<PackedHeader*>(packed) = hd;
   }
+  // A contraction launched right after this kernel with programmatic stream
+  // serialization reads the packed weights before it waits for this grid.
+  // This kernel never lets its dependents start early, so they start only
+  // after every CTA has exited; each CTA's writes are made visible first.
+  __threadfence();
 }
 
 }  // namespace

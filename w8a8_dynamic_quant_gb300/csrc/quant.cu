@@ -105,11 +105,16 @@ __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_
   }
 }
 
-// Lets a kernel launched after this one with programmatic stream serialization
-// (the decode contraction) start its prologue -- and its weight stream, which
-// reads nothing this kernel writes -- while this kernel still runs; that kernel
-// waits (griddepcontrol.wait) before it reads the codes or scales written here.
-__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Every quantisation kernel is launched with programmatic stream serialization
+// and opens with pdl_enter: it lets the kernel after it (the decode
+// contraction, whose weight stream reads nothing written here) start its
+// prologue at once, and it waits for the kernel before it -- which may still
+// read the codes and scales this launch overwrites -- before its first access
+// to global memory.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_trigger();
+  pdl_wait();
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -122,7 +127,7 @@ template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
                                                        int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                        float* __restrict__ scale) {
-  allow_dependent_launch();
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = K / 8;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
@@ -157,7 +162,7 @@ template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                       float* __restrict__ scale) {
-  allow_dependent_launch();
+  pdl_enter();
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
@@ -196,7 +201,7 @@ template <int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __restrict__ x, int64_t M,
                                                           int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                           float* __restrict__ scale) {
-  allow_dependent_launch();
+  pdl_enter();
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
@@ -219,6 +224,21 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
   }
 }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 g, dim3 b, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = g;
+  cfg.blockDim = b;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 template <int OUT>
 cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale,
                            cudaStream_t stream, int num_sms) {
@@ -230,20 +250,19 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
     const int ch = static_cast<int>((nchunk + 31) / 32);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 1) quant_warp_rows<1, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
-    else if (ch <= 2) quant_warp_rows<2, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
-    else if (ch <= 4) quant_warp_rows<4, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
-    else quant_warp_rows<8, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    else return launch_pdl(quant_warp_rows<8, OUT>, g, b, stream, x, M, K, q, q16, scale);
   } else {
     const int64_t blocks = std::min<int64_t>(M, max_grid);
     const int ch = static_cast<int>((nchunk + 255) / 256);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 2) quant_cta_rows<2, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
-    else if (ch <= 4) quant_cta_rows<4, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
-    else if (ch <= 8) quant_cta_rows<8, OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
-    else quant_cta_rows_any<OUT><<<g, b, 0, stream>>>(x, M, K, q, q16, scale);
+    if (ch <= 2) return launch_pdl(quant_cta_rows<2, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    else if (ch <= 4) return launch_pdl(quant_cta_rows<4, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    else if (ch <= 8) return launch_pdl(quant_cta_rows<8, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    else return launch_pdl(quant_cta_rows_any<OUT>, g, b, stream, x, M, K, q, q16, scale);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
