@@ -18,59 +18,70 @@ namespace w8a8 {
 
 namespace {
 
+// max |x| over 8 bf16 (two per 32-bit word): sign bits cleared, then packed bf16 maxima; the larger
+// half of the result, widened to binary32 (exact).
 __device__ __forceinline__ float absmax8(const uint4& v) {
+  uint32_t m01, m23, m;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m01) : "r"(v.x & 0x7fff7fffu), "r"(v.y & 0x7fff7fffu));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m23) : "r"(v.z & 0x7fff7fffu), "r"(v.w & 0x7fff7fffu));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+}
+
+// y + 1.5 * 2^23 rounds y (|y| < 2^22) to an integer, ties to even, held in the low mantissa bits: the
+// sum's low byte is the two's-complement int8 code and (sum - 1.5 * 2^23) the code as a float.
+constexpr float kRoundMagic = 12582912.0f;
+
+// The 8 codes of a chunk of 8 bf16 (x[e] = element e), as sums m[e] = code + kRoundMagic.
+// rint(x / s) with the quotient rounded to binary32 first (round half to even), clamped to +-127;
+// s > 0 and rs = the binary32 reciprocal of s, or s = rs = 0 (an all-zero row: every code 0).  y = x * rs is within |x / s| * 2^-23 + 2^-18 <= 2^-15 of
+// the correctly rounded quotient (|x / s| <= 128), so when y is more than 2^-14 from the nearest
+// half-integer both lie strictly inside the same rounding interval and round to the same integer, with
+// |code| <= 127 (|y| <= 127 * (1 + 2^-22)); otherwise (rare), and for non-finite y, the whole chunk
+// takes the quotient itself and the clamp.
+__device__ __forceinline__ void codes8(const uint4& v, float s, float rs, float (&m)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float m = 0.0f;
+  float x[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
-    m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
-  return m;
-}
-
-// rint(x / s) with the quotient rounded to binary32 first (round half to even), clamped to +-127;
-// s > 0, rs = the binary32 reciprocal of s.  y = x * rs is within |x / s| * 2^-23 + 2^-18 <= 2^-15 of
-// the correctly rounded quotient (|x / s| <= 128), so when y is more than 2^-14 from the nearest
-// half-integer both lie strictly inside the same rounding interval and round to the same integer;
-// otherwise (rare), and for non-finite y, the quotient itself is computed.
-__device__ __forceinline__ int q1(float xf, float s, float rs) {
-  const float y = __fmul_rn(xf, rs);
-  const float frac = __fsub_rn(y, floorf(y));  // exact for |y| < 2^23
-  const int r = fabsf(frac - 0.5f) > 0x1p-14f ? __float2int_rn(y) : __float2int_rn(__fdiv_rn(xf, s));
-  return max(-127, min(127, r));
-}
-
-// 8 bf16 -> 8 int8 packed in a uint2.
-__device__ __forceinline__ uint2 quant8(const uint4& v, float s, float rs) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[2] = {0u, 0u};
-  if (s > 0.0f) {
+  float dmax = 0.0f;  // max |y - rint(y)| over the chunk; NaN if any y is not finite
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int lo = q1(__uint_as_float(w[i] << 16), s, rs);
-      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s, rs);
-      const uint32_t pair = (static_cast<uint32_t>(lo) & 0xffu) | ((static_cast<uint32_t>(hi) & 0xffu) << 8);
-      out[i >> 1] |= pair << ((i & 1) * 16);
+  for (int e = 0; e < 8; ++e) {
+    const float y = __fmul_rn(x[e], rs);
+    m[e] = __fadd_rn(y, kRoundMagic);
+    const float t = __fsub_rn(y, __fsub_rn(m[e], kRoundMagic));  // y - rint(y), exact
+    asm("max.NaN.f32 %0, %0, %1;" : "+f"(dmax) : "f"(fabsf(t)));
+  }
+  if (__builtin_expect(!(dmax < 0.5f - 0x1p-14f), 0)) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int r = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], s))));
+      m[e] = __fadd_rn(static_cast<float>(r), kRoundMagic);
     }
   }
-  return make_uint2(out[0], out[1]);
 }
 
-// 8 bf16 -> 8 integer-valued fp16 (same codes as quant8) packed in a uint4.
-__device__ __forceinline__ uint4 quant8_f16(const uint4& v, float s, float rs) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[4] = {0u, 0u, 0u, 0u};
-  if (s > 0.0f) {
+// int8 codes of a chunk (low bytes of the sums) packed in a uint2.
+__device__ __forceinline__ uint2 pack_i8(const float (&m)[8]) {
+  uint32_t u[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int lo = q1(__uint_as_float(w[i] << 16), s, rs);
-      const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s, rs);
-      out[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
-               (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
-    }
-  }
-  return make_uint4(out[0], out[1], out[2], out[3]);
+  for (int e = 0; e < 8; ++e) u[e] = __float_as_uint(m[e]);
+  return make_uint2(__byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410),
+                    __byte_perm(__byte_perm(u[4], u[5], 0x0040), __byte_perm(u[6], u[7], 0x0040), 0x5410));
+}
+
+// the codes as integer-valued fp16 (exact) packed in a uint4.
+__device__ __forceinline__ uint4 pack_f16(const float (&m)[8]) {
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+        : "=r"(h[i])
+        : "f"(__fsub_rn(m[2 * i + 1], kRoundMagic)), "f"(__fsub_rn(m[2 * i], kRoundMagic)));
+  return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
@@ -81,28 +92,13 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
 }
 
 // OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both (each code computed once).
+// s = rs = 0 (an all-zero row) gives zero codes.
 __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_t row, int64_t K, int64_t idx,
                                        void* q, uint16_t* q16, int out) {
-  if (out == 0) {
-    reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = quant8(v, s, rs);
-  } else if (out == 1) {
-    reinterpret_cast<uint4*>(q16 + row * K)[idx] = quant8_f16(v, s, rs);
-  } else {
-    uint32_t b[4] = {0u, 0u, 0u, 0u}, h[4] = {0u, 0u, 0u, 0u};  // byte pairs / fp16 pairs of v.x .. v.w
-    if (s > 0.0f) {
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int lo = q1(__uint_as_float(w[i] << 16), s, rs);
-        const int hi = q1(__uint_as_float(w[i] & 0xffff0000u), s, rs);
-        b[i] = (static_cast<uint32_t>(lo) & 0xffu) | ((static_cast<uint32_t>(hi) & 0xffu) << 8);
-        h[i] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
-               (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
-      }
-    }
-    reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
-    reinterpret_cast<uint4*>(q16 + row * K)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
-  }
+  float m[8];
+  codes8(v, s, rs, m);
+  if (out != 1) reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = pack_i8(m);
+  if (out != 0) reinterpret_cast<uint4*>(q16 + row * K)[idx] = pack_f16(m);
 }
 
 // Every quantisation kernel is launched with programmatic stream serialization
@@ -122,9 +118,10 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).
+// One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).  At least four CTAs (32 warps, 32 rows of
+// loads in flight) per SM.
 template <int CH, int OUT>
-__global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
+__global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
                                                        int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                        float* __restrict__ scale) {
   pdl_enter();
@@ -157,42 +154,50 @@ __global__ void __launch_bounds__(256) quant_warp_rows(const uint16_t* __restric
   }
 }
 
-// One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).
+// One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).  A CTA takes rows
+// blockIdx.x, + gridDim.x, ...; the loads of its next row are issued before the current one is reduced
+// and quantised, so an SM keeps reading while it computes.
 template <int CH, int OUT>
 __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                       float* __restrict__ scale) {
   pdl_enter();
-  __shared__ float red[8];
+  __shared__ float red[2][8];
   const int64_t nchunk = K / 8;
-  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+  uint4 v[CH];
+  auto load_row = [&](int64_t row, uint4 (&dst)[CH]) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
-    uint4 v[CH];
 #pragma unroll
     for (int c = 0; c < CH; ++c) {  // every load of the row in flight before any is used
       const int64_t idx = threadIdx.x + 256 * c;
-      v[c] = idx < nchunk ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+      dst[c] = (row < M && idx < nchunk) ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
     }
+  };
+  load_row(blockIdx.x, v);
+  int buf = 0;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    uint4 vn[CH];
+    load_row(row + gridDim.x, vn);
     float amax = 0.0f;
 #pragma unroll
     for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
     amax = warp_max(amax);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
-    __syncthreads();
-    amax = red[0];
+    if ((threadIdx.x & 31) == 0) red[buf][threadIdx.x >> 5] = amax;
+    __syncthreads();  // (red[buf] was last read two rows ago, before the previous barrier)
+    amax = red[buf][0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[buf][w]);
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
     if (threadIdx.x == 0) scale[row] = s;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = threadIdx.x + 256 * c;
-      if (idx < nchunk) {
-        store8(v[c], s, rs, row, K, idx, q, q16, OUT);
-      }
+      if (idx < nchunk) store8(v[c], s, rs, row, K, idx, q, q16, OUT);
     }
-    __syncthreads();  // red[] is reused by the next row
+#pragma unroll
+    for (int c = 0; c < CH; ++c) v[c] = vn[c];
+    buf ^= 1;
   }
 }
 
@@ -239,6 +244,21 @@ cudaError_t launch_pdl(void (*k)(KArgs...), dim3 g, dim3 b, cudaStream_t stream,
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
+// CTAs of quant_cta_rows<CH, OUT> resident per SM (queried once).
+template <int CH, int OUT>
+int cta_rows_per_sm() {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_cta_rows<CH, OUT>, 256, 0) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    per_sm = n;
+  }
+  return per_sm;
+}
+
 template <int OUT>
 cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale,
                            cudaStream_t stream, int num_sms) {
@@ -255,13 +275,17 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT>, g, b, stream, x, M, K, q, q16, scale);
     else return launch_pdl(quant_warp_rows<8, OUT>, g, b, stream, x, M, K, q, q16, scale);
   } else {
-    const int64_t blocks = std::min<int64_t>(M, max_grid);
+    // as many CTAs as are resident at once; each then works through its rows
     const int ch = static_cast<int>((nchunk + 255) / 256);
-    dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 2) return launch_pdl(quant_cta_rows<2, OUT>, g, b, stream, x, M, K, q, q16, scale);
-    else if (ch <= 4) return launch_pdl(quant_cta_rows<4, OUT>, g, b, stream, x, M, K, q, q16, scale);
-    else if (ch <= 8) return launch_pdl(quant_cta_rows<8, OUT>, g, b, stream, x, M, K, q, q16, scale);
-    else return launch_pdl(quant_cta_rows_any<OUT>, g, b, stream, x, M, K, q, q16, scale);
+    dim3 b(256);
+    auto grid = [&](int per_sm) {
+      return dim3(static_cast<unsigned>(std::min<int64_t>(M, static_cast<int64_t>(num_sms) * per_sm)));
+    };
+    if (ch <= 2) return launch_pdl(quant_cta_rows<2, OUT>, grid(cta_rows_per_sm<2, OUT>()), b, stream, x, M, K, q, q16, scale);
+    if (ch <= 4) return launch_pdl(quant_cta_rows<4, OUT>, grid(cta_rows_per_sm<4, OUT>()), b, stream, x, M, K, q, q16, scale);
+    if (ch <= 8) return launch_pdl(quant_cta_rows<8, OUT>, grid(cta_rows_per_sm<8, OUT>()), b, stream, x, M, K, q, q16, scale);
+    const dim3 g(static_cast<unsigned>(std::min<int64_t>(M, max_grid)));
+    return launch_pdl(quant_cta_rows_any<OUT>, g, b, stream, x, M, K, q, q16, scale);
   }
 }
 
