@@ -110,6 +110,12 @@ reg_gemm_kernel(const GemmArgs a, const int ksplit) {
   const int64_t K = a.K;
   const int NB = static_cast<int>((N + T::BNW - 1) / T::BNW);
 
+  // Launched with programmatic stream serialization: the next kernel may be scheduled now, and this one
+  // touches memory only once the kernel before it (which may write the activations, the scales or the
+  // group list) has finished.
+  pdl_trigger();
+  pdl_wait();
+
   // ---- the packed weight must match the call
   if (tid == 0) {
     s_bad = 0;
@@ -441,24 +447,23 @@ cudaError_t launch_variant(const GemmArgs& a, const GemmPlan& p, cudaStream_t st
   switch (p.variant) {
     case 8: {
       auto k = reg_gemm_kernel<1, 1, 8, 1, MODE>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
-      k<<<p.grid, 256, p.smem, stream>>>(a, p.ksplit);
-      break;
+      if (cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem)))
+        return e;
+      return launch_pdl(k, dim3(p.grid), dim3(256), p.smem, stream, a, p.ksplit);
     }
     case 32: {
       auto k = reg_gemm_kernel<2, 2, 4, 2, MODE>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
-      k<<<p.grid, 256, p.smem, stream>>>(a, p.ksplit);
-      break;
+      if (cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem)))
+        return e;
+      return launch_pdl(k, dim3(p.grid), dim3(256), p.smem, stream, a, p.ksplit);
     }
     default: {
       auto k = reg_gemm_kernel<2, 4, 4, 2, MODE>;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
-      k<<<p.grid, 256, p.smem, stream>>>(a, p.ksplit);
-      break;
+      if (cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem)))
+        return e;
+      return launch_pdl(k, dim3(p.grid), dim3(256), p.smem, stream, a, p.ksplit);
     }
   }
-  return cudaGetLastError();
 }
 
 int bmt_of(int variant) { return variant == 8 ? 8 : variant == 32 ? 32 : 64; }

@@ -229,21 +229,6 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
   }
 }
 
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*k)(KArgs...), dim3 g, dim3 b, cudaStream_t stream, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = g;
-  cfg.blockDim = b;
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, args...);
-}
-
 // CTAs of quant_cta_rows<CH, OUT> resident per SM (queried once).
 template <int CH, int OUT>
 int cta_rows_per_sm() {
@@ -270,10 +255,10 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
     const int ch = static_cast<int>((nchunk + 31) / 32);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT>, g, b, stream, x, M, K, q, q16, scale);
-    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT>, g, b, stream, x, M, K, q, q16, scale);
-    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT>, g, b, stream, x, M, K, q, q16, scale);
-    else return launch_pdl(quant_warp_rows<8, OUT>, g, b, stream, x, M, K, q, q16, scale);
+    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
+    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
+    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
+    else return launch_pdl(quant_warp_rows<8, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
   } else {
     // as many CTAs as are resident at once; each then works through its rows
     const int ch = static_cast<int>((nchunk + 255) / 256);
@@ -281,11 +266,11 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     auto grid = [&](int per_sm) {
       return dim3(static_cast<unsigned>(std::min<int64_t>(M, static_cast<int64_t>(num_sms) * per_sm)));
     };
-    if (ch <= 2) return launch_pdl(quant_cta_rows<2, OUT>, grid(cta_rows_per_sm<2, OUT>()), b, stream, x, M, K, q, q16, scale);
-    if (ch <= 4) return launch_pdl(quant_cta_rows<4, OUT>, grid(cta_rows_per_sm<4, OUT>()), b, stream, x, M, K, q, q16, scale);
-    if (ch <= 8) return launch_pdl(quant_cta_rows<8, OUT>, grid(cta_rows_per_sm<8, OUT>()), b, stream, x, M, K, q, q16, scale);
+    if (ch <= 2) return launch_pdl(quant_cta_rows<2, OUT>, grid(cta_rows_per_sm<2, OUT>()), b, 0, stream, x, M, K, q, q16, scale);
+    if (ch <= 4) return launch_pdl(quant_cta_rows<4, OUT>, grid(cta_rows_per_sm<4, OUT>()), b, 0, stream, x, M, K, q, q16, scale);
+    if (ch <= 8) return launch_pdl(quant_cta_rows<8, OUT>, grid(cta_rows_per_sm<8, OUT>()), b, 0, stream, x, M, K, q, q16, scale);
     const dim3 g(static_cast<unsigned>(std::min<int64_t>(M, max_grid)));
-    return launch_pdl(quant_cta_rows_any<OUT>, g, b, stream, x, M, K, q, q16, scale);
+    return launch_pdl(quant_cta_rows_any<OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
   }
 }
 
