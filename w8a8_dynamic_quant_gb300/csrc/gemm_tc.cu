@@ -70,6 +70,59 @@ using namespace tc;
 
 __device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
 
+// Per-expert row offsets and work-unit prefix sums over the group list (block scans; an absent list is
+// one group of a.R rows): s_row_off[e], s_unit_prefix[e] for e <= E.  A count outside [0, R] flags
+// W8A8_ERR_GROUP_LIST in *s_bad (<< 8); returns the total rows (the caller checks it against R) and the
+// total units in *units_total.
+template <typename UnitsOf>
+__device__ __forceinline__ int scan_groups(const GemmArgs& a, int E, UnitsOf units_of, int* s_row_off,
+                                           int* s_unit_prefix, int* s_warp, int* s_bad, int* units_total) {
+  constexpr int kPer = (kMaxE + TC_THREADS - 1) / TC_THREADS;
+  const int tid = threadIdx.x;
+  int rows_loc = 0, units_loc = 0, neg = 0;
+  int cnts[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid * kPer + i;
+    int64_t c = 0;
+    if (e < E) c = a.group_list ? a.group_list[e] : a.R;
+    if (c < 0 || c > a.R) neg = 1;
+    const int ci = (c < 0 || c > a.R) ? 0 : static_cast<int>(c);
+    cnts[i] = ci;
+    rows_loc += ci;
+    units_loc += units_of(ci);
+  }
+  int rows_total;
+  int row_before = block_exclusive_scan<TC_THREADS>(rows_loc, rows_total, s_warp);
+  int unit_before = block_exclusive_scan<TC_THREADS>(units_loc, *units_total, s_warp);
+  if (neg) atomicOr(s_bad, W8A8_ERR_GROUP_LIST << 8);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid * kPer + i;
+    if (e < E) {
+      s_row_off[e] = row_before;
+      s_unit_prefix[e] = unit_before;
+    }
+    row_before += cnts[i];
+    unit_before += units_of(cnts[i]);
+  }
+  if (tid == 0) {
+    s_row_off[E] = rows_total;
+    s_unit_prefix[E] = *units_total;
+  }
+  return rows_total;
+}
+
+// Expert of work unit t: the last e with s_unit_prefix[e] <= t.
+__device__ __forceinline__ int expert_of(int t, int E, const int* s_unit_prefix) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_unit_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 struct TileInfo {
   int e, mb, nb, cnt;
   int share_a;   // 0: the pair shares the weight block, 1: it shares the activation block
@@ -87,11 +140,7 @@ __host__ __device__ __forceinline__ int pair_units(int cnt, int NB) {
 // of a unit may lie past the expert's n-blocks: it is computed and not stored.
 __device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int* tile_prefix, const int* row_off,
                                                 int rank) {
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_prefix[mid] <= t) lo = mid; else hi = mid;
-  }
+  const int lo = expert_of(t, E, tile_prefix);
   TileInfo ti;
   ti.e = lo;
   const int local = t - tile_prefix[lo];
@@ -252,39 +301,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
-  // ---- per-expert rows and tiles (block scans)
-  constexpr int kPer = (kMaxE + TC_THREADS - 1) / TC_THREADS;
-  int rows_loc = 0, tiles_loc = 0, neg = 0;
-  int cnts[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = tid * kPer + i;
-    int64_t c = 0;
-    if (e < E) c = a.group_list ? a.group_list[e] : a.R;
-    if (c < 0 || c > a.R) neg = 1;
-    const int ci = (c < 0 || c > a.R) ? 0 : static_cast<int>(c);
-    cnts[i] = ci;
-    rows_loc += ci;
-    tiles_loc += pair_units(ci, NB);
-  }
-  int rows_total, tiles_total;
-  int row_before = block_exclusive_scan<TC_THREADS>(rows_loc, rows_total, s_warp);
-  int tile_before = block_exclusive_scan<TC_THREADS>(tiles_loc, tiles_total, s_warp);
-  if (neg) atomicOr(&s_bad, W8A8_ERR_GROUP_LIST << 8);
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = tid * kPer + i;
-    if (e < E) {
-      s_row_off[e] = row_before;
-      s_tile_prefix[e] = tile_before;
-    }
-    row_before += cnts[i];
-    tile_before += pair_units(cnts[i], NB);
-  }
-  if (tid == 0) {
-    s_row_off[E] = rows_total;
-    s_tile_prefix[E] = tiles_total;
-  }
+  // ---- per-expert rows and work units (tile pairs)
+  int tiles_total;
+  const int rows_total = scan_groups(
+      a, E, [NB](int c) { return pair_units(c, NB); }, s_row_off, s_tile_prefix, s_warp, &s_bad, &tiles_total);
   // Both CTAs' barriers are initialised before either sends the other a copy or an arrival.
   tc_fence_before();
   cluster_sync_all();
@@ -449,8 +469,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
-// Dense contraction on CTA pairs (tcgen05 cta_group::2).  One tile is 256
-// rows x 256 columns; the even CTA of the cluster holds rows [0,128) of A and
+// Contraction on CTA pairs (tcgen05 cta_group::2), dense or grouped.  One tile
+// is 256 rows of one expert x 256 columns (the second 128 rows may lie past
+// the expert's rows: computed, not stored); the even CTA of the cluster holds rows [0,128) of A and
 // weight rows [0,128) of B, the odd CTA rows [128,256) and weight rows
 // [128,256), so a stage is 32 KB per CTA and six stages fit (more copies in
 // flight than the four 48 KB stages of the single-CTA tile).  One thread of
@@ -478,15 +499,17 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
   __shared__ int s_bad;
+  __shared__ int s_unit_prefix[kMaxE + 1];
+  __shared__ int s_row_off[kMaxE + 1];
+  __shared__ int s_warp[TC_THREADS / 32];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int64_t M = a.R;
+  const int E = static_cast<int>(a.E);
   const int64_t N = a.N;
   const int64_t K = a.K;
   const int NB = static_cast<int>((N + TC_BN - 1) / TC_BN);
-  const int MB = static_cast<int>((M + P_BM - 1) / P_BM);
   const int nkb = static_cast<int>((K + TC_BK - 1) / TC_BK);
   const int nchunk = (nkb + TC_KB_PER_CHUNK - 1) / TC_KB_PER_CHUNK;
 
@@ -522,18 +545,28 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  // ---- per-expert rows and work units (256-row tiles)
+  int units_total;
+  const int rows_total = scan_groups(
+      a, E, [NB](int c) { return ((c + P_BM - 1) / P_BM) * NB; }, s_row_off, s_unit_prefix, s_warp, &s_bad,
+      &units_total);
   tc_fence_before();
   cluster_sync_all();  // both CTAs' barriers and tensor memory exist before either touches the other's
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
-  const int bad = s_bad;
-  if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, static_cast<uint32_t>(bad), 0u);
-  const int units = bad ? 0 : MB * NB;
+  int bad = s_bad;
+  if (rows_total != a.R) bad |= W8A8_ERR_GROUP_LIST << 8;
+  if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, (bad & 0xff) ? (bad & 0xff) : (bad >> 8), 0u);
+  const int units = bad ? 0 : units_total;
 
-  // Rasterised like the single-CTA kernel: groups of TC_GROUP_N n-blocks, m-block slower.
-  auto tile_of = [&](int t, int& mb, int& nb) {
-    const int g = t / (MB * TC_GROUP_N);
-    const int rem = t - g * MB * TC_GROUP_N;
+  // Unit t -> expert e, 256-row block mb of the expert, n-block nb; rasterised like the single-CTA
+  // kernel: groups of TC_GROUP_N n-blocks, m-block slower.
+  auto tile_of = [&](int t, int& e, int& mb, int& nb) {
+    e = expert_of(t, E, s_unit_prefix);
+    const int local = t - s_unit_prefix[e];
+    const int MB = (s_row_off[e + 1] - s_row_off[e] + P_BM - 1) / P_BM;
+    const int g = local / (MB * TC_GROUP_N);
+    const int rem = local - g * MB * TC_GROUP_N;
     const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
     mb = rem / gn;
     nb = g * TC_GROUP_N + rem % gn;
@@ -545,10 +578,11 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       for (int t = static_cast<int>(cluster_id); t < units && !s_abort; t += static_cast<int>(nclusters)) {
-        int mb, nb;
-        tile_of(t, mb, nb);
-        const int ya = mb * P_BM + static_cast<int>(rank) * P_HALF;
-        const int yb = nb * TC_BN + static_cast<int>(rank) * P_HALF;
+        int e, mb, nb;
+        tile_of(t, e, mb, nb);
+        const int ya = s_row_off[e] + mb * P_BM + static_cast<int>(rank) * P_HALF;
+        const int yb = static_cast<int>(static_cast<int64_t>(e) * N + static_cast<int64_t>(nb) * TC_BN) +
+                       static_cast<int>(rank) * P_HALF;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
           const uint32_t full = smem_u32(&bar_full[stage]);
@@ -621,8 +655,8 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
     uint32_t acc_count = 0;
     for (int t = static_cast<int>(cluster_id); t < units && !s_abort; t += static_cast<int>(nclusters)) {
-      int mb, nb;
-      tile_of(t, mb, nb);
+      int e, mb, nb;
+      tile_of(t, e, mb, nb);
       int sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
@@ -653,9 +687,10 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ++acc_count;
       }
       if (!ok) break;
-      const int64_t m0 = static_cast<int64_t>(mb) * P_BM + static_cast<int64_t>(rank) * P_HALF;
+      const int m0 = mb * P_BM + static_cast<int>(rank) * P_HALF;  // first row of this CTA inside the expert
       const int64_t n_base = static_cast<int64_t>(nb) * TC_BN + half * 128;
-      if (m0 + r_loc < M && n_base < N) store_row<MODE>(a, 0, m0 + r_loc, n_base, sums);
+      if (m0 + r_loc < s_row_off[e + 1] - s_row_off[e] && n_base < N)
+        store_row<MODE>(a, e, static_cast<int64_t>(s_row_off[e]) + m0 + r_loc, n_base, sums);
     }
   }
 
@@ -723,10 +758,13 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f
   if (a.R == 0) return cudaSuccess;
   CUtensorMap ma, mb;
   if (a.group_list == nullptr && a.E == 1 && a.mode != EPI_SWIGLU) {
-    // Dense: 256-row tiles on CTA pairs.
+    // Dense: 256-row tiles on CTA pairs.  (Grouped contractions stay on the single-CTA tiles: an expert
+    // with an odd number of 128-row blocks would leave half a pair tile idle, about 9 % more work on the
+    // MoE prefill layer, which costs more than the deeper pipeline gains.)
     if (!make_map(&ma, a_f16, a.R, a.K, P_HALF)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, b_f16, a.N, a.K, P_HALF)) return cudaErrorInvalidValue;
-    const int64_t units = ((a.R + P_BM - 1) / P_BM) * ((a.N + TC_BN - 1) / TC_BN);
+    if (!make_map(&mb, b_f16, a.E * a.N, a.K, P_HALF)) return cudaErrorInvalidValue;
+    const int64_t units =
+        ((a.R + P_BM - 1) / P_BM + (a.group_list != nullptr ? a.E : 0)) * ((a.N + TC_BN - 1) / TC_BN);
     const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / TC_CLUSTER));
     const int grid = static_cast<int>(clusters * TC_CLUSTER);
     const size_t smem = static_cast<size_t>(P_STAGES) * P_STAGE_BYTES + 1024;
