@@ -69,7 +69,7 @@ KERNEL_SOURCES = {
     "dynamic_quant": ["quant.cu", "common.cuh", "kernels.cuh"],
     "quant_matmul": ["gemm_reg.cu", "gemm_dec.cu", "gemm_tc.cu", "tc_common.cuh", "capi.cu", "common.cuh",
                      "kernels.cuh"],
-    "moe_layer": ["gemm_reg.cu", "gemm_tc.cu", "tc_common.cuh", "quant.cu", "capi.cu", "common.cuh", "kernels.cuh"],
+    "moe_layer": ["gemm_reg.cu", "gemm_tc.cu", "gemm_tcw.cu", "tc_common.cuh", "quant.cu", "capi.cu", "common.cuh", "kernels.cuh"],
 }
 
 

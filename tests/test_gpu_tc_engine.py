@@ -84,7 +84,10 @@ def test_tc_dense_prefill_config_sampled_rows():
 
 @pytest.mark.parametrize("gl,K,N", [([300, 0, 129, 77, 0, 200], 512, 256), ([64] * 8, 1024, 512),
                                     ([0, 0, 1000, 24], 2064, 384), ([385, 0, 129, 1], 576, 768)])
-def test_tc_grouped_exact(gl, K, N):
+@pytest.mark.parametrize("f16_copy", [True, False])
+def test_tc_grouped_exact(gl, K, N, f16_copy):
+    """Grouped contraction on the tensor cores, with the packed fp16 weight copy (fp16 weights by TMA)
+    and without it (int8 weights widened in tensor memory)."""
     rng = np.random.default_rng(sum(gl) + K)
     R, E = int(sum(gl)), len(gl)
     x = S.to_bf16_bits(rng.standard_normal((R, K)).astype(np.float32))
@@ -92,7 +95,7 @@ def test_tc_grouped_exact(gl, K, N):
     w = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
     wsc = rng.uniform(1e-3, 1e-2, (E, N)).astype(np.float32)
     glnp = np.asarray(gl, np.int64)
-    wp = W.w8a8_prepack_weight(dev(w), F16)
+    wp = W.w8a8_prepack_weight(dev(w), F16 if f16_copy else 0)
     ws = W.workspace(W.grouped_matmul_workspace_bytes(E, R, N, K))
     y = torch.full((R, N), 3.0, dtype=torch.bfloat16, device="cuda")
     y = W.w8a8_grouped_matmul(dev(q), dev(xs), dev(glnp), wp, dev(wsc), ws=ws, y=y)
@@ -105,9 +108,10 @@ def test_tc_grouped_exact(gl, K, N):
     assert np.array_equal(host_bits(y), y_ref)
 
 
-def tc_moe(m):
-    w13p = W.w8a8_prepack_weight(m.w13.cuda(), W.PACK_GATE_UP | F16)
-    w2p = W.w8a8_prepack_weight(m.w2.cuda(), F16)
+def tc_moe(m, f16_copy=True):
+    extra = F16 if f16_copy else 0
+    w13p = W.w8a8_prepack_weight(m.w13.cuda(), W.PACK_GATE_UP | extra)
+    w2p = W.w8a8_prepack_weight(m.w2.cuda(), extra)
     x, xs = (dev_bf16(m.x), None) if m.x_scale is None else (dev(m.x), dev(m.x_scale))
     ws = W.workspace(W.moe_workspace_bytes(m.R, m.H, m.I, m.E))
     y = W.moe_w13_swiglu_requant_w2(x, xs, dev(m.group_list), w13p, dev(m.s13), w2p, dev(m.s2), ws=ws)
@@ -126,10 +130,11 @@ def ws_slice(ws, m, which, dtype, shape):
 
 
 @pytest.mark.parametrize("prequant", [False, True])
-def test_tc_moe_small_full(prequant):
+@pytest.mark.parametrize("f16_copy", [True, False])
+def test_tc_moe_small_full(prequant, f16_copy):
     m = S.make_moe(T=256, H=256, I=128, E=4, topk=2, routing="zipf", zipf_s=1.1, n_dead=0,
                    prequant=prequant, seed=21)
-    y, ws = tc_moe(m)
+    y, ws = tc_moe(m, f16_copy)
     y_ref, it = oracle.moe_w13_swiglu_requant_w2(m.x, m.x_scale, m.group_list, m.w13.numpy(), m.s13,
                                                  m.w2.numpy(), m.s2, intermediates=True)
     assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I)), it["h"])
@@ -138,9 +143,10 @@ def test_tc_moe_small_full(prequant):
     assert np.array_equal(y, y_ref)
 
 
-def test_tc_moe_prefill_config_sampled_rows():
+@pytest.mark.parametrize("f16_copy", [True, False])
+def test_tc_moe_prefill_config_sampled_rows(f16_copy):
     m = S.moe_config(4, device="cuda")
-    y, ws = tc_moe(m)
+    y, ws = tc_moe(m, f16_copy)
     rows = sample_rows(m.R, 24, seed=9)
     y_ref, it = moe_subset_oracle(m, rows)
     assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I))[rows], it["h"])

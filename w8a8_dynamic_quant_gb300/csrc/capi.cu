@@ -180,12 +180,19 @@ thread_local int t_last_engine = W8A8_ENGINE_NONE;
 w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream, int sms) {
   bind_ws(a, ws, L);
   a.status = static_cast<DeviceStatus*>(ws);
-  const void* b16 = (L.a16 < L.total) ? pack_f16(a.packed, a.E, a.N, a.K, a.pack_flags) : nullptr;
-  if (b16 != nullptr) {
-    uint16_t* a16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.a16);
+  // the workspace holds an fp16 copy of the codes only for shapes a tensor-core engine takes
+  const bool tc_rows = L.dec > L.a16;
+  uint16_t* a16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.a16);
+  const void* b16 = tc_rows ? pack_f16(a.packed, a.E, a.N, a.K, a.pack_flags) : nullptr;
+  if (b16 != nullptr) {  // the packed fp16 weight copy (dense: CTA pairs; grouped: clusters of two)
     if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
     t_last_engine = W8A8_ENGINE_TC;
     return cuda_status(launch_tc_gemm(a, a16, b16, sms, stream));
+  }
+  if (tc_rows && a.group_list != nullptr) {  // grouped without the fp16 copy: int8 weights widened in TMEM
+    if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
+    t_last_engine = W8A8_ENGINE_TC;
+    return cuda_status(launch_tcw_gemm(a, a16, sms, stream));
   }
   if (a.group_list == nullptr && a.mode != EPI_SWIGLU && L.dec < L.total) {
     const int ks = dec_plan_ksplit(a.R, a.N, a.K, sms);  // dense decode: int8 weights widened in TMEM
@@ -395,9 +402,12 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
   int8_t* hq = reinterpret_cast<int8_t*>(b + L.hq);
   float* hs = reinterpret_cast<float*>(b + L.hs);
-  const void* w13_16 = L.xq16 ? pack_f16(w13_packed, E, 2 * I, H, W8A8_PACK_GATE_UP) : nullptr;
-  const void* w2_16 = L.xq16 ? pack_f16(w2_packed, E, H, I, 0u) : nullptr;
-  const bool tc = w13_16 != nullptr && w2_16 != nullptr;
+  // tensor-core engines for shapes that take them: the packed fp16 weight copies when both packs carry
+  // them, else the int8 weights widened in tensor memory
+  const bool tc = L.xq16 != 0;
+  const void* w13_16 = tc ? pack_f16(w13_packed, E, 2 * I, H, W8A8_PACK_GATE_UP) : nullptr;
+  const void* w2_16 = tc ? pack_f16(w2_packed, E, H, I, 0u) : nullptr;
+  const bool f16w = w13_16 != nullptr && w2_16 != nullptr;
   uint16_t* xq16 = tc ? reinterpret_cast<uint16_t*>(b + L.xq16) : nullptr;
   uint16_t* hq16 = tc ? reinterpret_cast<uint16_t*>(b + L.hq16) : nullptr;
 
@@ -429,7 +439,8 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   a13.mode = EPI_SWIGLU;
   bind_ws(a13, gws, L.g);
   a13.status = static_cast<DeviceStatus*>(ws);
-  const cudaError_t e13 = tc ? launch_tc_gemm(a13, xq16, w13_16, sms, st)
+  const cudaError_t e13 = f16w ? launch_tc_gemm(a13, xq16, w13_16, sms, st)
+                         : tc ? launch_tcw_gemm(a13, xq16, sms, st)
                              : launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st);
   if (e13 != cudaSuccess) return W8A8_ERR_CUDA;
 
@@ -452,7 +463,8 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   a2.mode = EPI_BF16;
   bind_ws(a2, gws, L.g);
   a2.status = static_cast<DeviceStatus*>(ws);
-  const cudaError_t e2 = tc ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
+  const cudaError_t e2 = f16w ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
+                        : tc ? launch_tcw_gemm(a2, hq16, sms, st)
                             : launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st);
   t_last_engine = tc ? W8A8_ENGINE_TC : W8A8_ENGINE_WARP;
   return e2 == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;

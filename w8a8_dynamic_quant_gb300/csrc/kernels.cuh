@@ -65,6 +65,9 @@ cudaError_t launch_reg_gemm(const GemmArgs& a, const GemmPlan& p, cudaStream_t s
 // tcgen05 engine (large M): both operands as integer-valued fp16, K-major.
 // a_f16: [R,K] activations; b_f16: [E*N,K] packed weights (fp16 copy).
 cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream);
+// tcgen05 engine for grouped contractions: int8 weights (the packed payload) widened in TMEM as the A
+// operand, a_f16: [R,K] activations as fp16 (B operand).
+cudaError_t launch_tcw_gemm(const GemmArgs& a, const void* a_f16, int num_sms, cudaStream_t stream);
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
 // tcgen05 decode engine (dense, M <= 64): int8 weights widened into TMEM, K

@@ -5,7 +5,7 @@
 
 #include <cuda.h>
 
-#include "common.cuh"
+#include "kernels.cuh"
 
 namespace w8a8 {
 namespace tc {
@@ -207,6 +207,59 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* s_wa
   __syncthreads();
   total = tot;
   return before + x - v;
+}
+
+// Per-expert row offsets and work-unit prefix sums over the group list (block scans; an absent list is
+// one group of a.R rows): s_row_off[e], s_unit_prefix[e] for e <= E.  A count outside [0, R] flags
+// W8A8_ERR_GROUP_LIST in *s_bad (<< 8); returns the total rows (the caller checks it against R) and the
+// total units in *units_total.
+template <int NT, int MAXE, typename UnitsOf>
+__device__ __forceinline__ int scan_groups(const GemmArgs& a, int E, UnitsOf units_of, int* s_row_off,
+                                           int* s_unit_prefix, int* s_warp, int* s_bad, int* units_total) {
+  constexpr int kPer = (MAXE + NT - 1) / NT;
+  const int tid = threadIdx.x;
+  int rows_loc = 0, units_loc = 0, neg = 0;
+  int cnts[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid * kPer + i;
+    int64_t c = 0;
+    if (e < E) c = a.group_list ? a.group_list[e] : a.R;
+    if (c < 0 || c > a.R) neg = 1;
+    const int ci = (c < 0 || c > a.R) ? 0 : static_cast<int>(c);
+    cnts[i] = ci;
+    rows_loc += ci;
+    units_loc += units_of(ci);
+  }
+  int rows_total;
+  int row_before = block_exclusive_scan<NT>(rows_loc, rows_total, s_warp);
+  int unit_before = block_exclusive_scan<NT>(units_loc, *units_total, s_warp);
+  if (neg) atomicOr(s_bad, W8A8_ERR_GROUP_LIST << 8);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid * kPer + i;
+    if (e < E) {
+      s_row_off[e] = row_before;
+      s_unit_prefix[e] = unit_before;
+    }
+    row_before += cnts[i];
+    unit_before += units_of(cnts[i]);
+  }
+  if (tid == 0) {
+    s_row_off[E] = rows_total;
+    s_unit_prefix[E] = *units_total;
+  }
+  return rows_total;
+}
+
+// Expert of work unit t: the last e with s_unit_prefix[e] <= t.
+__device__ __forceinline__ int expert_of(int t, int E, const int* s_unit_prefix) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_unit_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
 }
 
 // ------------------------------------------------------------ host: TMA maps
