@@ -104,3 +104,24 @@ def test_dec_chained_calls_share_buffers():
     for x, y in zip(xs, ys):
         qo, so = oracle.dynamic_quant(x)
         assert np.array_equal(host_bits(y), oracle.quant_matmul(qo, so, w, wsc, None))
+
+
+def test_dec_small_m_with_fp16_pack_stays_in_workspace():
+    """A dense call with at most 64 rows on weights packed WITH the fp16 copy runs the decode engine
+    and writes nothing past the workspace it was given (its workspace holds no fp16 code copy)."""
+    M, N, K = 64, 256, 7168
+    rng = np.random.default_rng(5)
+    q = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    xs = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    wsc = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    wp = W.w8a8_prepack_weight(dev(w), W.PACK_F16)
+    nbytes = W.quant_matmul_workspace_bytes(M, N, K)
+    guard = 1 << 20
+    buf = torch.zeros(nbytes + guard, dtype=torch.uint8, device="cuda")
+    buf[nbytes:] = 0xA5
+    y = W.w8a8_quant_matmul(dev(q), dev(xs), wp, dev(wsc), N, ws=buf[:nbytes])
+    assert W.last_engine() == W.ENGINE_DECODE
+    torch.cuda.synchronize()
+    assert bool((buf[nbytes:] == 0xA5).all()), "write past the workspace"
+    assert np.array_equal(host_bits(y), oracle.quant_matmul(q, xs, w, wsc, None))
