@@ -1,7 +1,9 @@
-"""GPU parity of the tcgen05 engine (large-M shapes, weights packed with their
-fp16 copy): INT32 accumulators, BF16 outputs and the MoE intermediates must be
-bit-exact against the oracle.  Each test also checks that the engine really
-ran, through the fp16 activation copy it leaves in the workspace."""
+"""GPU parity of the tcgen05 engines (large-M shapes; weights packed with their
+fp16 copy, and for grouped calls also without it, when the int8 weights are
+widened in tensor memory): INT32 accumulators, BF16 outputs and the MoE
+intermediates must be bit-exact against the oracle.  Each test also checks
+that a tcgen05 engine really ran, through the fp16 activation copy it leaves in
+the workspace."""
 import numpy as np
 import pytest
 import torch
@@ -83,7 +85,9 @@ def test_tc_dense_prefill_config_sampled_rows():
 
 
 @pytest.mark.parametrize("gl,K,N", [([300, 0, 129, 77, 0, 200], 512, 256), ([64] * 8, 1024, 512),
-                                    ([0, 0, 1000, 24], 2064, 384), ([385, 0, 129, 1], 576, 768)])
+                                    ([0, 0, 1000, 24], 2064, 384), ([385, 0, 129, 1], 576, 768),
+                                    ([150, 0, 70], 80, 200),
+                                    ([70 + (e * 37) % 90 if e % 7 else 0 for e in range(300)], 64, 128)])
 @pytest.mark.parametrize("f16_copy", [True, False])
 def test_tc_grouped_exact(gl, K, N, f16_copy):
     """Grouped contraction on the tensor cores, with the packed fp16 weight copy (fp16 weights by TMA)
