@@ -69,6 +69,12 @@ def _load(path: str) -> ctypes.CDLL:
     L.oracle_moe_w13_swiglu_requant_w2.argtypes = [
         _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, _vp,
         _vp, _vp, _vp, _vp, _vp, _vp]
+    L.oracle_moe_route.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
+    L.oracle_moe_permute_quant.argtypes = [_vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp,
+                                           _vp, _vp]
+    L.oracle_moe_unpermute_combine.argtypes = [_vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _vp]
+    L.oracle_moe_layer.argtypes = [_vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _vp,
+                                   _vp, _vp, _vp, _vp, _vp]
     return L
 
 
@@ -220,3 +226,78 @@ def moe_w13_swiglu_requant_w2(x, x_scale, group_list, w13, s13, w2, s2, intermed
                _p(inter.get("xq")), _p(inter.get("xs")), _p(inter.get("y13")),
                _p(inter.get("h")), _p(inter.get("hq")), _p(inter.get("hs"))))
     return (y, inter) if intermediates else y
+
+
+def moe_route(topk_ids, E: int):
+    """int64 topk_ids [T,k] -> (int64 group_list [E], int32 pos [T,k]): routed rows ordered by
+    (expert, token, slot); pos[t,j] is the routed row of token t's j-th choice."""
+    ids = _c(topk_ids, np.int64)
+    T, k = ids.shape
+    g = np.empty((E,), np.int64)
+    pos = np.empty((T, k), np.int32)
+    _check("oracle_moe_route", lib().oracle_moe_route(_p(ids), T, k, E, _p(g), _p(pos)))
+    return g, pos
+
+
+def moe_permute_quant(x, x_scale, topk_ids, E: int):
+    """Token rows -> routed rows.  x: bf16 bits [T,H] (x_scale None) or int8 [T,H] with fp32
+    x_scale [T].  Returns (int8 xq [T*k,H], fp32 xs [T*k], int64 group_list [E], int32 pos [T,k])."""
+    ids = _c(topk_ids, np.int64)
+    T, k = ids.shape
+    if x_scale is None:
+        x = _c(x, np.uint16)
+        xs_in = None
+    else:
+        x = _c(x, np.int8)
+        xs_in = _c(x_scale, np.float32)
+    assert x.shape[0] == T
+    H = x.shape[1]
+    xq = np.empty((T * k, H), np.int8)
+    xs = np.empty((T * k,), np.float32)
+    g = np.empty((E,), np.int64)
+    pos = np.empty((T, k), np.int32)
+    _check("oracle_moe_permute_quant", lib().oracle_moe_permute_quant(
+        _p(x), _p(xs_in), _p(ids), T, k, E, H, _p(xq), _p(xs), _p(g), _p(pos)))
+    return xq, xs, g, pos
+
+
+def moe_unpermute_combine(y_routed, pos, topk_weights):
+    """bf16 bits y_routed [T*k,H], int32 pos [T,k], fp32 weights [T,k] -> bf16 bits y [T,H]."""
+    yr = _c(y_routed, np.uint16)
+    pos = _c(pos, np.int32)
+    w = _c(topk_weights, np.float32)
+    T, k = pos.shape
+    assert w.shape == (T, k) and yr.shape[0] == T * k
+    H = yr.shape[1]
+    y = np.empty((T, H), np.uint16)
+    _check("oracle_moe_unpermute_combine",
+           lib().oracle_moe_unpermute_combine(_p(yr), _p(pos), _p(w), T, k, H, _p(y)))
+    return y
+
+
+def moe_layer(x, x_scale, topk_ids, topk_weights, w13, s13, w2, s2, want_routed=False):
+    """Whole MoE layer from token rows: permute + quant -> W13 -> SwiGLU -> requant -> W2 ->
+    weighted combine.  Returns bf16 bits y [T,H] (and the routed W2 output [T*k,H])."""
+    ids = _c(topk_ids, np.int64)
+    w = _c(topk_weights, np.float32)
+    w13 = _c(w13, np.int8)
+    s13 = _c(s13, np.float32)
+    w2 = _c(w2, np.int8)
+    s2 = _c(s2, np.float32)
+    E, twoI, H = w13.shape
+    I = twoI // 2
+    T, k = ids.shape
+    assert w.shape == (T, k) and w2.shape == (E, H, I)
+    if x_scale is None:
+        x = _c(x, np.uint16)
+        xs_in = None
+    else:
+        x = _c(x, np.int8)
+        xs_in = _c(x_scale, np.float32)
+    assert x.shape == (T, H)
+    y = np.empty((T, H), np.uint16)
+    yr = np.empty((T * k, H), np.uint16) if want_routed else None
+    _check("oracle_moe_layer", lib().oracle_moe_layer(
+        _p(x), _p(xs_in), _p(ids), _p(w), T, k, E, H, I, _p(w13), _p(s13), _p(w2), _p(s2), _p(y),
+        _p(yr)))
+    return (y, yr) if want_routed else y

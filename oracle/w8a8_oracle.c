@@ -42,6 +42,8 @@
  *   W2       grouped GEMM with W2 [E,H,I], no bias, BF16 out.
  *   skip     a non-NULL x_scale means x is already INT8 + per-token scale and
  *            is not quantised again.
+ *   route / permute / combine (token rows in, token rows out): see the
+ *            readings above oracle_moe_route at the end of this file.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared
  * (contraction off: no hidden FMA may change a rounding).
@@ -58,6 +60,7 @@
 #define ORC_ERR_SHAPE 2
 #define ORC_ERR_GROUP_LIST 5
 #define ORC_ERR_ALLOC 9
+#define ORC_ERR_TOPK_IDS 10
 
 /* Largest reduction depth for which |acc| <= K * 128 * 127 < 2^31. */
 #define ORC_MAX_K 131072
@@ -360,5 +363,133 @@ done:
   free(h);
   free(hq);
   free(hs);
+  return rc;
+}
+
+/* ------------------------------------------- routing permute and combine -- */
+/*
+ * [P1] §三 (DeepEP INT8 dispatch and the Ascend runner input): the dispatch
+ * turns each token's BF16 hidden row into INT8 + one per-token scale, and the
+ * runner input regroups the routed rows by expert with expert_tokens (rows
+ * per expert) as its group list; topk_ids / topk_weights come with it.
+ *
+ * READING (route): every (token t, slot j) pair of topk_ids [T,k] is one
+ *   routed row; R = T*k.  Rows are ordered by expert, then token, then slot;
+ *   pos[t*k + j] is the routed row of (t, j) and group_list[e] the number of
+ *   pairs naming expert e.  An id outside [0, E) is an error.
+ * READING (permute + quant): a token is quantised once over its H columns
+ *   (the dispatch quantises before it sends) and its codes and scale are
+ *   copied to each of its routed rows; an INT8 token with a scale is copied
+ *   as it is.
+ * READING (combine): y[t, c] = bf16_rne(s), s = 0 then, for j = 0..k-1 in
+ *   order, s = s + w[t,j] * float(y_routed[pos[t,j], c]) with each product
+ *   and sum rounded to binary32 (no FMA); the weights are binary32.
+ */
+int oracle_moe_route(const int64_t* topk_ids, int64_t T, int64_t k, int64_t E,
+                     int64_t* group_list, int32_t* pos) {
+  if (T < 0 || k <= 0 || E <= 0 || T * k > (int64_t)INT32_MAX) return ORC_ERR_SHAPE;
+  const int64_t n = T * k;
+  for (int64_t i = 0; i < n; ++i)
+    if (topk_ids[i] < 0 || topk_ids[i] >= E) return ORC_ERR_TOPK_IDS;
+  int64_t row = 0;
+  for (int64_t e = 0; e < E; ++e) {
+    int64_t cnt = 0;
+    for (int64_t i = 0; i < n; ++i) /* i = t*k + j: token-major, then slot */
+      if (topk_ids[i] == e) {
+        pos[i] = (int32_t)row;
+        ++row;
+        ++cnt;
+      }
+    group_list[e] = cnt;
+  }
+  return ORC_OK;
+}
+
+/* x: BF16 [T,H] (x_scale NULL) or INT8 [T,H] with x_scale [T].
+ * Out: xq [T*k,H] int8, xs [T*k], group_list [E], pos [T*k]. */
+int oracle_moe_permute_quant(const void* x, const float* x_scale, const int64_t* topk_ids,
+                             int64_t T, int64_t k, int64_t E, int64_t H, int8_t* xq, float* xs,
+                             int64_t* group_list, int32_t* pos) {
+  if (H <= 0) return ORC_ERR_SHAPE;
+  int rc = oracle_moe_route(topk_ids, T, k, E, group_list, pos);
+  if (rc) return rc;
+  const size_t t_rows = (size_t)T;
+  int8_t* qt = malloc(t_rows * (size_t)H + 1);
+  float* st = malloc(t_rows * sizeof(float) + 4);
+  rc = ORC_ERR_ALLOC;
+  if (!qt || !st) goto done;
+  if (x_scale == NULL) {
+    rc = oracle_dynamic_quant((const uint16_t*)x, T, H, qt, st);
+    if (rc) goto done;
+  } else {
+    memcpy(qt, x, t_rows * (size_t)H);
+    memcpy(st, x_scale, t_rows * sizeof(float));
+  }
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t r = pos[t * k + j];
+      memcpy(xq + r * H, qt + t * H, (size_t)H);
+      xs[r] = st[t];
+    }
+  rc = ORC_OK;
+done:
+  free(qt);
+  free(st);
+  return rc;
+}
+
+/* y_routed: BF16 [R,H] with R = T*k; pos [T*k]; w fp32 [T*k] -> y BF16 [T,H]. */
+int oracle_moe_unpermute_combine(const uint16_t* y_routed, const int32_t* pos, const float* w,
+                                 int64_t T, int64_t k, int64_t H, uint16_t* y) {
+  if (T < 0 || k <= 0 || H <= 0) return ORC_ERR_SHAPE;
+  const int64_t R = T * k;
+  for (int64_t i = 0; i < R; ++i)
+    if (pos[i] < 0 || pos[i] >= R) return ORC_ERR_SHAPE;
+  int64_t t;
+#pragma omp parallel for schedule(static)
+  for (t = 0; t < T; ++t)
+    for (int64_t c = 0; c < H; ++c) {
+      float s = 0.0f;
+      for (int64_t j = 0; j < k; ++j) {
+        const float v = oracle_bf16_to_f32(y_routed[(int64_t)pos[t * k + j] * H + c]);
+        const float p = w[t * k + j] * v;
+        s = s + p;
+      }
+      y[t * H + c] = oracle_f32_to_bf16(s);
+    }
+  return ORC_OK;
+}
+
+/* Whole MoE layer from token rows and router output: permute + quant, the
+ * expert chain on the routed rows (pre-quantised, so not quantised again),
+ * then the weighted combine.  y_routed_out [T*k,H] (optional) receives the
+ * expert chain's BF16 output. */
+int oracle_moe_layer(const void* x, const float* x_scale, const int64_t* topk_ids,
+                     const float* topk_weights, int64_t T, int64_t k, int64_t E, int64_t H,
+                     int64_t I, const int8_t* w13, const float* s13, const int8_t* w2,
+                     const float* s2, uint16_t* y, uint16_t* y_routed_out) {
+  if (T < 0 || k <= 0 || E <= 0 || H <= 0 || I <= 0) return ORC_ERR_SHAPE;
+  const size_t R = (size_t)(T * k);
+  int8_t* xq = malloc(R * (size_t)H + 1);
+  float* xs = malloc(R * sizeof(float) + 4);
+  int64_t* gl = malloc((size_t)E * sizeof(int64_t));
+  int32_t* pos = malloc(R * sizeof(int32_t) + 4);
+  uint16_t* yr = malloc(R * (size_t)H * sizeof(uint16_t) + 2);
+  int rc = ORC_ERR_ALLOC;
+  if (!xq || !xs || !gl || !pos || !yr) goto done;
+  rc = oracle_moe_permute_quant(x, x_scale, topk_ids, T, k, E, H, xq, xs, gl, pos);
+  if (rc) goto done;
+  rc = oracle_moe_w13_swiglu_requant_w2(xq, xs, gl, E, (int64_t)R, H, I, w13, s13, w2, s2, yr,
+                                        NULL, NULL, NULL, NULL, NULL, NULL);
+  if (rc) goto done;
+  rc = oracle_moe_unpermute_combine(yr, pos, topk_weights, T, k, H, y);
+  if (rc) goto done;
+  if (y_routed_out) memcpy(y_routed_out, yr, R * (size_t)H * sizeof(uint16_t));
+done:
+  free(xq);
+  free(xs);
+  free(gl);
+  free(pos);
+  free(yr);
   return rc;
 }

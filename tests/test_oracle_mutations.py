@@ -36,6 +36,16 @@ MUTATIONS = [
      "test_grouped_rejects_bad_group_lists", ()),
     ("pre-quantised input quantised again", "if (x_scale == NULL) {", "if (1) {",
      "test_moe_chain_composition_and_no_double_quant", ()),
+    ("routed row not advanced", "        pos[i] = (int32_t)row;\n        ++row;", "        pos[i] = (int32_t)row;",
+     "test_route_is_a_stable_sort_by_expert", (50, 4, 9, True)),
+    ("expert id upper bound off by one", "topk_ids[i] >= E) return ORC_ERR_TOPK_IDS;",
+     "topk_ids[i] > E) return ORC_ERR_TOPK_IDS;", "test_route_rejects_ids_outside_the_experts", ()),
+    ("routed scale taken from the wrong token", "xs[r] = st[t];", "xs[r] = st[(t + 1) % T];",
+     "test_permute_quant_is_quant_of_the_gathered_rows", (True,)),
+    ("combine drops the last choice", "for (int64_t j = 0; j < k; ++j) {\n        const float v",
+     "for (int64_t j = 0; j + 1 < k; ++j) {\n        const float v", "test_combine_against_float64", ()),
+    ("combine sums in double", "      float s = 0.0f;\n      for (int64_t j", "      double s = 0.0;\n      for (int64_t j",
+     "test_combine_closed_forms_and_order", ()),
 ]
 
 

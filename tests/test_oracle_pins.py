@@ -360,3 +360,140 @@ def test_moe_prequant_case_runs_and_rejects_bad_groups():
     bad[0] += 1
     with pytest.raises(oracle.OracleError):
         oracle.moe_w13_swiglu_requant_w2(m.x, m.x_scale, bad, m.w13.numpy(), m.s13, m.w2.numpy(), m.s2)
+
+
+# ------------------------------------------------- route, permute, combine ----
+
+def _ids(T, k, E, seed, distinct=True):
+    rng = np.random.default_rng(seed)
+    if distinct and T == 0:
+        return np.zeros((0, k), np.int64)
+    if distinct:
+        return np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int64)
+    return rng.integers(0, E, size=(T, k), dtype=np.int64)
+
+
+@pytest.mark.parametrize("T,k,E,distinct", [(50, 4, 9, True), (31, 3, 5, False), (17, 1, 4, True),
+                                            (0, 2, 3, True), (64, 8, 300, True)])
+def test_route_is_a_stable_sort_by_expert(T, k, E, distinct):
+    ids = _ids(T, k, E, seed=T + k + E, distinct=distinct)
+    g, pos = oracle.moe_route(ids, E)
+    flat = ids.ravel()
+    # library pins: counts are a histogram; the routed order is numpy's stable sort of the ids
+    assert np.array_equal(g, np.bincount(flat, minlength=E))
+    order = np.argsort(flat, kind="stable")
+    want = np.empty(T * k, np.int64)
+    want[order] = np.arange(T * k)
+    assert np.array_equal(pos.ravel().astype(np.int64), want)
+    # rows of expert e are the block [sum_{e'<e} g, + g[e]) of the routed order
+    off = np.concatenate([[0], np.cumsum(g)])
+    assert np.all((pos.ravel() >= off[flat]) & (pos.ravel() < off[flat + 1]))
+
+
+def test_route_matches_synthetic_expert_rows():
+    m = _small_moe(seed=7)
+    g, pos = oracle.moe_route(m.topk_ids, m.E)
+    assert np.array_equal(g, m.group_list)
+    token_of_row = np.empty(m.R, np.int64)
+    token_of_row[pos.ravel()] = np.repeat(np.arange(m.T), m.topk)
+    assert np.array_equal(token_of_row, m.token_index)
+
+
+def test_route_rejects_ids_outside_the_experts():
+    ids = _ids(5, 2, 4, seed=1)
+    for bad in (4, -1):
+        ids2 = ids.copy()
+        ids2[3, 1] = bad
+        try:
+            oracle.moe_route(ids2, 4)
+            code = 0
+        except oracle.OracleError as e:
+            code = e.code
+        assert code == 10
+
+
+@pytest.mark.parametrize("prequant", [False, True])
+def test_permute_quant_is_quant_of_the_gathered_rows(prequant):
+    m = _small_moe(prequant=prequant, seed=11)
+    xq, xs, g, pos = oracle.moe_permute_quant(m.x_tok, m.x_tok_scale, m.topk_ids, m.E)
+    assert np.array_equal(g, m.group_list)
+    if prequant:  # already INT8 with a per-token scale: copied, not quantised again
+        assert np.array_equal(xq, m.x_tok[m.token_index])
+        assert np.array_equal(xs.view(np.uint32), m.x_tok_scale[m.token_index].view(np.uint32))
+    else:         # quantising a token once and copying it = quantising each routed copy
+        q, s = oracle.dynamic_quant(m.x)
+        assert np.array_equal(xq, q) and np.array_equal(xs.view(np.uint32), s.view(np.uint32))
+
+
+def test_combine_against_float64():
+    rng = np.random.default_rng(5)
+    T, k, H = 23, 6, 40
+    ids = _ids(T, k, 11, seed=2)
+    _, pos = oracle.moe_route(ids, 11)
+    yr = S.to_bf16_bits(rng.standard_normal((T * k, H)).astype(np.float32) * np.float32(3))
+    w = rng.uniform(-1, 1, (T, k)).astype(np.float32)
+    y = f32(oracle.moe_unpermute_combine(yr, pos, w)).astype(np.float64)
+    v = f32(yr).astype(np.float64)[pos.astype(np.int64)]          # [T,k,H]
+    terms = w.astype(np.float64)[:, :, None] * v
+    exact = terms.sum(axis=1)
+    # k binary32 products and sums (error <= k * 2^-24 * sum|terms|), then one bf16 rounding
+    bound = bf16_ulp(exact) * 0.5 * 1.01 + k * 2.0 ** -24 * np.abs(terms).sum(axis=1) * 1.01
+    assert np.all(np.abs(y - exact) <= bound)
+
+
+def test_combine_closed_forms_and_order():
+    rng = np.random.default_rng(6)
+    T, H = 9, 24
+    yr = S.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    pos = rng.permutation(T).astype(np.int32).reshape(T, 1)
+    # one choice with weight 1: the routed row comes back unchanged
+    assert np.array_equal(oracle.moe_unpermute_combine(yr, pos, np.ones((T, 1), np.float32)),
+                          yr[pos[:, 0]])
+    # weights 0: +0 everywhere
+    assert np.all(oracle.moe_unpermute_combine(yr, pos, np.zeros((T, 1), np.float32)) == 0)
+    # two equal halves of one row give the row back exactly
+    yr2 = np.concatenate([yr, yr])
+    pos2 = np.stack([np.arange(T), np.arange(T) + T], axis=1).astype(np.int32)
+    assert np.array_equal(oracle.moe_unpermute_combine(yr2, pos2, np.full((T, 2), 0.5, np.float32)), yr)
+    # slot order, binary32 sums, one final rounding: terms 1+2^-8 then four of 2^-25.  In slot
+    # order each small term is lost (a quarter ulp of binary32 at 1) and the bf16 rounding of the
+    # tie 1+2^-8 goes to even, 1.0; summed in reverse (or exactly) they reach 1+2^-8+2^-23, which
+    # rounds up to 1+2^-7.
+    one = S.to_bf16_bits(np.ones((5, 1), np.float32))
+    w5 = np.array([[1 + 2.0 ** -8] + [2.0 ** -25] * 4], np.float32)
+    p5 = np.arange(5, dtype=np.int32).reshape(1, 5)
+    assert oracle.moe_unpermute_combine(one, p5, w5)[0, 0] == 0x3F80
+    assert oracle.moe_unpermute_combine(one, p5[:, ::-1].copy(), w5[:, ::-1].copy())[0, 0] == 0x3F81
+
+
+def test_moe_layer_reduces_to_the_expert_chain():
+    """With one choice per token and weight 1, the layer is the expert chain on the
+    expert-sorted token rows, put back in token order."""
+    m = S.make_moe(T=40, H=96, I=48, E=6, topk=1, routing="zipf", zipf_s=1.1, n_dead=1, seed=13)
+    w13, w2 = m.w13.numpy(), m.w2.numpy()
+    y = oracle.moe_layer(m.x_tok, None, m.topk_ids, np.ones((m.T, 1), np.float32), w13, m.s13, w2, m.s2)
+    y_rows = oracle.moe_w13_swiglu_requant_w2(m.x, None, m.group_list, w13, m.s13, w2, m.s2)
+    want = np.empty_like(y)
+    want[m.token_index] = y_rows
+    assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("prequant", [False, True])
+def test_moe_layer_routed_output_and_float64_combine(prequant):
+    m = _small_moe(prequant=prequant, seed=17)
+    w13, w2 = m.w13.numpy(), m.w2.numpy()
+    y, yr = oracle.moe_layer(m.x_tok, m.x_tok_scale, m.topk_ids, m.topk_weights, w13, m.s13, w2, m.s2,
+                             want_routed=True)
+    # the routed rows are the expert chain's output on the expert-sorted rows
+    assert np.array_equal(yr, oracle.moe_w13_swiglu_requant_w2(m.x, m.x_scale, m.group_list, w13, m.s13,
+                                                                w2, m.s2))
+    # token t's output is the weighted sum of its k routed rows (rows found by the synthetic order)
+    row_of = {}
+    for r, t in enumerate(m.token_index):
+        row_of.setdefault(int(t), []).append(r)
+    v = f32(yr).astype(np.float64)
+    for t in range(m.T):
+        rows = [row_of[t][sorted(m.topk_ids[t]).index(e)] for e in m.topk_ids[t]]
+        exact = sum(float(m.topk_weights[t, j]) * v[rows[j]] for j in range(m.topk))
+        got = f32(y[t]).astype(np.float64)
+        assert np.all(np.abs(got - exact) <= bf16_ulp(exact) * 0.51 + 1e-6 * np.abs(v[rows]).sum(0))

@@ -19,7 +19,9 @@ Recipe (one generator per case, seed 0 unless stated; draw order fixed):
          (the weights of the big cases are GBs); scales U[1e-3,1e-2].
          Pre-quantised cases draw an INT8 payload uniform in [-127,127] and a
          per-token fp32 scale U[1e-3,5e-2] per TOKEN, and routed rows carry
-         their token's payload and scale.
+         their token's payload and scale.  Token rows are kept too, with
+         router weights drawn last: U[0.05,1] per chosen expert, divided by
+         the token's sum, fp32.
 BF16 rounding of the drawn fp32 values uses torch's conversion.
 """
 from __future__ import annotations
@@ -122,6 +124,9 @@ class MoEInputs:
     w2: torch.Tensor           # int8 [E,H,I]
     s2: np.ndarray             # fp32 [E,H]
     extra: dict = field(default_factory=dict)
+    x_tok: Optional[np.ndarray] = None        # token rows: uint16 BF16 [T,H] or int8 [T,H] (prequant)
+    x_tok_scale: Optional[np.ndarray] = None  # fp32 [T] when pre-quantised, else None
+    topk_weights: Optional[np.ndarray] = None  # fp32 [T, topk] router weights, each row sums to ~1
 
     @property
     def R(self):
@@ -176,17 +181,22 @@ def make_moe(T: int, H: int, I: int, E: int, topk: int, routing: str = "uniform"
     s2 = rng.uniform(1e-3, 1e-2, size=(E, H)).astype(np.float32)
     topk_ids, p = route(rng, T, E, topk, routing, zipf_s, n_dead)
     token_index, counts = expert_sorted_rows(topk_ids, E)
+    s_tok = None
     if prequant:
-        q_tok = rng.integers(-127, 128, size=(T, H), dtype=np.int8)
+        x_tok = rng.integers(-127, 128, size=(T, H), dtype=np.int8)
         s_tok = rng.uniform(1e-3, 5e-2, size=T).astype(np.float32)
-        x = q_tok[token_index]
+        x = x_tok[token_index]
         x_scale = s_tok[token_index]
     else:
         x = x_tok[token_index]
         x_scale = None
+    # router weights of the chosen experts: positive, normalised per token
+    u = rng.uniform(0.05, 1.0, size=(T, topk))
+    topk_weights = (u / u.sum(axis=1, keepdims=True)).astype(np.float32)
     return MoEInputs(name=name, T=T, H=H, I=I, E=E, topk=topk, topk_ids=topk_ids,
                      token_index=token_index, group_list=counts, x=np.ascontiguousarray(x),
-                     x_scale=x_scale, w13=w13, s13=s13, w2=w2, s2=s2, extra=dict(p=p))
+                     x_scale=x_scale, w13=w13, s13=s13, w2=w2, s2=s2, extra=dict(p=p),
+                     x_tok=x_tok, x_tok_scale=s_tok, topk_weights=topk_weights)
 
 
 def moe_config(cfg_id: int, seed: int = 0, device: str = "cpu") -> MoEInputs:
