@@ -70,10 +70,13 @@ typedef enum {
   W8A8_ERR_DEVICE_TIMEOUT = 6, /* device: a bounded wait gave up */
   W8A8_ERR_CUDA = 7,           /* a CUDA runtime call failed (launch error etc.) */
   W8A8_ERR_UNSUPPORTED = 8,    /* the device is not sm_103 / a mode is not built */
-  W8A8_ERR_PACKED = 9          /* device: packed weight header does not match the call */
+  W8A8_ERR_PACKED = 9,         /* device: packed weight header does not match the call */
+  W8A8_ERR_TOPK_IDS = 10       /* device: a topk id outside [0,E), or a routed row index outside [0,T*k) */
 } w8a8_status;
 
 #define W8A8_MAX_K 65536
+#define W8A8_MAX_EXPERTS 1024
+#define W8A8_STATUS_BYTES 256 /* the status word at the start of every workspace */
 
 /* Human-readable name of a status code (static string). */
 W8A8_API const char* w8a8_status_string(int status);
@@ -190,8 +193,70 @@ W8A8_API w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_sca
 
 /* Offsets (bytes from ws) of the MoE intermediates kept in the workspace after
  * a call: 0 xq int8 [R,H], 1 xs fp32 [R], 2 h bf16 [R,I], 3 hq int8 [R,I],
- * 4 hs fp32 [R].  Returns -1 for an unknown index.  (Validation aid.) */
+ * 4 hs fp32 [R], and on shapes the tensor-core engine takes 5 xq as fp16
+ * [R,H] and 6 hq as fp16 [R,I].  Returns -1 for an unknown index or a copy the
+ * shape does not keep.  (Validation aid.) */
 W8A8_API int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int which);
+
+/* ------------------------------------------------------------------------ */
+/* MoE routing around the expert chain -- [P1] §三: the DeepEP INT8 dispatch */
+/* quantises each token's BF16 hidden row once (INT8 + one per-token scale); */
+/* the Ascend runner input regroups the routed rows by expert, its           */
+/* expert_tokens (rows per expert) being the grouped matmul's group_list;    */
+/* topk_ids and topk_weights travel with the dispatch output.                */
+/*   Every (token t, slot j) pair of topk_ids [T,k] is one routed row,       */
+/*   R = T*k.  Routed rows are ordered by expert, then token, then slot:     */
+/*   pos[t*k+j] is the routed row of (t, j), group_list[e] the number of     */
+/*   pairs naming expert e.                                                  */
+/*   combine: y[t,c] = bf16_rne(s) with s = 0, then for j = 0..k-1 in order  */
+/*   s = s + w[t,j] * float(y_routed[pos[t,j], c]), every product and sum     */
+/*   rounded to binary32 (no fused multiply-add).                            */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace of moe_permute_quant (status word + per-chunk expert counts). */
+W8A8_API size_t moe_route_workspace_bytes(int64_t T, int64_t k, int64_t E);
+
+/* x: bf16 [T,H] token rows when x_scale == NULL (each token quantised once,
+ * as w8a8_dynamic_quant would), else int8 [T,H] with per-token scales
+ * x_scale [T] fp32 (copied, not quantised again).  topk_ids int64 [T,k].
+ * Out (caller-owned device buffers): xq int8 [T*k,H] routed rows, xs fp32
+ * [T*k], group_list int64 [E], pos int32 [T,k].  H % 16 == 0, x and xq 16-byte
+ * aligned, k >= 1, T*k <= INT32_MAX, 1 <= E <= W8A8_MAX_EXPERTS.  ws: zero-filled,
+ * at least moe_route_workspace_bytes(T, k, E).  An id outside [0,E) sets
+ * W8A8_ERR_TOPK_IDS on the device: its pair gets pos = -1 and no routed row,
+ * so the counts sum to less than T*k and a grouped call given them refuses
+ * them. */
+W8A8_API w8a8_status moe_permute_quant(const void* x, const float* x_scale, const int64_t* topk_ids,
+                                       int64_t T, int64_t k, int64_t E, int64_t H, int8_t* xq, float* xs,
+                                       int64_t* group_list, int32_t* pos, void* ws, size_t ws_bytes,
+                                       w8a8_stream_t stream);
+
+/* y_routed bf16 [T*k,H], pos int32 [T,k] (as moe_permute_quant writes it),
+ * topk_weights fp32 [T,k] -> y bf16 [T,H].  H % 8 == 0, y_routed and y 16-byte
+ * aligned.  ws: zero-filled, at least W8A8_STATUS_BYTES (only the status word
+ * is used).  A pos outside [0,T*k) sets W8A8_ERR_TOPK_IDS on the device and its
+ * term is left out of the sum. */
+W8A8_API w8a8_status moe_unpermute_combine(const uint16_t* y_routed, const int32_t* pos,
+                                           const float* topk_weights, int64_t T, int64_t k, int64_t H,
+                                           uint16_t* y, void* ws, size_t ws_bytes, w8a8_stream_t stream);
+
+/* The whole MoE layer from token rows and router output:
+ * moe_permute_quant -> moe_w13_swiglu_requant_w2 on the routed rows (already
+ * quantised, so not quantised again) -> moe_unpermute_combine.  Arguments as
+ * in those calls; y bf16 [T,H].  I % 64 == 0, H % 16 == 0. */
+W8A8_API size_t moe_layer_workspace_bytes(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E);
+W8A8_API w8a8_status moe_layer(const void* x, const float* x_scale, const int64_t* topk_ids,
+                               const float* topk_weights, int64_t T, int64_t k, int64_t E, int64_t H,
+                               int64_t I, const void* w13_packed, const float* w13_scale,
+                               const void* w2_packed, const float* w2_scale, void* ws, size_t ws_bytes,
+                               uint16_t* y, w8a8_stream_t stream);
+
+/* Offsets (bytes from ws) of what moe_layer leaves in its workspace: 0..6 as
+ * moe_workspace_offset with R = T*k (on shapes the tensor-core engine takes,
+ * the routed codes are kept only as their fp16 copy, index 5), 7 group_list
+ * int64 [E], 8 pos int32 [T,k], 9 y_routed bf16 [T*k,H].  -1 for an unknown
+ * index.  (Validation aid.) */
+W8A8_API int64_t moe_layer_workspace_offset(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E, int which);
 
 /* ------------------------------------------------------------------------ */
 /* Dense quantised matmul without a caller workspace.  The pages have no     */

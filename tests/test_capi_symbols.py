@@ -59,6 +59,14 @@ def test_status_strings_and_sizes(lib):
     offs = [lib.moe_workspace_offset(100, 256, 128, 8, i) for i in range(5)]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lib.moe_workspace_offset(100, 256, 128, 8, 9) == -1
+    assert lib.w8a8_status_string(10).startswith(b"W8A8_ERR_TOPK_IDS")
+    assert lib.moe_route_workspace_bytes(4096, 8, 64) >= 256 + 64 * 4 * (4096 * 8 // 512)
+    assert lib.moe_route_workspace_bytes(4, 0, 8) == 0
+    T, k, H, I, E = 100, 3, 256, 128, 8
+    lo = [lib.moe_layer_workspace_offset(T, k, H, I, E, i) for i in (0, 1, 2, 3, 4, 7, 8, 9)]
+    assert lo == sorted(lo) and all(o % 256 == 0 for o in lo)
+    assert lo[:5] == [lib.moe_workspace_offset(T * k, H, I, E, i) for i in range(5)]
+    assert lib.moe_layer_workspace_bytes(T, k, H, I, E) >= lo[-1] + T * k * H * 2
 
 
 def test_host_validation_rejects_before_launch(lib):
@@ -76,3 +84,22 @@ def test_host_validation_rejects_before_launch(lib):
                                          fake, None) == 2  # I % 64 != 0
     assert lib.w8a8_prepack_weight(fake, 1, 130, 64, 1, ctypes.c_void_p(256), None) == 2  # gate/up needs I % 64 == 0
     assert lib.w8a8_prepack_weight(fake, 1, 128, 64, 8, ctypes.c_void_p(256), None) == 2  # unknown flag
+    # routing: k < 1, E out of range, H % 16, T*k past int32, missing workspace
+    big = 1 << 20
+    assert lib.moe_permute_quant(fake, None, fake, 4, 0, 8, 64, fake, fake, fake, fake, fake, big, None) == 2
+    assert lib.moe_permute_quant(fake, None, fake, 4, 2, 2000, 64, fake, fake, fake, fake, fake, big, None) == 2
+    assert lib.moe_permute_quant(fake, None, fake, 4, 2, 8, 72, fake, fake, fake, fake, fake, big, None) == 3
+    assert lib.moe_permute_quant(fake, None, fake, 1 << 30, 4, 8, 64, fake, fake, fake, fake, fake, big, None) == 2
+    assert lib.moe_permute_quant(fake, None, fake, 4, 2, 8, 64, fake, fake, fake, fake, None, big, None) == 4
+    assert lib.moe_permute_quant(fake, None, fake, 4, 2, 8, 64, fake, fake, fake, fake, fake, 16, None) == 4
+    assert lib.moe_unpermute_combine(fake, fake, fake, 4, 2, 60, fake, fake, big, None) == 3
+    assert lib.moe_unpermute_combine(fake, fake, fake, 4, 2, 64, fake, fake, 16, None) == 4
+    assert lib.moe_unpermute_combine(fake, None, fake, 4, 2, 64, fake, fake, big, None) == 1
+    assert lib.moe_unpermute_combine(fake, fake, fake, 0, 2, 64, fake, fake, big, None) == 0
+    assert lib.moe_layer(fake, None, fake, fake, 4, 2, 8, 64, 96, fake, fake, fake, fake, fake, 1 << 30,
+                         fake, None) == 2  # I % 64 != 0
+    p256 = ctypes.c_void_p(256)
+    assert lib.moe_layer(fake, None, fake, fake, 4, 2, 8, 64, 128, p256, fake, p256, fake, fake, 16,
+                         fake, None) == 4
+    assert lib.moe_layer(fake, None, fake, fake, 0, 2, 8, 64, 128, fake, fake, fake, fake, fake, 16,
+                         fake, None) == 0  # no tokens: nothing to do

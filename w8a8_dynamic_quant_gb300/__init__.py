@@ -25,6 +25,8 @@ __all__ = [
     "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
     "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
+    "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
+    "moe_layer_workspace_offset", "moe_layer",
 ]
 
 
@@ -231,6 +233,105 @@ def moe_w13_swiglu_requant_w2(x: torch.Tensor, x_scale: Optional[torch.Tensor],
             x.data_ptr(), _ptr(x_scale), group_list.data_ptr(), E, R, H, I, w13_packed.data_ptr(),
             w13_scale.data_ptr(), w2_packed.data_ptr(), w2_scale.data_ptr(), ws.data_ptr(),
             ws.numel(), y.data_ptr(), _stream(dev)))
+    return y
+
+
+def moe_route_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(_capi.lib().moe_route_workspace_bytes(T, k, E))
+
+
+def moe_permute_quant(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_ids: torch.Tensor, E: int,
+                      ws: Optional[torch.Tensor] = None):
+    """Token rows -> routed rows grouped by expert.  x bf16 [T,H] (x_scale None: each token quantised
+    once) or int8 [T,H] with x_scale [T]; topk_ids int64 [T,k].  Returns (int8 xq [T*k,H],
+    float32 xs [T*k], int64 group_list [E], int32 pos [T,k])."""
+    T, H = x.shape
+    dev = x.device
+    if x_scale is None:
+        _need(x, "x", torch.bfloat16)
+    else:
+        _need(x, "x", torch.int8)
+        _need(x_scale, "x_scale", torch.float32, (T,), dev)
+    _need(topk_ids, "topk_ids", torch.int64, None, dev)
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != T:
+        raise ValueError("topk_ids must be [T,k]")
+    k = topk_ids.shape[1]
+    ws = workspace(moe_route_workspace_bytes(T, k, E), dev) if ws is None else ws
+    _need(ws, "ws", torch.uint8, None, dev)
+    xq = torch.empty((T * k, H), dtype=torch.int8, device=dev)
+    xs = torch.empty((T * k,), dtype=torch.float32, device=dev)
+    group_list = torch.empty((E,), dtype=torch.int64, device=dev)
+    pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _capi.check("moe_permute_quant", _capi.lib().moe_permute_quant(
+            x.data_ptr(), _ptr(x_scale), topk_ids.data_ptr(), T, k, E, H, xq.data_ptr(), xs.data_ptr(),
+            group_list.data_ptr(), pos.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)))
+    return xq, xs, group_list, pos
+
+
+def moe_unpermute_combine(y_routed: torch.Tensor, pos: torch.Tensor, topk_weights: torch.Tensor,
+                          ws: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None):
+    """bf16 y_routed [T*k,H], int32 pos [T,k], float32 topk_weights [T,k] -> bf16 y [T,H]."""
+    _need(y_routed, "y_routed", torch.bfloat16)
+    dev = y_routed.device
+    _need(pos, "pos", torch.int32, None, dev)
+    if pos.dim() != 2:
+        raise ValueError("pos must be [T,k]")
+    T, k = pos.shape
+    H = y_routed.shape[1]
+    if y_routed.shape[0] != T * k:
+        raise ValueError("y_routed must have T*k rows")
+    _need(topk_weights, "topk_weights", torch.float32, (T, k), dev)
+    ws = workspace(_capi.STATUS_BYTES, dev) if ws is None else ws
+    _need(ws, "ws", torch.uint8, None, dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+    _need(y, "y", torch.bfloat16, (T, H), dev)
+    with torch.cuda.device(dev):
+        _capi.check("moe_unpermute_combine", _capi.lib().moe_unpermute_combine(
+            y_routed.data_ptr(), pos.data_ptr(), topk_weights.data_ptr(), T, k, H, y.data_ptr(),
+            ws.data_ptr(), ws.numel(), _stream(dev)))
+    return y
+
+
+def moe_layer_workspace_bytes(T: int, k: int, H: int, I: int, E: int) -> int:
+    return int(_capi.lib().moe_layer_workspace_bytes(T, k, H, I, E))
+
+
+def moe_layer_workspace_offset(T: int, k: int, H: int, I: int, E: int, which: int) -> int:
+    return int(_capi.lib().moe_layer_workspace_offset(T, k, H, I, E, which))
+
+
+def moe_layer(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_ids: torch.Tensor,
+              topk_weights: torch.Tensor, w13_packed: torch.Tensor, w13_scale: torch.Tensor,
+              w2_packed: torch.Tensor, w2_scale: torch.Tensor, ws: Optional[torch.Tensor] = None,
+              y: Optional[torch.Tensor] = None):
+    """MoE layer from token rows and router output: x bf16 [T,H] (or int8 with x_scale [T]),
+    topk_ids int64 [T,k], topk_weights float32 [T,k] -> bf16 y [T,H]."""
+    T, H = x.shape
+    dev = x.device
+    if x_scale is None:
+        _need(x, "x", torch.bfloat16)
+    else:
+        _need(x, "x", torch.int8)
+        _need(x_scale, "x_scale", torch.float32, (T,), dev)
+    _need(topk_ids, "topk_ids", torch.int64, None, dev)
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != T:
+        raise ValueError("topk_ids must be [T,k]")
+    k = topk_ids.shape[1]
+    _need(topk_weights, "topk_weights", torch.float32, (T, k), dev)
+    _need(w13_scale, "w13_scale", torch.float32, None, dev)
+    E = w13_scale.shape[0]
+    I = w13_scale.shape[-1] // 2
+    _need(w2_scale, "w2_scale", torch.float32, (E, H), dev)
+    ws = workspace(moe_layer_workspace_bytes(T, k, H, I, E), dev) if ws is None else ws
+    _need(ws, "ws", torch.uint8, None, dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+    _need(y, "y", torch.bfloat16, (T, H), dev)
+    with torch.cuda.device(dev):
+        _capi.check("moe_layer", _capi.lib().moe_layer(
+            x.data_ptr(), _ptr(x_scale), topk_ids.data_ptr(), topk_weights.data_ptr(), T, k, E, H, I,
+            w13_packed.data_ptr(), w13_scale.data_ptr(), w2_packed.data_ptr(), w2_scale.data_ptr(),
+            ws.data_ptr(), ws.numel(), y.data_ptr(), _stream(dev)))
     return y
 
 

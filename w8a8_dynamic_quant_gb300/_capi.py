@@ -34,6 +34,13 @@ SIGNATURES = {
     "moe_workspace_offset": (_i64, [_i64, _i64, _i64, _i64, _int]),
     "moe_w13_swiglu_requant_w2": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz,
                                          _vp, _vp]),
+    "moe_route_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "moe_permute_quant": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_unpermute_combine": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "moe_layer_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
+    "moe_layer": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                         _vp]),
+    "moe_layer_workspace_offset": (_i64, [_i64, _i64, _i64, _i64, _i64, _int]),
     "w8a8_quant_matmul_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp]),
     "w8a8_read_device_status": (_int, [_vp, _vp]),
     "w8a8_last_engine": (_int, []),
@@ -41,7 +48,8 @@ SIGNATURES = {
 
 STATUS = {0: "W8A8_OK", 1: "W8A8_ERR_NULL", 2: "W8A8_ERR_SHAPE", 3: "W8A8_ERR_ALIGN",
           4: "W8A8_ERR_WORKSPACE", 5: "W8A8_ERR_GROUP_LIST", 6: "W8A8_ERR_DEVICE_TIMEOUT",
-          7: "W8A8_ERR_CUDA", 8: "W8A8_ERR_UNSUPPORTED", 9: "W8A8_ERR_PACKED"}
+          7: "W8A8_ERR_CUDA", 8: "W8A8_ERR_UNSUPPORTED", 9: "W8A8_ERR_PACKED", 10: "W8A8_ERR_TOPK_IDS"}
+STATUS_BYTES = 256
 PACK_GATE_UP = 1
 PACK_F16 = 2
 

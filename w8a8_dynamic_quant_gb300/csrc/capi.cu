@@ -172,6 +172,35 @@ MoeWs moe_layout(int64_t R, int64_t H, int64_t I, int64_t E) {
   return L;
 }
 
+// Workspace of the MoE layer from token rows: the expert chain's workspace first (its status word is
+// the layer's), then the routing results, the routing scratch and the chain's routed output.
+struct LayerWs {
+  MoeWs m;
+  size_t group_list, pos, counts, y_routed, total;
+};
+LayerWs layer_layout(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E) {
+  LayerWs L;
+  const int64_t R = T * k;
+  L.m = moe_layout(R, H, I, E);
+  size_t off = align_up(L.m.total, 256);
+  L.group_list = off; off = align_up(off + static_cast<uint64_t>(E) * 8, 256);
+  L.pos = off;        off = align_up(off + static_cast<uint64_t>(R) * 4, 256);
+  L.counts = off;     off = align_up(off + static_cast<uint64_t>(route_scratch_ints(R, E)) * 4, 256);
+  L.y_routed = off;   off = align_up(off + static_cast<uint64_t>(R) * H * 2, 256);
+  L.total = off;
+  return L;
+}
+
+// Sizes shared by the routing calls: T tokens with k choices each, R = T*k routed rows.
+w8a8_status check_route_shape(int64_t T, int64_t k, int64_t E) {
+  if (T < 0 || k < 1 || k > INT32_MAX || E < 1 || E > kMaxE) return W8A8_ERR_SHAPE;
+  if (T > 0 && k > INT32_MAX / T) return W8A8_ERR_SHAPE;
+  return W8A8_OK;
+}
+
+// The combine launches one block per (token, 1024 columns).
+bool combine_grid_ok(int64_t T, int64_t H) { return T * ((H / 8 + 127) / 128) <= INT32_MAX; }
+
 // One contraction on the engine its shape calls for: tcgen05 (activations
 // widened to fp16 in the workspace) when the shape is large and the weight
 // carries its fp16 copy, else the warp-level engine.
@@ -207,6 +236,91 @@ w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream,
   return cuda_status(launch_reg_gemm(a, p, stream));
 }
 
+// The expert chain on routed rows (workspace laid out by moe_layout at `ws`).  x16_ready: the routed
+// codes are already in the workspace's fp16 copy (the layer's permute wrote them there), so an INT8
+// input is not widened again.
+w8a8_status moe_chain(const void* x, const float* x_scale, bool x16_ready, const int64_t* group_list, int64_t E,
+                      int64_t R, int64_t H, int64_t I, const void* w13_packed, const float* w13_scale,
+                      const void* w2_packed, const float* w2_scale, void* ws, uint16_t* y, cudaStream_t st,
+                      int sms) {
+  const MoeWs L = moe_layout(R, H, I, E);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  void* gws = b + L.gemm;
+
+  const int8_t* xq = static_cast<const int8_t*>(x);
+  const float* xs = x_scale;
+  uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
+  int8_t* hq = reinterpret_cast<int8_t*>(b + L.hq);
+  float* hs = reinterpret_cast<float*>(b + L.hs);
+  // tensor-core engines for shapes that take them: the packed fp16 weight copies when both packs carry
+  // them, else the int8 weights widened in tensor memory
+  const bool tc = L.xq16 != 0;
+  const void* w13_16 = tc ? pack_f16(w13_packed, E, 2 * I, H, W8A8_PACK_GATE_UP) : nullptr;
+  const void* w2_16 = tc ? pack_f16(w2_packed, E, H, I, 0u) : nullptr;
+  const bool f16w = w13_16 != nullptr && w2_16 != nullptr;
+  uint16_t* xq16 = tc ? reinterpret_cast<uint16_t*>(b + L.xq16) : nullptr;
+  uint16_t* hq16 = tc ? reinterpret_cast<uint16_t*>(b + L.hq16) : nullptr;
+
+  if (x_scale == nullptr) {  // BF16 input: quantise once; an INT8 input with its scale is used as is
+    int8_t* q = reinterpret_cast<int8_t*>(b + L.xq);
+    float* s = reinterpret_cast<float*>(b + L.xs);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    const cudaError_t e = tc ? launch_dynamic_quant_dual(xb, R, H, q, xq16, s, st, sms)
+                             : launch_dynamic_quant(xb, R, H, q, s, st, sms);
+    if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    xq = q;
+    xs = s;
+  } else if (tc && !x16_ready) {
+    if (w8a8_status e = cuda_status(launch_s8_to_f16(xq, xq16, R * H, st, sms))) return e;
+  }
+
+  GemmArgs a13;
+  a13.q = xq;
+  a13.x_scale = xs;
+  a13.group_list = group_list;
+  a13.E = E;
+  a13.R = R;
+  a13.K = H;
+  a13.N = 2 * I;
+  a13.packed = w13_packed;
+  a13.pack_flags = W8A8_PACK_GATE_UP;
+  a13.w_scale = w13_scale;
+  a13.out = h;
+  a13.mode = EPI_SWIGLU;
+  bind_ws(a13, gws, L.g);
+  a13.status = static_cast<DeviceStatus*>(ws);
+  const cudaError_t e13 = f16w ? launch_tc_gemm(a13, xq16, w13_16, sms, st)
+                         : tc ? launch_tcw_gemm(a13, xq16, sms, st)
+                             : launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st);
+  if (e13 != cudaSuccess) return W8A8_ERR_CUDA;
+
+  const cudaError_t eq = tc ? launch_dynamic_quant_dual(h, R, I, hq, hq16, hs, st, sms)
+                            : launch_dynamic_quant(h, R, I, hq, hs, st, sms);
+  if (eq != cudaSuccess) return W8A8_ERR_CUDA;
+
+  GemmArgs a2;
+  a2.q = hq;
+  a2.x_scale = hs;
+  a2.group_list = group_list;
+  a2.E = E;
+  a2.R = R;
+  a2.K = I;
+  a2.N = H;
+  a2.packed = w2_packed;
+  a2.pack_flags = 0u;
+  a2.w_scale = w2_scale;
+  a2.out = y;
+  a2.mode = EPI_BF16;
+  bind_ws(a2, gws, L.g);
+  a2.status = static_cast<DeviceStatus*>(ws);
+  const cudaError_t e2 = f16w ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
+                        : tc ? launch_tcw_gemm(a2, hq16, sms, st)
+                            : launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st);
+  t_last_engine = tc ? W8A8_ENGINE_TC : W8A8_ENGINE_WARP;
+  return e2 == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -223,6 +337,7 @@ const char* w8a8_status_string(int s) {
     case W8A8_ERR_CUDA: return "W8A8_ERR_CUDA: a CUDA runtime call failed";
     case W8A8_ERR_UNSUPPORTED: return "W8A8_ERR_UNSUPPORTED: needs a compute capability 10.3 (GB300) device";
     case W8A8_ERR_PACKED: return "W8A8_ERR_PACKED: packed weight header does not match the call";
+    case W8A8_ERR_TOPK_IDS: return "W8A8_ERR_TOPK_IDS: a topk id outside [0,E) or a routed row index outside [0,T*k)";
     default: return "W8A8 unknown status";
   }
 }
@@ -393,81 +508,119 @@ w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_scale, const
   if (ws_bytes < L.total || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
   int sms = 0;
   if (w8a8_status s = device_info(sms)) return s;
+  return moe_chain(x, x_scale, false, group_list, E, R, H, I, w13_packed, w13_scale, w2_packed, w2_scale, ws, y,
+                   reinterpret_cast<cudaStream_t>(stream), sms);
+}
+
+size_t moe_route_workspace_bytes(int64_t T, int64_t k, int64_t E) {
+  if (check_route_shape(T, k, E) != W8A8_OK) return 0;
+  return kStatusBytes + align_up(static_cast<uint64_t>(route_scratch_ints(T * k, E)) * 4, 256);
+}
+
+w8a8_status moe_permute_quant(const void* x, const float* x_scale, const int64_t* topk_ids, int64_t T, int64_t k,
+                              int64_t E, int64_t H, int8_t* xq, float* xs, int64_t* group_list, int32_t* pos,
+                              void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+  if (w8a8_status s = check_route_shape(T, k, E)) return s;
+  if (H <= 0 || H > INT32_MAX) return W8A8_ERR_SHAPE;
+  if (H % 16 != 0) return W8A8_ERR_ALIGN;
+  if (!group_list) return W8A8_ERR_NULL;
+  if (!ws) return W8A8_ERR_WORKSPACE;
+  if (T > 0 && (!x || !topk_ids || !xq || !xs || !pos)) return W8A8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq)) return W8A8_ERR_ALIGN;
+  if (ws_bytes < moe_route_workspace_bytes(T, k, E) || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(ws);
-  void* gws = b + L.gemm;
+  const int64_t n = T * k;
+  if (w8a8_status e = cuda_status(launch_route(topk_ids, n, static_cast<int>(E), reinterpret_cast<int32_t*>(b + kStatusBytes),
+                                               group_list, pos, static_cast<DeviceStatus*>(ws), st)))
+    return e;
+  if (n == 0) return W8A8_OK;
+  const cudaError_t e = x_scale == nullptr
+      ? launch_quant_scatter(static_cast<const uint16_t*>(x), T, H, pos, static_cast<int>(k), xq, nullptr, xs, 0, st, sms)
+      : launch_scatter_rows_i8(static_cast<const int8_t*>(x), x_scale, T, H, pos, static_cast<int>(k), xq, nullptr,
+                               xs, 0, st, sms);
+  return cuda_status(e);
+}
 
-  const int8_t* xq = static_cast<const int8_t*>(x);
-  const float* xs = x_scale;
-  uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
-  int8_t* hq = reinterpret_cast<int8_t*>(b + L.hq);
-  float* hs = reinterpret_cast<float*>(b + L.hs);
-  // tensor-core engines for shapes that take them: the packed fp16 weight copies when both packs carry
-  // them, else the int8 weights widened in tensor memory
-  const bool tc = L.xq16 != 0;
-  const void* w13_16 = tc ? pack_f16(w13_packed, E, 2 * I, H, W8A8_PACK_GATE_UP) : nullptr;
-  const void* w2_16 = tc ? pack_f16(w2_packed, E, H, I, 0u) : nullptr;
-  const bool f16w = w13_16 != nullptr && w2_16 != nullptr;
-  uint16_t* xq16 = tc ? reinterpret_cast<uint16_t*>(b + L.xq16) : nullptr;
-  uint16_t* hq16 = tc ? reinterpret_cast<uint16_t*>(b + L.hq16) : nullptr;
+w8a8_status moe_unpermute_combine(const uint16_t* y_routed, const int32_t* pos, const float* topk_weights, int64_t T,
+                                  int64_t k, int64_t H, uint16_t* y, void* ws, size_t ws_bytes,
+                                  w8a8_stream_t stream) {
+  if (w8a8_status s = check_route_shape(T, k, 1)) return s;
+  if (H <= 0 || H > INT32_MAX || !combine_grid_ok(T, H)) return W8A8_ERR_SHAPE;
+  if (H % 8 != 0) return W8A8_ERR_ALIGN;
+  if (T == 0) return W8A8_OK;
+  if (!y_routed || !pos || !topk_weights || !y) return W8A8_ERR_NULL;
+  if (!ws) return W8A8_ERR_WORKSPACE;
+  if (!aligned16(y_routed) || !aligned16(y)) return W8A8_ERR_ALIGN;
+  if (ws_bytes < static_cast<size_t>(kStatusBytes) || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_combine(y_routed, pos, topk_weights, T, static_cast<int>(k), H, y,
+                                    static_cast<DeviceStatus*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+}
 
-  if (x_scale == nullptr) {  // BF16 input: quantise once; an INT8 input with its scale is used as is
-    int8_t* q = reinterpret_cast<int8_t*>(b + L.xq);
-    float* s = reinterpret_cast<float*>(b + L.xs);
-    const uint16_t* xb = static_cast<const uint16_t*>(x);
-    const cudaError_t e = tc ? launch_dynamic_quant_dual(xb, R, H, q, xq16, s, st, sms)
-                             : launch_dynamic_quant(xb, R, H, q, s, st, sms);
-    if (e != cudaSuccess) return W8A8_ERR_CUDA;
-    xq = q;
-    xs = s;
-  } else if (tc) {
-    if (w8a8_status e = cuda_status(launch_s8_to_f16(xq, xq16, R * H, st, sms))) return e;
+size_t moe_layer_workspace_bytes(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E) {
+  if (check_route_shape(T, k, E) != W8A8_OK || H <= 0 || I <= 0) return 0;
+  return layer_layout(T, k, H, I, E).total;
+}
+
+int64_t moe_layer_workspace_offset(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E, int which) {
+  if (check_route_shape(T, k, E) != W8A8_OK || H <= 0 || I <= 0) return -1;
+  const LayerWs L = layer_layout(T, k, H, I, E);
+  switch (which) {
+    case 7: return static_cast<int64_t>(L.group_list);
+    case 8: return static_cast<int64_t>(L.pos);
+    case 9: return static_cast<int64_t>(L.y_routed);
+    default: return moe_workspace_offset(T * k, H, I, E, which);
   }
+}
 
-  GemmArgs a13;
-  a13.q = xq;
-  a13.x_scale = xs;
-  a13.group_list = group_list;
-  a13.E = E;
-  a13.R = R;
-  a13.K = H;
-  a13.N = 2 * I;
-  a13.packed = w13_packed;
-  a13.pack_flags = W8A8_PACK_GATE_UP;
-  a13.w_scale = w13_scale;
-  a13.out = h;
-  a13.mode = EPI_SWIGLU;
-  bind_ws(a13, gws, L.g);
-  a13.status = static_cast<DeviceStatus*>(ws);
-  const cudaError_t e13 = f16w ? launch_tc_gemm(a13, xq16, w13_16, sms, st)
-                         : tc ? launch_tcw_gemm(a13, xq16, sms, st)
-                             : launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st);
-  if (e13 != cudaSuccess) return W8A8_ERR_CUDA;
-
-  const cudaError_t eq = tc ? launch_dynamic_quant_dual(h, R, I, hq, hq16, hs, st, sms)
-                            : launch_dynamic_quant(h, R, I, hq, hs, st, sms);
-  if (eq != cudaSuccess) return W8A8_ERR_CUDA;
-
-  GemmArgs a2;
-  a2.q = hq;
-  a2.x_scale = hs;
-  a2.group_list = group_list;
-  a2.E = E;
-  a2.R = R;
-  a2.K = I;
-  a2.N = H;
-  a2.packed = w2_packed;
-  a2.pack_flags = 0u;
-  a2.w_scale = w2_scale;
-  a2.out = y;
-  a2.mode = EPI_BF16;
-  bind_ws(a2, gws, L.g);
-  a2.status = static_cast<DeviceStatus*>(ws);
-  const cudaError_t e2 = f16w ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
-                        : tc ? launch_tcw_gemm(a2, hq16, sms, st)
-                            : launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st);
-  t_last_engine = tc ? W8A8_ENGINE_TC : W8A8_ENGINE_WARP;
-  return e2 == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
+w8a8_status moe_layer(const void* x, const float* x_scale, const int64_t* topk_ids, const float* topk_weights,
+                      int64_t T, int64_t k, int64_t E, int64_t H, int64_t I, const void* w13_packed,
+                      const float* w13_scale, const void* w2_packed, const float* w2_scale, void* ws, size_t ws_bytes,
+                      uint16_t* y, w8a8_stream_t stream) {
+  if (w8a8_status s = check_route_shape(T, k, E)) return s;
+  if (H <= 0 || I <= 0 || !combine_grid_ok(T, H)) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(H)) return s;
+  if (w8a8_status s = check_k(I)) return s;
+  if (I % kGateUpBlock != 0) return W8A8_ERR_SHAPE;
+  if (T == 0) return W8A8_OK;
+  if (!x || !topk_ids || !topk_weights || !w13_packed || !w13_scale || !w2_packed || !w2_scale || !y)
+    return W8A8_ERR_NULL;
+  if (!ws) return W8A8_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(w13_packed) & 255u) ||
+      (reinterpret_cast<uintptr_t>(w2_packed) & 255u))
+    return W8A8_ERR_ALIGN;
+  const LayerWs L = layer_layout(T, k, H, I, E);
+  if (ws_bytes < L.total || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  DeviceStatus* status = static_cast<DeviceStatus*>(ws);
+  const int64_t R = T * k;
+  const int kk = static_cast<int>(k);
+  int64_t* gl = reinterpret_cast<int64_t*>(b + L.group_list);
+  int32_t* pos = reinterpret_cast<int32_t*>(b + L.pos);
+  int8_t* xq = reinterpret_cast<int8_t*>(b + L.m.xq);
+  float* xs = reinterpret_cast<float*>(b + L.m.xs);
+  uint16_t* xq16 = L.m.xq16 ? reinterpret_cast<uint16_t*>(b + L.m.xq16) : nullptr;
+  uint16_t* yr = reinterpret_cast<uint16_t*>(b + L.y_routed);
+  if (w8a8_status e = cuda_status(launch_route(topk_ids, R, static_cast<int>(E), reinterpret_cast<int32_t*>(b + L.counts),
+                                               gl, pos, status, st)))
+    return e;
+  // the routed codes go where the chain's engine reads them: fp16 for the tensor-core engines, else int8
+  const int out = xq16 != nullptr ? 1 : 0;
+  const cudaError_t ep = x_scale == nullptr
+      ? launch_quant_scatter(static_cast<const uint16_t*>(x), T, H, pos, kk, xq, xq16, xs, out, st, sms)
+      : launch_scatter_rows_i8(static_cast<const int8_t*>(x), x_scale, T, H, pos, kk, xq, xq16, xs, out, st, sms);
+  if (ep != cudaSuccess) return W8A8_ERR_CUDA;
+  if (w8a8_status e = moe_chain(xq, xs, true, gl, E, R, H, I, w13_packed, w13_scale, w2_packed, w2_scale, ws, yr,
+                                st, sms))
+    return e;
+  return cuda_status(launch_combine(yr, pos, topk_weights, T, kk, H, y, status, st));
 }
 
 w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream) {

@@ -23,6 +23,25 @@ cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t
 cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
                                       float* scale, cudaStream_t stream, int num_sms);
 
+// MoE routing permute: token row m of x [T,H] quantised once, its codes and scale written to the
+// routed rows dst[m*k + j] (j < k; an index < 0 is skipped).  out: 0 int8 into q, 1 fp16 into q_f16,
+// 2 both.
+cudaError_t launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, const int32_t* dst, int k, int8_t* q,
+                                 uint16_t* q_f16, float* scale, int out, cudaStream_t stream, int num_sms);
+
+// MoE routing (route.cu).  Stable counting sort of the T*k (token, slot) pairs by expert.
+// counts: int32 scratch of route_scratch_ints(T*k, E) entries.
+int64_t route_scratch_ints(int64_t n, int64_t E);
+cudaError_t launch_route(const int64_t* topk_ids, int64_t n, int E, int32_t* counts, int64_t* group_list,
+                         int32_t* pos, DeviceStatus* status, cudaStream_t stream);
+// Routed copies of already-quantised token rows: xq_tok [T,H] int8 + xs_tok [T] -> rows dst[t*k + j].
+cudaError_t launch_scatter_rows_i8(const int8_t* xq_tok, const float* xs_tok, int64_t T, int64_t H,
+                                   const int32_t* dst, int k, int8_t* q, uint16_t* q_f16, float* scale, int out,
+                                   cudaStream_t stream, int num_sms);
+// Top-k weighted combine of the routed rows back into token rows.
+cudaError_t launch_combine(const uint16_t* y_routed, const int32_t* pos, const float* w, int64_t T, int k,
+                           int64_t H, uint16_t* y, DeviceStatus* status, cudaStream_t stream);
+
 // Epilogue of the contraction.
 enum EpiMode : int {
   EPI_BF16 = 0,    // y[r,n] = bf16(((float)acc * sx[r]) * sw[e,n] (+ bias[n]))

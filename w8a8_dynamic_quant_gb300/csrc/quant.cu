@@ -9,6 +9,9 @@
 //   -127, 127) with ties to even; an all-zero row gets s = 0, q = 0.
 //
 // HBM-bound: 2 bytes read + 1 byte written per element (+4 bytes per row).
+// The MoE routing permute uses the same kernels with a scatter: a token row is
+// quantised once and its codes and scale go to each of its k routed rows (the
+// DeepEP INT8 dispatch of §三 quantises before it sends).
 // Each row is read once with 16-byte vector loads and held in registers
 // between the absmax pass and the quantise pass; absmax is reduced with warp
 // shuffles (and shared memory across the warps of a CTA).
@@ -91,14 +94,44 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   return r;
 }
 
+// Where a quantised row goes.  Plain quantisation: row m of the output.  Scatter (the MoE routing
+// permute): the k routed rows dst[m*k + j], j < k, of token m, each getting the same codes and scale;
+// a routed row index < 0 (a pair whose expert id was rejected) is skipped.
+template <bool SC>
+struct RowDst {
+  const int32_t* dst;
+  int k;
+  __device__ __forceinline__ int n() const { return SC ? k : 1; }
+  __device__ __forceinline__ int64_t row(int64_t m, int j) const {
+    return SC ? static_cast<int64_t>(dst[m * k + j]) : m;
+  }
+};
+
 // OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both (each code computed once).
 // s = rs = 0 (an all-zero row) gives zero codes.
+template <int OUT, bool SC>
 __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_t row, int64_t K, int64_t idx,
-                                       void* q, uint16_t* q16, int out) {
+                                       void* q, uint16_t* q16, const RowDst<SC>& d) {
   float m[8];
   codes8(v, s, rs, m);
-  if (out != 1) reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K)[idx] = pack_i8(m);
-  if (out != 0) reinterpret_cast<uint4*>(q16 + row * K)[idx] = pack_f16(m);
+  uint2 c = make_uint2(0u, 0u);
+  uint4 f = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (OUT != 1) c = pack_i8(m);
+  if constexpr (OUT != 0) f = pack_f16(m);
+  for (int j = 0; j < d.n(); ++j) {
+    const int64_t r = d.row(row, j);
+    if (r < 0) continue;
+    if (OUT != 1) reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + r * K)[idx] = c;
+    if (OUT != 0) reinterpret_cast<uint4*>(q16 + r * K)[idx] = f;
+  }
+}
+
+template <bool SC>
+__device__ __forceinline__ void store_scale(float s, int64_t row, float* scale, const RowDst<SC>& d) {
+  for (int j = 0; j < d.n(); ++j) {
+    const int64_t r = d.row(row, j);
+    if (r >= 0) scale[r] = s;
+  }
 }
 
 // Every quantisation kernel is launched with programmatic stream serialization
@@ -120,10 +153,10 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).  At least four CTAs (32 warps, 32 rows of
 // loads in flight) per SM.
-template <int CH, int OUT>
+template <int CH, int OUT, bool SC>
 __global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
                                                        int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                       float* __restrict__ scale) {
+                                                       float* __restrict__ scale, RowDst<SC> d) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = K / 8;
@@ -143,12 +176,12 @@ __global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __rest
     amax = warp_max(amax);
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (lane == 0) scale[row] = s;
+    if (lane == 0) store_scale(s, row, scale, d);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = lane + 32 * c;
       if (idx < nchunk) {
-        store8(v[c], s, rs, row, K, idx, q, q16, OUT);
+        store8<OUT>(v[c], s, rs, row, K, idx, q, q16, d);
       }
     }
   }
@@ -157,10 +190,10 @@ __global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __rest
 // One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).  A CTA takes rows
 // blockIdx.x, + gridDim.x, ...; the loads of its next row are issued before the current one is reduced
 // and quantised, so an SM keeps reading while it computes.
-template <int CH, int OUT>
+template <int CH, int OUT, bool SC>
 __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                      float* __restrict__ scale) {
+                                                      float* __restrict__ scale, RowDst<SC> d) {
   pdl_enter();
   __shared__ float red[2][8];
   const int64_t nchunk = K / 8;
@@ -189,11 +222,11 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[buf][w]);
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (threadIdx.x == 0) scale[row] = s;
+    if (threadIdx.x == 0) store_scale(s, row, scale, d);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int64_t idx = threadIdx.x + 256 * c;
-      if (idx < nchunk) store8(v[c], s, rs, row, K, idx, q, q16, OUT);
+      if (idx < nchunk) store8<OUT>(v[c], s, rs, row, K, idx, q, q16, d);
     }
 #pragma unroll
     for (int c = 0; c < CH; ++c) v[c] = vn[c];
@@ -202,10 +235,10 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
 }
 
 // Any K: two passes over the row (the second read mostly hits L2).
-template <int OUT>
+template <int OUT, bool SC>
 __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __restrict__ x, int64_t M,
                                                           int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                          float* __restrict__ scale) {
+                                                          float* __restrict__ scale, RowDst<SC> d) {
   pdl_enter();
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
@@ -221,21 +254,22 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (threadIdx.x == 0) scale[row] = s;
+    if (threadIdx.x == 0) store_scale(s, row, scale, d);
     for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) {
-      store8(xr[idx], s, rs, row, K, idx, q, q16, OUT);
+      store8<OUT>(xr[idx], s, rs, row, K, idx, q, q16, d);
     }
     __syncthreads();
   }
 }
 
-// CTAs of quant_cta_rows<CH, OUT> resident per SM (queried once).
-template <int CH, int OUT>
+// CTAs of quant_cta_rows<CH, OUT, SC> resident per SM (queried once).
+template <int CH, int OUT, bool SC>
 int cta_rows_per_sm() {
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_cta_rows<CH, OUT>, 256, 0) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_cta_rows<CH, OUT, SC>, 256, 0) != cudaSuccess ||
+        n < 1) {
       cudaGetLastError();
       n = 1;
     }
@@ -244,9 +278,9 @@ int cta_rows_per_sm() {
   return per_sm;
 }
 
-template <int OUT>
+template <int OUT, bool SC>
 cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale,
-                           cudaStream_t stream, int num_sms) {
+                           RowDst<SC> d, cudaStream_t stream, int num_sms) {
   if (M == 0) return cudaSuccess;
   const int64_t nchunk = K / 8;
   const int64_t max_grid = static_cast<int64_t>(num_sms) * 64;
@@ -255,10 +289,10 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
     const int ch = static_cast<int>((nchunk + 31) / 32);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
-    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
-    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
-    else return launch_pdl(quant_warp_rows<8, OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
+    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    else return launch_pdl(quant_warp_rows<8, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
   } else {
     // as many CTAs as are resident at once; each then works through its rows
     const int ch = static_cast<int>((nchunk + 255) / 256);
@@ -266,11 +300,17 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     auto grid = [&](int per_sm) {
       return dim3(static_cast<unsigned>(std::min<int64_t>(M, static_cast<int64_t>(num_sms) * per_sm)));
     };
-    if (ch <= 2) return launch_pdl(quant_cta_rows<2, OUT>, grid(cta_rows_per_sm<2, OUT>()), b, 0, stream, x, M, K, q, q16, scale);
-    if (ch <= 4) return launch_pdl(quant_cta_rows<4, OUT>, grid(cta_rows_per_sm<4, OUT>()), b, 0, stream, x, M, K, q, q16, scale);
-    if (ch <= 8) return launch_pdl(quant_cta_rows<8, OUT>, grid(cta_rows_per_sm<8, OUT>()), b, 0, stream, x, M, K, q, q16, scale);
+    if (ch <= 2)
+      return launch_pdl(quant_cta_rows<2, OUT, SC>, grid(cta_rows_per_sm<2, OUT, SC>()), b, 0, stream, x, M, K, q,
+                        q16, scale, d);
+    if (ch <= 4)
+      return launch_pdl(quant_cta_rows<4, OUT, SC>, grid(cta_rows_per_sm<4, OUT, SC>()), b, 0, stream, x, M, K, q,
+                        q16, scale, d);
+    if (ch <= 8)
+      return launch_pdl(quant_cta_rows<8, OUT, SC>, grid(cta_rows_per_sm<8, OUT, SC>()), b, 0, stream, x, M, K, q,
+                        q16, scale, d);
     const dim3 g(static_cast<unsigned>(std::min<int64_t>(M, max_grid)));
-    return launch_pdl(quant_cta_rows_any<OUT>, g, b, 0, stream, x, M, K, q, q16, scale);
+    return launch_pdl(quant_cta_rows_any<OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
   }
 }
 
@@ -278,12 +318,20 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
 
 cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                  cudaStream_t stream, int num_sms) {
-  return launch_quant_t<0>(x, M, K, q, nullptr, scale, stream, num_sms);
+  return launch_quant_t<0>(x, M, K, q, nullptr, scale, RowDst<false>{nullptr, 1}, stream, num_sms);
 }
 
 cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
                                       float* scale, cudaStream_t stream, int num_sms) {
-  return launch_quant_t<2>(x, M, K, q, q_f16, scale, stream, num_sms);
+  return launch_quant_t<2>(x, M, K, q, q_f16, scale, RowDst<false>{nullptr, 1}, stream, num_sms);
+}
+
+cudaError_t launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, const int32_t* dst, int k, int8_t* q,
+                                 uint16_t* q_f16, float* scale, int out, cudaStream_t stream, int num_sms) {
+  const RowDst<true> d{dst, k};
+  if (out == 0) return launch_quant_t<0>(x, T, H, q, nullptr, scale, d, stream, num_sms);
+  if (out == 1) return launch_quant_t<1>(x, T, H, nullptr, q_f16, scale, d, stream, num_sms);
+  return launch_quant_t<2>(x, T, H, q, q_f16, scale, d, stream, num_sms);
 }
 
 }  // namespace w8a8
