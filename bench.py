@@ -265,7 +265,7 @@ class Dense:
 class MoE:
     """MoE expert FFN: (quant) -> W13 grouped GEMM + SwiGLU -> requant -> W2 grouped GEMM."""
 
-    def __init__(self, cfg_id: int, device):
+    def __init__(self, cfg_id: int, device, pack_weights: bool = True):
         import numpy as np
         import torch
         import w8a8_dynamic_quant_gb300 as W
@@ -276,8 +276,8 @@ class MoE:
         self.name = m.name
         self.n_sets = 1
         f16 = W.PACK_F16 if m.R >= 64 * m.E else 0  # prefill-sized groups: tcgen05 engine
-        self.w13p = W.w8a8_prepack_weight(m.w13, W.PACK_GATE_UP | f16)
-        self.w2p = W.w8a8_prepack_weight(m.w2, f16)
+        self.w13p = W.w8a8_prepack_weight(m.w13, W.PACK_GATE_UP | f16) if pack_weights else None
+        self.w2p = W.w8a8_prepack_weight(m.w2, f16) if pack_weights else None
         self.gl = torch.from_numpy(m.group_list).to(device)
         self.s13 = torch.from_numpy(m.s13).to(device)
         self.s2 = torch.from_numpy(m.s2).to(device)
@@ -373,9 +373,136 @@ class MoE:
         return self.m.R
 
 
-def make_workload(cfg_id, device):
+class MoETokens(MoE):
+    """The MoE layer from token rows and router output: routing permute + quant -> the expert chain ->
+    top-k weighted combine (one moe_layer call).  The permute and the combine are also timed alone,
+    through their own calls, for their HBM rooflines."""
+
+    def __init__(self, cfg_id: int, device, kernels=None):
+        # the routing kernels alone (profiling) need no packed weights
+        super().__init__(cfg_id, device, pack_weights=kernels is None or "moe_layer" in kernels)
+        W, torch, m = self.W, self.torch, self.m
+        T, k, H, I, E, R = m.T, m.topk, m.H, m.I, m.E, m.R
+        self.name = m.name + "_from_tokens"
+        if m.x_tok_scale is None:
+            self.xt = torch.from_numpy(m.x_tok.view("int16")).to(device).view(torch.bfloat16)
+            self.xts = None
+        else:
+            self.xt = torch.from_numpy(m.x_tok).to(device)
+            self.xts = torch.from_numpy(m.x_tok_scale).to(device)
+        self.ids = torch.from_numpy(m.topk_ids).to(device)
+        self.tw = torch.from_numpy(m.topk_weights).to(device)
+        self.lws = W.workspace(W.moe_layer_workspace_bytes(T, k, H, I, E), device)
+        self.yt = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        # buffers of the permute and combine timed alone
+        self.rws = W.workspace(W.moe_route_workspace_bytes(T, k, E), device)
+        self.pq_out = (torch.empty((R, H), dtype=torch.int8, device=device),
+                       torch.empty((R,), dtype=torch.float32, device=device),
+                       torch.empty((E,), dtype=torch.int64, device=device),
+                       torch.empty((T, k), dtype=torch.int32, device=device))
+        self.cws = W.workspace(256, device)
+        self.yr = torch.empty((R, H), dtype=torch.bfloat16, device=device)
+        self.yc = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        self.kernels = ["moe_layer", "moe_permute_quant", "moe_unpermute_combine"]
+        self.step_kernels = ["moe_layer"]
+        if kernels is not None:  # profiling: only the named calls, each one a step
+            self.kernels = [k for k in self.kernels if k in kernels]
+            self.step_kernels = list(self.kernels)
+        xin = T * H * (1 if m.x_tok_scale is not None else 2) + (4 * T if m.x_tok_scale is not None else 0)
+        route = 8 * R + 4 * R + 8 * E  # ids read, routed row index written, group list
+        permute = xin + route + R * H + 4 * R  # token rows in, int8 routed rows + scales out
+        combine = 2 * R * H + 8 * R + 2 * T * H  # routed rows, weights and indices in, token rows out
+        chain = self.alg_bytes["moe_layer"] - R * H * (1 if m.x_scale is not None else 2 + 1 + 1)
+        # the layer: token rows in, routed codes written once and read by W13, chain, combine
+        self.alg_bytes = {"moe_layer": xin + route + 2 * R * H + 4 * R + chain + combine,
+                          "moe_permute_quant": permute, "moe_unpermute_combine": combine}
+        route = 1 if R <= 8192 else 3  # one-CTA sort for decode-sized batches, else count / scan / assign
+        per_call = {"moe_layer": route + 1 + 3 + 1,  # route, permute, W13 + requant + W2, combine
+                    "moe_permute_quant": route + 1, "moe_unpermute_combine": 1}
+        self.launches_per_step = sum(per_call[k] for k in self.step_kernels)
+        if "moe_layer" not in self.step_kernels:
+            self.bound = "hbm"
+
+    def launch(self, kernel: str, i: int):
+        W = self.W
+        if kernel == "moe_layer":
+            W.moe_layer(self.xt, self.xts, self.ids, self.tw, self.w13p, self.s13, self.w2p, self.s2, self.lws,
+                        self.yt)
+        elif kernel == "moe_permute_quant":
+            W.moe_permute_quant(self.xt, self.xts, self.ids, self.m.E, self.rws, out=self.pq_out)
+        else:
+            W.moe_unpermute_combine(self.yr, self.pq_out[3], self.tw, self.cws, self.yc)
+
+    def config(self):
+        c = super().config()
+        c["workload"] = self.name
+        c["input"] = "token rows [T,H] + top-k ids and weights [T,topk]"
+        return c
+
+    def e2e_setup(self, device):
+        torch, m = self.torch, self.m
+        if m.x_tok_scale is None:
+            self.hx = torch.from_numpy(m.x_tok.view("int16")).view(torch.bfloat16).pin_memory()
+            self.hxs = None
+        else:
+            self.hx = torch.from_numpy(m.x_tok).pin_memory()
+            self.hxs = torch.from_numpy(m.x_tok_scale).pin_memory()
+        self.hids = torch.from_numpy(m.topk_ids).pin_memory()
+        self.htw = torch.from_numpy(m.topk_weights).pin_memory()
+        self.hy = torch.empty((m.T, m.H), dtype=torch.bfloat16).pin_memory()
+        self.h2d = self.hx.numel() * self.hx.element_size() + (0 if self.hxs is None else self.hxs.numel() * 4) + \
+            self.hids.numel() * 8 + self.htw.numel() * 4
+        self.d2h = self.hy.numel() * 2
+
+    def e2e_step(self):
+        self.xt.copy_(self.hx, non_blocking=True)
+        if self.hxs is not None:
+            self.xts.copy_(self.hxs, non_blocking=True)
+        self.ids.copy_(self.hids, non_blocking=True)
+        self.tw.copy_(self.htw, non_blocking=True)
+        if "moe_layer" in self.step_kernels:
+            y = self.W.moe_layer(self.xt, self.xts, self.ids, self.tw, self.w13p, self.s13, self.w2p, self.s2,
+                                 self.lws, self.yt)
+        else:  # profiling runs of the routing calls alone
+            for k in self.step_kernels:
+                self.launch(k, 0)
+            y = self.yc
+        self.hy.copy_(y, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    # CPU oracle on a subset of tokens (units = tokens)
+    def oracle_units(self, rows):
+        return rows
+
+    def _token_subset(self, n):
+        cache = getattr(self, "_tok_cache", {})
+        self._tok_cache = cache
+        if n not in cache:
+            np, m = self.np, self.m
+            toks = np.unique(np.linspace(0, m.T - 1, n).astype(np.int64))
+            ids = m.topk_ids[toks]
+            experts = np.unique(ids)
+            idx = self.torch.as_tensor(experts, device=m.w13.device)
+            cache[n] = (m.x_tok[toks], None if m.x_tok_scale is None else m.x_tok_scale[toks],
+                        np.searchsorted(experts, ids).astype(np.int64), m.topk_weights[toks],
+                        m.w13.index_select(0, idx).cpu().numpy(), m.s13[experts],
+                        m.w2.index_select(0, idx).cpu().numpy(), m.s2[experts])
+        return cache[n]
+
+    def oracle_step(self, rows):
+        import oracle
+        oracle.moe_layer(*self._token_subset(rows))
+
+    @property
+    def oracle_full_rows(self):
+        return self.m.T
+
+
+def make_workload(cfg_id, device, from_tokens=False, kernels=None):
     from w8a8_dynamic_quant_gb300 import synthetic as S
-    return Dense(cfg_id, device) if S.CONFIGS[cfg_id]["kind"] == "dense" else MoE(cfg_id, device)
+    if S.CONFIGS[cfg_id]["kind"] == "dense":
+        return Dense(cfg_id, device)
+    return MoETokens(cfg_id, device, kernels) if from_tokens else MoE(cfg_id, device)
 
 
 # -------------------------------------------------------------- the arms --
@@ -415,7 +542,7 @@ def run_reference(args):
     if S.CONFIGS[args.workload]["kind"] == "dense":
         wl = _HostDense(args.workload)
     else:
-        wl = _HostMoE(args.workload)
+        wl = _HostMoETokens(args.workload) if args.from_tokens else _HostMoE(args.workload)
     for _ in range(args.warmup):
         wl.oracle_step(wl.step_rows)
     t0 = time.perf_counter()
@@ -461,6 +588,19 @@ class _HostMoE(MoE):
         self.step_rows = 8
 
 
+class _HostMoETokens(MoETokens):
+    def __init__(self, cfg_id):
+        import numpy as np
+        import torch
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        self.np, self.torch = np, torch
+        self.m = S.moe_config(cfg_id, device="cpu")
+        self.name = self.m.name + "_from_tokens"
+        self.unit = "tokens/s"
+        self.input_note = "host arrays (CPU oracle)"
+        self.step_rows = 1  # tokens (each with topk routed rows)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -473,7 +613,9 @@ def run_gpu(args):
     import __graft_entry__
     __graft_entry__.build()
     peaks = load_peaks()
-    wl = make_workload(args.workload, device)
+    kernels = args.kernels.split(",") if args.kernels else None
+    wl = make_workload(args.workload, device, args.from_tokens, kernels)
+    step_kernels = getattr(wl, "step_kernels", wl.kernels)
     stream = torch.cuda.current_stream(device)
 
     # one CUDA graph per kernel type over all rotating input sets
@@ -495,7 +637,7 @@ def run_gpu(args):
     step_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(step_graph):
         for i in range(wl.n_sets):
-            for k in wl.kernels:
+            for k in step_kernels:
                 wl.launch(k, i)
     torch.cuda.synchronize()
 
@@ -552,7 +694,7 @@ def run_gpu(args):
     e_units, e_seconds = aggregate(wl.units_per_step * e2e_steps, e2e_s)
 
     # dominant kernel roofline
-    dom = max(per_kernel_ms, key=per_kernel_ms.get)
+    dom = max(step_kernels, key=per_kernel_ms.get)
     dur_s = per_kernel_ms[dom] / 1e3
     if wl.bound == "hbm":
         achieved = wl.alg_bytes[dom] / dur_s / 1e9
@@ -566,11 +708,18 @@ def run_gpu(args):
                 if peaks["source"] == "measured" else "fallback",
                 "alg_bytes_per_launch": wl.alg_bytes[dom],
                 "per_kernel_us": {k: v * 1e3 for k, v in per_kernel_ms.items()},
-                "sum_of_kernels_us": sum(per_kernel_ms.values()) * 1e3}
+                "sum_of_kernels_us": sum(per_kernel_ms[k] for k in step_kernels) * 1e3}
     if "dynamic_quant" in per_kernel_ms:
         roofline["quant_gbs"] = wl.alg_bytes["dynamic_quant"] / (per_kernel_ms["dynamic_quant"] / 1e3) / 1e9
     if dom in wl.alg_flops:
         roofline["tops_dominant"] = wl.alg_flops[dom] / dur_s / 1e12
+    # the routing kernels timed alone (HBM-bound)
+    for k in wl.kernels:
+        if k in step_kernels:
+            continue
+        gbs = wl.alg_bytes[k] / (per_kernel_ms[k] / 1e3) / 1e9
+        roofline.setdefault("others", {})[k] = {"us": per_kernel_ms[k] * 1e3, "alg_bytes": wl.alg_bytes[k],
+                                                "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
 
     line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,
             "warmup": rounds_w * wl.n_sets, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -599,6 +748,12 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--from-tokens", action="store_true",
+                    help="MoE workloads: the layer from token rows and router output (routing permute + quant, "
+                         "expert chain, top-k weighted combine) instead of expert-sorted routed rows")
+    ap.add_argument("--kernels", default=None,
+                    help="with --from-tokens: time only these calls (comma list of moe_layer, moe_permute_quant, "
+                         "moe_unpermute_combine), for profiler captures")
     ap.add_argument("--quick", action="store_true",
                     help="short run for profiler captures: no clock-sampling hold, 3 e2e steps")
     args = ap.parse_args(argv)

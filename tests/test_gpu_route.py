@@ -48,7 +48,10 @@ def gpu_permute(x, xs, ids, E):
 @pytest.mark.parametrize("T,k,E,H,distinct", [(1, 1, 1, 16, True), (7, 2, 3, 64, True),
                                               (300, 8, 64, 512, True), (1000, 3, 5, 96, False),
                                               (171, 4, 1024, 272, True), (2500, 1, 7, 128, True),
-                                              (33, 6, 6, 4096, True)])
+                                              (33, 6, 6, 4096, True),
+                                              # past the one-CTA sort: more than 65536 pairs, or 1024 experts
+                                              # with 40000 pairs (its shared memory would pass 200 KB)
+                                              (20000, 4, 64, 64, True), (10000, 4, 1024, 16, True)])
 @pytest.mark.parametrize("prequant", [False, True])
 def test_permute_quant_exact(T, k, E, H, distinct, prequant):
     ids = ids_for(T, k, E, seed=T * 7 + E, distinct=distinct)
@@ -71,8 +74,9 @@ def test_permute_quant_no_tokens():
     assert gl.cpu().tolist() == [0] * 5
 
 
-def test_permute_quant_bad_id_is_reported():
-    T, k, E, H = 600, 2, 8, 64
+@pytest.mark.parametrize("T", [600, 40000])
+def test_permute_quant_bad_id_is_reported(T):
+    k, E, H = 2, 8, 64
     ids = ids_for(T, k, E, seed=3)
     ids[555, 1] = E       # past the last expert
     ids[20, 0] = -4       # negative
@@ -90,7 +94,8 @@ def test_permute_quant_bad_id_is_reported():
     assert np.array_equal(np.sort(pos[good]), np.arange(T * k - 2))
 
 
-@pytest.mark.parametrize("T,k,H", [(1, 1, 8), (5, 9, 1040), (300, 8, 4096), (129, 3, 2056), (64, 8, 7168)])
+@pytest.mark.parametrize("T,k,H", [(1, 1, 8), (5, 9, 1040), (300, 8, 4096), (129, 3, 2056), (64, 8, 7168),
+                                   (2, 17, 24), (3000, 2, 1024)])
 def test_combine_exact(T, k, H):
     rng = np.random.default_rng(T + k + H)
     ids = ids_for(T, k, max(k, 11), seed=T)

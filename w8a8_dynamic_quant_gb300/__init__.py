@@ -241,10 +241,10 @@ def moe_route_workspace_bytes(T: int, k: int, E: int) -> int:
 
 
 def moe_permute_quant(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_ids: torch.Tensor, E: int,
-                      ws: Optional[torch.Tensor] = None):
+                      ws: Optional[torch.Tensor] = None, out=None):
     """Token rows -> routed rows grouped by expert.  x bf16 [T,H] (x_scale None: each token quantised
     once) or int8 [T,H] with x_scale [T]; topk_ids int64 [T,k].  Returns (int8 xq [T*k,H],
-    float32 xs [T*k], int64 group_list [E], int32 pos [T,k])."""
+    float32 xs [T*k], int64 group_list [E], int32 pos [T,k]), written into `out` when given."""
     T, H = x.shape
     dev = x.device
     if x_scale is None:
@@ -258,10 +258,16 @@ def moe_permute_quant(x: torch.Tensor, x_scale: Optional[torch.Tensor], topk_ids
     k = topk_ids.shape[1]
     ws = workspace(moe_route_workspace_bytes(T, k, E), dev) if ws is None else ws
     _need(ws, "ws", torch.uint8, None, dev)
-    xq = torch.empty((T * k, H), dtype=torch.int8, device=dev)
-    xs = torch.empty((T * k,), dtype=torch.float32, device=dev)
-    group_list = torch.empty((E,), dtype=torch.int64, device=dev)
-    pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if out is None:
+        out = (torch.empty((T * k, H), dtype=torch.int8, device=dev),
+               torch.empty((T * k,), dtype=torch.float32, device=dev),
+               torch.empty((E,), dtype=torch.int64, device=dev),
+               torch.empty((T, k), dtype=torch.int32, device=dev))
+    xq, xs, group_list, pos = out
+    _need(xq, "xq", torch.int8, (T * k, H), dev)
+    _need(xs, "xs", torch.float32, (T * k,), dev)
+    _need(group_list, "group_list", torch.int64, (E,), dev)
+    _need(pos, "pos", torch.int32, (T, k), dev)
     with torch.cuda.device(dev):
         _capi.check("moe_permute_quant", _capi.lib().moe_permute_quant(
             x.data_ptr(), _ptr(x_scale), topk_ids.data_ptr(), T, k, E, H, xq.data_ptr(), xs.data_ptr(),

@@ -198,7 +198,7 @@ w8a8_status check_route_shape(int64_t T, int64_t k, int64_t E) {
   return W8A8_OK;
 }
 
-// The combine launches one block per (token, 1024 columns).
+// The combine numbers its work items (token, 1024 columns) with 32-bit integers.
 bool combine_grid_ok(int64_t T, int64_t H) { return T * ((H / 8 + 127) / 128) <= INT32_MAX; }
 
 // One contraction on the engine its shape calls for: tcgen05 (activations
@@ -558,7 +558,7 @@ w8a8_status moe_unpermute_combine(const uint16_t* y_routed, const int32_t* pos, 
   int sms = 0;
   if (w8a8_status s = device_info(sms)) return s;
   return cuda_status(launch_combine(y_routed, pos, topk_weights, T, static_cast<int>(k), H, y,
-                                    static_cast<DeviceStatus*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+                                    static_cast<DeviceStatus*>(ws), reinterpret_cast<cudaStream_t>(stream), sms));
 }
 
 size_t moe_layer_workspace_bytes(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E) {
@@ -620,7 +620,7 @@ w8a8_status moe_layer(const void* x, const float* x_scale, const int64_t* topk_i
   if (w8a8_status e = moe_chain(xq, xs, true, gl, E, R, H, I, w13_packed, w13_scale, w2_packed, w2_scale, ws, yr,
                                 st, sms))
     return e;
-  return cuda_status(launch_combine(yr, pos, topk_weights, T, kk, H, y, status, st));
+  return cuda_status(launch_combine(yr, pos, topk_weights, T, kk, H, y, status, st, sms));
 }
 
 w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream) {

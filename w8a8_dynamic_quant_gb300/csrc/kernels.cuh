@@ -40,7 +40,7 @@ cudaError_t launch_scatter_rows_i8(const int8_t* xq_tok, const float* xs_tok, in
                                    cudaStream_t stream, int num_sms);
 // Top-k weighted combine of the routed rows back into token rows.
 cudaError_t launch_combine(const uint16_t* y_routed, const int32_t* pos, const float* w, int64_t T, int k,
-                           int64_t H, uint16_t* y, DeviceStatus* status, cudaStream_t stream);
+                           int64_t H, uint16_t* y, DeviceStatus* status, cudaStream_t stream, int num_sms);
 
 // Epilogue of the contraction.
 enum EpiMode : int {
