@@ -69,6 +69,7 @@ def _load(path: str) -> ctypes.CDLL:
     L.oracle_moe_w13_swiglu_requant_w2.argtypes = [
         _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, _vp,
         _vp, _vp, _vp, _vp, _vp, _vp]
+    L.oracle_quantize_weight.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
     L.oracle_moe_route.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
     L.oracle_moe_permute_quant.argtypes = [_vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp,
                                            _vp, _vp]
@@ -226,6 +227,17 @@ def moe_w13_swiglu_requant_w2(x, x_scale, group_list, w13, s13, w2, s2, intermed
                _p(inter.get("xq")), _p(inter.get("xs")), _p(inter.get("y13")),
                _p(inter.get("h")), _p(inter.get("hq")), _p(inter.get("hs"))))
     return (y, inter) if intermediates else y
+
+
+def quantize_weight(w):
+    """bf16 bits W [N,K] or [E,N,K] -> (int8 q of the same shape, fp32 per-channel scales [N] or [E,N])."""
+    w = _c(w, np.uint16)
+    w3 = w.reshape((1,) + w.shape) if w.ndim == 2 else w
+    E, N, K = w3.shape
+    q = np.empty((E, N, K), np.int8)
+    s = np.empty((E, N), np.float32)
+    _check("oracle_quantize_weight", lib().oracle_quantize_weight(_p(w3), E, N, K, _p(q), _p(s)))
+    return (q[0], s[0]) if w.ndim == 2 else (q, s)
 
 
 def moe_route(topk_ids, E: int):

@@ -243,6 +243,30 @@ int oracle_quant_matmul(const int8_t* q, const float* x_scale, int64_t M, int64_
   return ORC_OK;
 }
 
+/* ------------------------------------------- per-channel weight quant -- */
+/*
+ * [P1] §一 (msModelSlim recipe: weight scope per_channel, dtype int8,
+ * symmetric) and §二 (the checkpoint weight [N,K] is already INT8 at load:
+ * the quantisation happened offline, from the BF16 weight).
+ * READING: per channel = per output channel n, over its K inputs; the
+ * symmetric recipe is the activation one: s[n] = amax_k |W[n,k]| / 127,
+ * q = clamp(rint(W / s), -127, 127), ties to even; an all-zero channel gets
+ * s = 0 and q = 0.  W is BF16 [E,N,K] (E = 1 for a dense layer); scales are
+ * fp32 [E,N] in channel order.
+ */
+int oracle_quantize_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K, int8_t* q, float* scale) {
+  if (E <= 0 || N <= 0 || K <= 0) return ORC_ERR_SHAPE;
+  for (int64_t e = 0; e < E; ++e) {
+    /* each expert's N channels, one at a time: the per-row quantiser on one row */
+    for (int64_t n = 0; n < N; ++n) {
+      const int64_t row = e * N + n;
+      const int rc = oracle_dynamic_quant(w + row * K, 1, K, q + row * K, scale + row);
+      if (rc) return rc;
+    }
+  }
+  return ORC_OK;
+}
+
 /* ---------------------------------------------------------- grouped GEMM -- */
 
 int oracle_check_group_list(const int64_t* group_list, int64_t E, int64_t R) {

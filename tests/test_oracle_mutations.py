@@ -44,6 +44,8 @@ MUTATIONS = [
      "test_permute_quant_is_quant_of_the_gathered_rows", (True,)),
     ("combine drops the last choice", "for (int64_t j = 0; j < k; ++j) {\n        const float v",
      "for (int64_t j = 0; j + 1 < k; ++j) {\n        const float v", "test_combine_against_float64", ()),
+    ("weight channel read from the first expert", "oracle_dynamic_quant(w + row * K, 1, K, q + row * K, scale + row);",
+     "oracle_dynamic_quant(w + n * K, 1, K, q + row * K, scale + row);", "test_weight_quant_is_per_output_channel", ()),
     ("combine sums in double", "      float s = 0.0f;\n      for (int64_t j", "      double s = 0.0;\n      for (int64_t j",
      "test_combine_closed_forms_and_order", ()),
 ]

@@ -497,3 +497,31 @@ def test_moe_layer_routed_output_and_float64_combine(prequant):
         exact = sum(float(m.topk_weights[t, j]) * v[rows[j]] for j in range(m.topk))
         got = f32(y[t]).astype(np.float64)
         assert np.all(np.abs(got - exact) <= bf16_ulp(exact) * 0.51 + 1e-6 * np.abs(v[rows]).sum(0))
+
+
+# ------------------------------------------------- per-channel weight quant ----
+
+def test_weight_quant_is_per_output_channel():
+    """Channels (rows of W [N,K]) with very different ranges get their own scales: s[n] = max_k |W[n,k]| / 127
+    (a per-tensor or per-input-column scale would give other values), the codes reproduce W within s/2, and
+    each channel's largest element maps to +-127."""
+    rng = np.random.default_rng(21)
+    E, N, K = 3, 40, 96
+    mags = (2.0 ** rng.integers(-6, 6, (E, N, 1))).astype(np.float32)
+    w = S.to_bf16_bits(rng.standard_normal((E, N, K)).astype(np.float32) * mags)
+    w[1, 5] = 0  # an all-zero channel: scale 0, codes 0
+    q, s = oracle.quantize_weight(w)
+    wf = f32(w).astype(np.float64)
+    amax = np.abs(wf).max(axis=2)
+    assert np.array_equal(s, (amax / 127.0).astype(np.float32))  # exact: binary32 divide of an exact amax
+    assert np.all(q[1, 5] == 0) and s[1, 5] == 0
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    err = np.abs(wf - q.astype(np.float64) * s[..., None].astype(np.float64))
+    assert np.all(err <= s[..., None].astype(np.float64) * (0.5 + 127 * 2.0 ** -24) + 1e-30)
+    big = np.argmax(np.abs(wf), axis=2)
+    top = np.take_along_axis(q, big[..., None], axis=2)[..., 0]
+    live = amax > 0
+    assert np.all(np.abs(top[live]) == 127)
+    # a 2-D weight is one expert
+    q2, s2 = oracle.quantize_weight(w[2])
+    assert np.array_equal(q2, q[2]) and np.array_equal(s2, s[2])
