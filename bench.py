@@ -504,8 +504,95 @@ class MoETokens(MoE):
         return self.m.T
 
 
-def make_workload(cfg_id, device, from_tokens=False, kernels=None):
+class WeightPrep:
+    """Offline weight quantisation (per output channel, symmetric INT8) from BF16, written straight into
+    the packed buffers the contractions read: the workload's dense weight, or its W13 and W2 stacks."""
+
+    def __init__(self, cfg_id: int, device, host_only: bool = False):
+        import numpy as np
+        import torch
+        import w8a8_dynamic_quant_gb300 as W
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        self.W, self.torch, self.np = W, torch, np
+        c = S.CONFIGS[cfg_id]
+        if c["kind"] == "dense":
+            f16 = W.PACK_F16 if c["M"] >= 128 else 0
+            self.shapes = [(1, c["N"], c["K"], f16)]
+        else:
+            R, E, H, I = c["T"] * c["topk"], c["E"], c["H"], c["I"]
+            f16 = W.PACK_F16 if R >= 64 * E else 0
+            self.shapes = [(E, 2 * I, H, W.PACK_GATE_UP | f16), (E, H, I, f16)]
+        self.name = "weight_quant_" + c["name"]
+        self.n_sets = 1
+        self.unit = "GB/s"
+        self.bound = "hbm"
+        self.kernels = ["quantize_prepack_weight"]
+        nbytes = sum(E * N * K * (2 + 1 + (2 if f & W.PACK_F16 else 0)) + 4 * E * N for E, N, K, f in self.shapes)
+        self.alg_bytes = {"quantize_prepack_weight": nbytes}
+        self.alg_flops = {}
+        self.units_per_step = float(nbytes)
+        self.launches_per_step = 2 * len(self.shapes)  # quantise-and-pack, header
+        self.channels = sum(E * N for E, N, _, _ in self.shapes)
+        total_bf16 = sum(2 * E * N * K for E, N, K, _ in self.shapes)
+        self.input_note = f"bf16 weights {total_bf16 / 1e9:.2f} GB > 129 MB L2 (single set)"
+        self.step_rows = 256
+        if host_only:
+            return
+        self.w = [S.make_bf16_weight(E, N, K, seed=i, device=str(device)) for i, (E, N, K, _) in enumerate(self.shapes)]
+        self.packed = [torch.empty(W.prepacked_bytes(E, N, K, f), dtype=torch.uint8, device=device)
+                       for E, N, K, f in self.shapes]
+        self.scales = [torch.empty((E, N), dtype=torch.float32, device=device) for E, N, _, _ in self.shapes]
+
+    def launch(self, kernel: str, i: int):
+        for w, (_, _, _, f), p, sc in zip(self.w, self.shapes, self.packed, self.scales):
+            self.W.w8a8_quantize_prepack_weight(w, f, p, sc)
+
+    def config(self):
+        return {"workload": self.name, "weights": [list(x[:3]) for x in self.shapes],
+                "flags": [x[3] for x in self.shapes], "source": "bf16", "seed": 0, "inputs": self.input_note}
+
+    def value(self, units, seconds):
+        return units / seconds / 1e9
+
+    def e2e_setup(self, device):
+        self.hw = [w.cpu().pin_memory() for w in self.w]
+        self.hs = [torch_s.cpu().pin_memory() for torch_s in self.scales]
+        self.h2d = sum(w.numel() * 2 for w in self.hw)
+        self.d2h = sum(x.numel() * 4 for x in self.hs)
+
+    def e2e_step(self):
+        for w, hw in zip(self.w, self.hw):
+            w.copy_(hw, non_blocking=True)
+        self.launch("quantize_prepack_weight", 0)
+        for sc, hs in zip(self.scales, self.hs):
+            hs.copy_(sc, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    # CPU oracle on `rows` output channels of the first weight (units: algorithmic bytes of those channels)
+    def oracle_units(self, rows):
+        E, N, K, f = self.shapes[0]
+        return rows * (K * (2 + 1 + (2 if f & self.W.PACK_F16 else 0)) + 4)
+
+    def oracle_step(self, rows):
+        import oracle
+        cache = getattr(self, "_host_cache", {})
+        self._host_cache = cache
+        if rows not in cache:
+            from w8a8_dynamic_quant_gb300 import synthetic as S
+            K = self.shapes[0][2]
+            w = S.make_bf16_weight(1, rows, K, seed=0, device="cpu")
+            cache[rows] = w.view(self.torch.int16).numpy().view(self.np.uint16)
+        oracle.quantize_weight(cache[rows])
+
+    @property
+    def oracle_full_rows(self):
+        return self.channels
+
+
+def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False):
     from w8a8_dynamic_quant_gb300 import synthetic as S
+    if prepare:
+        return WeightPrep(cfg_id, device)
     if S.CONFIGS[cfg_id]["kind"] == "dense":
         return Dense(cfg_id, device)
     return MoETokens(cfg_id, device, kernels) if from_tokens else MoE(cfg_id, device)
@@ -545,7 +632,9 @@ def run_reference(args):
     import oracle  # noqa: F401
     from w8a8_dynamic_quant_gb300 import synthetic as S
     # the oracle arm needs only host data: build the workload's host side on the CPU
-    if S.CONFIGS[args.workload]["kind"] == "dense":
+    if args.prepare:
+        wl = WeightPrep(args.workload, "cpu", host_only=True)
+    elif S.CONFIGS[args.workload]["kind"] == "dense":
         wl = _HostDense(args.workload)
     else:
         wl = _HostMoETokens(args.workload) if args.from_tokens else _HostMoE(args.workload)
@@ -620,7 +709,7 @@ def run_gpu(args):
     __graft_entry__.build()
     peaks = load_peaks()
     kernels = args.kernels.split(",") if args.kernels else None
-    wl = make_workload(args.workload, device, args.from_tokens, kernels)
+    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare)
     step_kernels = getattr(wl, "step_kernels", wl.kernels)
     stream = torch.cuda.current_stream(device)
 
@@ -761,6 +850,9 @@ def main(argv=None):
     ap.add_argument("--from-tokens", action="store_true",
                     help="MoE workloads: the layer from token rows and router output (routing permute + quant, "
                          "expert chain, top-k weighted combine) instead of expert-sorted routed rows")
+    ap.add_argument("--prepare", action="store_true",
+                    help="time the load-time weight preparation instead: the workload's weights quantised per "
+                         "channel from BF16 and packed in one pass (GB/s)")
     ap.add_argument("--kernels", default=None,
                     help="with --from-tokens: time only these calls (comma list of moe_layer, moe_permute_quant, "
                          "moe_unpermute_combine), for profiler captures")

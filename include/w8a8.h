@@ -112,6 +112,30 @@ W8A8_API w8a8_status w8a8_prepack_weight(const int8_t* w, int64_t E, int64_t N, 
                                 void* packed, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Offline weight quantisation -- [P1] §一 (the msModelSlim recipe: weight   */
+/* scope per_channel, dtype int8, symmetric) and §二 (the checkpoint weight  */
+/* is already INT8 when loaded: it was quantised once, offline, from BF16).  */
+/* Per output channel n of W [E,N,K] over its K inputs:                      */
+/* s[e,n] = max_k |W[e,n,k]| / 127 (binary32 divide),                        */
+/* q = clamp(rint(W / s), -127, 127), ties to even; an all-zero channel gets */
+/* s = 0 and q = 0 -- the activation recipe applied to each channel.         */
+/* ------------------------------------------------------------------------ */
+
+/* w [E,N,K] bf16 -> q [E,N,K] int8 (the checkpoint layout) and scale [E,N]
+ * fp32.  K % 16 == 0 (<= W8A8_MAX_K), w and q 16-byte aligned. */
+W8A8_API w8a8_status w8a8_quantize_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K, int8_t* q,
+                                          float* scale, w8a8_stream_t stream);
+
+/* The same quantisation written straight into a packed buffer (as
+ * w8a8_prepack_weight would pack the INT8 weight, flags alike: the W13
+ * gate/up interleave and the fp16 copy), one pass over the BF16 weight;
+ * scale [E,N] in the ORIGINAL channel order (what the contractions take).
+ * packed: w8a8_prepacked_bytes(E, N, K, flags) bytes, 256-byte aligned. */
+W8A8_API w8a8_status w8a8_quantize_prepack_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K,
+                                                  uint32_t flags, void* packed, float* scale,
+                                                  w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Dynamic per-token quantisation -- [P1] §二 npu_dynamic_quant and §三      */
 /* HiddenStatesDynamicQuant: amax = max_k |x[m,k]|, scale[m] = amax / 127    */
 /* (binary32 divide), q = clamp(rint(x / scale), -127, 127), rint = ties to  */

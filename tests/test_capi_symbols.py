@@ -84,6 +84,13 @@ def test_host_validation_rejects_before_launch(lib):
                                          fake, None) == 2  # I % 64 != 0
     assert lib.w8a8_prepack_weight(fake, 1, 130, 64, 1, ctypes.c_void_p(256), None) == 2  # gate/up needs I % 64 == 0
     assert lib.w8a8_prepack_weight(fake, 1, 128, 64, 8, ctypes.c_void_p(256), None) == 2  # unknown flag
+    # weight quantisation: K % 16, E out of range, unknown flag, gate/up needs (N/2) % 64, packed alignment
+    assert lib.w8a8_quantize_weight(fake, 1, 8, 24, fake, fake, None) == 3
+    assert lib.w8a8_quantize_weight(fake, 2000, 8, 32, fake, fake, None) == 2
+    assert lib.w8a8_quantize_weight(None, 1, 8, 32, fake, fake, None) == 1
+    assert lib.w8a8_quantize_prepack_weight(fake, 1, 128, 64, 8, ctypes.c_void_p(256), fake, None) == 2
+    assert lib.w8a8_quantize_prepack_weight(fake, 1, 130, 64, 1, ctypes.c_void_p(256), fake, None) == 2
+    assert lib.w8a8_quantize_prepack_weight(fake, 1, 128, 64, 0, ctypes.c_void_p(272), fake, None) == 3
     # routing: k < 1, E out of range, H % 16, T*k past int32, missing workspace
     big = 1 << 20
     assert lib.moe_permute_quant(fake, None, fake, 4, 0, 8, 64, fake, fake, fake, fake, fake, big, None) == 2

@@ -25,7 +25,7 @@ __all__ = [
     "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
     "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
-    "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
+    "w8a8_quantize_weight", "w8a8_quantize_prepack_weight", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
     "moe_layer_workspace_offset", "moe_layer",
 ]
 
@@ -77,6 +77,45 @@ def w8a8_prepack_weight(w: torch.Tensor, flags: int = 0) -> torch.Tensor:
         _capi.check("w8a8_prepack_weight", _capi.lib().w8a8_prepack_weight(
             w3.data_ptr(), E, N, K, flags, packed.data_ptr(), _stream(w.device)))
     return packed
+
+
+def _weight3(w: torch.Tensor):
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    if w3.dim() != 3:
+        raise ValueError("w must be [N,K] or [E,N,K]")
+    _need(w3, "w", torch.bfloat16)
+    return w3
+
+
+def w8a8_quantize_weight(w: torch.Tensor):
+    """BF16 weight [N,K] or [E,N,K] -> (int8 q of the same shape, float32 per-channel scales [N] / [E,N])."""
+    w3 = _weight3(w)
+    E, N, K = w3.shape
+    q = torch.empty((E, N, K), dtype=torch.int8, device=w.device)
+    scale = torch.empty((E, N), dtype=torch.float32, device=w.device)
+    with torch.cuda.device(w.device):
+        _capi.check("w8a8_quantize_weight", _capi.lib().w8a8_quantize_weight(
+            w3.data_ptr(), E, N, K, q.data_ptr(), scale.data_ptr(), _stream(w.device)))
+    return (q[0], scale[0]) if w.dim() == 2 else (q, scale)
+
+
+def w8a8_quantize_prepack_weight(w: torch.Tensor, flags: int = 0, packed: Optional[torch.Tensor] = None,
+                                 scale: Optional[torch.Tensor] = None):
+    """BF16 weight [N,K] or [E,N,K] -> (packed device buffer, float32 per-channel scales [N] / [E,N]),
+    quantised per channel and packed in one pass."""
+    w3 = _weight3(w)
+    E, N, K = w3.shape
+    nbytes = prepacked_bytes(E, N, K, flags)
+    if nbytes == 0:
+        raise ValueError("bad weight shape")
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=w.device) if packed is None else packed
+    _need(packed, "packed", torch.uint8, (nbytes,), w.device)
+    scale = torch.empty((E, N), dtype=torch.float32, device=w.device) if scale is None else scale.view(E, N)
+    _need(scale, "scale", torch.float32, (E, N), w.device)
+    with torch.cuda.device(w.device):
+        _capi.check("w8a8_quantize_prepack_weight", _capi.lib().w8a8_quantize_prepack_weight(
+            w3.data_ptr(), E, N, K, flags, packed.data_ptr(), scale.data_ptr(), _stream(w.device)))
+    return packed, (scale[0] if w.dim() == 2 else scale)
 
 
 def w8a8_dynamic_quant(x: torch.Tensor, q: Optional[torch.Tensor] = None,

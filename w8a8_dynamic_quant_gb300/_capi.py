@@ -23,6 +23,8 @@ SIGNATURES = {
     "w8a8_version": (_int, []),
     "w8a8_prepacked_bytes": (_sz, [_i64, _i64, _i64, _u32]),
     "w8a8_prepack_weight": (_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp]),
+    "w8a8_quantize_weight": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "w8a8_quantize_prepack_weight": (_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp]),
     "w8a8_dynamic_quant": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "w8a8_quant_matmul_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "w8a8_quant_matmul": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]),

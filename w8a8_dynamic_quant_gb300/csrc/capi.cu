@@ -365,6 +365,33 @@ w8a8_status w8a8_prepack_weight(const int8_t* w, int64_t E, int64_t N, int64_t K
   return st;
 }
 
+w8a8_status w8a8_quantize_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K, int8_t* q, float* scale,
+                                 w8a8_stream_t stream) {
+  if (!w || !q || !scale) return W8A8_ERR_NULL;
+  if (E <= 0 || N <= 0 || E > kMaxE || N > INT32_MAX || E * N > INT32_MAX) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (!aligned16(w) || !aligned16(q)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_dynamic_quant(w, E * N, K, q, scale, reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+w8a8_status w8a8_quantize_prepack_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags,
+                                         void* packed, float* scale, w8a8_stream_t stream) {
+  if (!w || !packed || !scale) return W8A8_ERR_NULL;
+  if (E <= 0 || N <= 0 || E > kMaxE || N > INT32_MAX || E * N > INT32_MAX) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (flags & ~(W8A8_PACK_GATE_UP | W8A8_PACK_F16)) return W8A8_ERR_SHAPE;
+  if ((flags & W8A8_PACK_GATE_UP) && (N % 2 != 0 || (N / 2) % kGateUpBlock != 0)) return W8A8_ERR_SHAPE;
+  if (!aligned16(w) || (reinterpret_cast<uintptr_t>(packed) & 255u)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  const w8a8_status st = cuda_status(
+      launch_quant_pack(w, E, N, K, flags, packed, scale, reinterpret_cast<cudaStream_t>(stream), sms));
+  if (st == W8A8_OK) record_pack(packed, E, N, K, flags);
+  return st;
+}
+
 w8a8_status w8a8_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                w8a8_stream_t stream) {
   if (M < 0 || M > INT32_MAX) return W8A8_ERR_SHAPE;

@@ -16,6 +16,12 @@ PackLayout pack_layout(int64_t E, int64_t N, int64_t K, uint32_t flags);
 
 cudaError_t launch_prepack(const int8_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags, void* packed,
                            cudaStream_t stream, int num_sms);
+// The header of a packed buffer whose payload a kernel before it on the stream wrote.
+cudaError_t launch_pack_header(int64_t E, int64_t N, int64_t K, uint32_t flags, void* packed, cudaStream_t stream);
+// Offline weight quantisation straight into a packed buffer: channel (e, c) of w [E,N,K] bf16 quantised
+// per channel over K, codes (and their fp16 copy if flags ask) to its packed row, scale to scale[e*N + c].
+cudaError_t launch_quant_pack(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags, void* packed,
+                              float* scale, cudaStream_t stream, int num_sms);
 
 cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                  cudaStream_t stream, int num_sms);

@@ -19,6 +19,31 @@ namespace w8a8 {
 
 namespace {
 
+__device__ __forceinline__ void write_header(uint8_t* packed, int64_t E, int64_t N, int64_t K, uint32_t flags,
+                                             uint64_t i8_off, uint64_t f16_off) {
+  PackedHeader hd;
+  hd.magic = kPackMagic;
+  hd.version = kPackVersion;
+  hd.E = E;
+  hd.N = N;
+  hd.K = K;
+  hd.flags = flags;
+  hd.reserved = 0u;
+  hd.i8_offset = i8_off;
+  hd.f16_offset = f16_off;
+  *reinterpret_cast<PackedHeader*>(packed) = hd;
+}
+
+// The header of a buffer whose payload the kernel before it wrote (the weight quantiser).  Launched
+// without programmatic serialization and never letting its dependents start early: a contraction
+// launched right after it reads the packed weights before its own wait, so it must start only after
+// this kernel and, through stream order, the payload writer have completed.
+__global__ void pack_header_kernel(int64_t E, int64_t N, int64_t K, uint32_t flags, uint8_t* packed, uint64_t i8_off,
+                                   uint64_t f16_off) {
+  write_header(packed, E, N, K, flags, i8_off, f16_off);
+  __threadfence();
+}
+
 __global__ void __launch_bounds__(256) prepack_kernel(const int8_t* __restrict__ w, int64_t E, int64_t N,
                                                       int64_t K, uint32_t flags, uint8_t* __restrict__ packed,
                                                       uint64_t i8_off, uint64_t f16_off) {
@@ -47,19 +72,7 @@ __global__ void __launch_bounds__(256) prepack_kernel(const int8_t* __restrict__
       d[1] = make_uint4(h[4], h[5], h[6], h[7]);
     }
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    PackedHeader hd;
-    hd.magic = kPackMagic;
-    hd.version = kPackVersion;
-    hd.E = E;
-    hd.N = N;
-    hd.K = K;
-    hd.flags = flags;
-    hd.reserved = 0u;
-    hd.i8_offset = i8_off;
-    hd.f16_offset = f16_off;
-    *reinterpret_cast<PackedHeader*>(packed) = hd;
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) write_header(packed, E, N, K, flags, i8_off, f16_off);
   // A contraction launched right after this kernel with programmatic stream
   // serialization reads the packed weights before it waits for this grid.
   // This kernel never lets its dependents start early, so they start only
@@ -86,6 +99,12 @@ cudaError_t launch_prepack(const int8_t* w, int64_t E, int64_t N, int64_t K, uin
   const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms) * 16));
   prepack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       w, E, N, K, flags, static_cast<uint8_t*>(packed), L.i8_offset, L.f16_offset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_header(int64_t E, int64_t N, int64_t K, uint32_t flags, void* packed, cudaStream_t stream) {
+  const PackLayout L = pack_layout(E, N, K, flags);
+  pack_header_kernel<<<1, 1, 0, stream>>>(E, N, K, flags, static_cast<uint8_t*>(packed), L.i8_offset, L.f16_offset);
   return cudaGetLastError();
 }
 

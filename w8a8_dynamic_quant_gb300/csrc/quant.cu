@@ -11,7 +11,9 @@
 // HBM-bound: 2 bytes read + 1 byte written per element (+4 bytes per row).
 // The MoE routing permute uses the same kernels with a scatter: a token row is
 // quantised once and its codes and scale go to each of its k routed rows (the
-// DeepEP INT8 dispatch of §三 quantises before it sends).
+// DeepEP INT8 dispatch of §三 quantises before it sends), and the offline
+// weight quantisation (§一: weight per_channel, int8, symmetric) uses them
+// with each output channel as a row, written straight into a packed buffer.
 // Each row is read once with 16-byte vector loads and held in registers
 // between the absmax pass and the quantise pass; absmax is reduced with warp
 // shuffles (and shared memory across the warps of a CTA).
@@ -94,24 +96,44 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   return r;
 }
 
-// Where a quantised row goes.  Plain quantisation: row m of the output.  Scatter (the MoE routing
-// permute): the k routed rows dst[m*k + j], j < k, of token m, each getting the same codes and scale;
-// a routed row index < 0 (a pair whose expert id was rejected) is skipped.
-template <bool SC>
-struct RowDst {
+// Where a quantised row goes: n() destinations, codes to row(m, j), the scale to scale_row(m, j); an
+// index < 0 is skipped.
+// Plain quantisation: row m of the output.
+struct RowId {
+  __device__ __forceinline__ int n() const { return 1; }
+  __device__ __forceinline__ int64_t row(int64_t m, int) const { return m; }
+  __device__ __forceinline__ int64_t scale_row(int64_t m, int) const { return m; }
+};
+// The MoE routing permute: the k routed rows dst[m*k + j] of token m, each with the same codes and scale
+// (an index < 0 belongs to a pair whose expert id was rejected).
+struct RowScatter {
   const int32_t* dst;
   int k;
-  __device__ __forceinline__ int n() const { return SC ? k : 1; }
-  __device__ __forceinline__ int64_t row(int64_t m, int j) const {
-    return SC ? static_cast<int64_t>(dst[m * k + j]) : m;
+  __device__ __forceinline__ int n() const { return k; }
+  __device__ __forceinline__ int64_t row(int64_t m, int j) const { return dst[m * k + j]; }
+  __device__ __forceinline__ int64_t scale_row(int64_t m, int j) const { return dst[m * k + j]; }
+};
+// Weight channels into a packed buffer: channel m = e*N + c goes to its packed row (the W13 gate/up
+// interleave when asked), its scale stays in channel order.
+struct RowPack {
+  int64_t N;
+  bool gate_up;
+  __device__ __forceinline__ int n() const { return 1; }
+  __device__ __forceinline__ int64_t row(int64_t m, int) const {
+    if (!gate_up) return m;
+    const int64_t e = m / N, c = m % N, I = N / 2;
+    // inverse of gate_up_orig_row: gate channel c -> block c/64, first half; up channel -> second half
+    const int64_t g = c < I ? c : c - I;
+    return e * N + (g / kGateUpBlock) * 2 * kGateUpBlock + (c < I ? 0 : kGateUpBlock) + g % kGateUpBlock;
   }
+  __device__ __forceinline__ int64_t scale_row(int64_t m, int) const { return m; }
 };
 
 // OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both (each code computed once).
 // s = rs = 0 (an all-zero row) gives zero codes.
-template <int OUT, bool SC>
+template <int OUT, class D>
 __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_t row, int64_t K, int64_t idx,
-                                       void* q, uint16_t* q16, const RowDst<SC>& d) {
+                                       void* q, uint16_t* q16, const D& d) {
   float m[8];
   codes8(v, s, rs, m);
   uint2 c = make_uint2(0u, 0u);
@@ -126,10 +148,10 @@ __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_
   }
 }
 
-template <bool SC>
-__device__ __forceinline__ void store_scale(float s, int64_t row, float* scale, const RowDst<SC>& d) {
+template <class D>
+__device__ __forceinline__ void store_scale(float s, int64_t row, float* scale, const D& d) {
   for (int j = 0; j < d.n(); ++j) {
-    const int64_t r = d.row(row, j);
+    const int64_t r = d.scale_row(row, j);
     if (r >= 0) scale[r] = s;
   }
 }
@@ -153,10 +175,10 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).  At least four CTAs (32 warps, 32 rows of
 // loads in flight) per SM.
-template <int CH, int OUT, bool SC>
+template <int CH, int OUT, class D>
 __global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
                                                        int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                       float* __restrict__ scale, RowDst<SC> d) {
+                                                       float* __restrict__ scale, D d) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = K / 8;
@@ -190,10 +212,10 @@ __global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __rest
 // One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).  A CTA takes rows
 // blockIdx.x, + gridDim.x, ...; the loads of its next row are issued before the current one is reduced
 // and quantised, so an SM keeps reading while it computes.
-template <int CH, int OUT, bool SC>
+template <int CH, int OUT, class D>
 __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                      float* __restrict__ scale, RowDst<SC> d) {
+                                                      float* __restrict__ scale, D d) {
   pdl_enter();
   __shared__ float red[2][8];
   const int64_t nchunk = K / 8;
@@ -235,10 +257,10 @@ __global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict
 }
 
 // Any K: two passes over the row (the second read mostly hits L2).
-template <int OUT, bool SC>
+template <int OUT, class D>
 __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __restrict__ x, int64_t M,
                                                           int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                          float* __restrict__ scale, RowDst<SC> d) {
+                                                          float* __restrict__ scale, D d) {
   pdl_enter();
   __shared__ float red[8];
   const int64_t nchunk = K / 8;
@@ -262,13 +284,13 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
   }
 }
 
-// CTAs of quant_cta_rows<CH, OUT, SC> resident per SM (queried once).
-template <int CH, int OUT, bool SC>
+// CTAs of quant_cta_rows<CH, OUT, D> resident per SM (queried once).
+template <int CH, int OUT, class D>
 int cta_rows_per_sm() {
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_cta_rows<CH, OUT, SC>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_cta_rows<CH, OUT, D>, 256, 0) != cudaSuccess ||
         n < 1) {
       cudaGetLastError();
       n = 1;
@@ -278,9 +300,9 @@ int cta_rows_per_sm() {
   return per_sm;
 }
 
-template <int OUT, bool SC>
+template <int OUT, class D>
 cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale,
-                           RowDst<SC> d, cudaStream_t stream, int num_sms) {
+                           D d, cudaStream_t stream, int num_sms) {
   if (M == 0) return cudaSuccess;
   const int64_t nchunk = K / 8;
   const int64_t max_grid = static_cast<int64_t>(num_sms) * 64;
@@ -289,10 +311,10 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
     const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
     const int ch = static_cast<int>((nchunk + 31) / 32);
     dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-    else return launch_pdl(quant_warp_rows<8, OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    else return launch_pdl(quant_warp_rows<8, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
   } else {
     // as many CTAs as are resident at once; each then works through its rows
     const int ch = static_cast<int>((nchunk + 255) / 256);
@@ -301,16 +323,16 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
       return dim3(static_cast<unsigned>(std::min<int64_t>(M, static_cast<int64_t>(num_sms) * per_sm)));
     };
     if (ch <= 2)
-      return launch_pdl(quant_cta_rows<2, OUT, SC>, grid(cta_rows_per_sm<2, OUT, SC>()), b, 0, stream, x, M, K, q,
+      return launch_pdl(quant_cta_rows<2, OUT, D>, grid(cta_rows_per_sm<2, OUT, D>()), b, 0, stream, x, M, K, q,
                         q16, scale, d);
     if (ch <= 4)
-      return launch_pdl(quant_cta_rows<4, OUT, SC>, grid(cta_rows_per_sm<4, OUT, SC>()), b, 0, stream, x, M, K, q,
+      return launch_pdl(quant_cta_rows<4, OUT, D>, grid(cta_rows_per_sm<4, OUT, D>()), b, 0, stream, x, M, K, q,
                         q16, scale, d);
     if (ch <= 8)
-      return launch_pdl(quant_cta_rows<8, OUT, SC>, grid(cta_rows_per_sm<8, OUT, SC>()), b, 0, stream, x, M, K, q,
+      return launch_pdl(quant_cta_rows<8, OUT, D>, grid(cta_rows_per_sm<8, OUT, D>()), b, 0, stream, x, M, K, q,
                         q16, scale, d);
     const dim3 g(static_cast<unsigned>(std::min<int64_t>(M, max_grid)));
-    return launch_pdl(quant_cta_rows_any<OUT, SC>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+    return launch_pdl(quant_cta_rows_any<OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
   }
 }
 
@@ -318,20 +340,33 @@ cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uin
 
 cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                  cudaStream_t stream, int num_sms) {
-  return launch_quant_t<0>(x, M, K, q, nullptr, scale, RowDst<false>{nullptr, 1}, stream, num_sms);
+  return launch_quant_t<0>(x, M, K, q, nullptr, scale, RowId{}, stream, num_sms);
 }
 
 cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
                                       float* scale, cudaStream_t stream, int num_sms) {
-  return launch_quant_t<2>(x, M, K, q, q_f16, scale, RowDst<false>{nullptr, 1}, stream, num_sms);
+  return launch_quant_t<2>(x, M, K, q, q_f16, scale, RowId{}, stream, num_sms);
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, const int32_t* dst, int k, int8_t* q,
                                  uint16_t* q_f16, float* scale, int out, cudaStream_t stream, int num_sms) {
-  const RowDst<true> d{dst, k};
+  const RowScatter d{dst, k};
   if (out == 0) return launch_quant_t<0>(x, T, H, q, nullptr, scale, d, stream, num_sms);
   if (out == 1) return launch_quant_t<1>(x, T, H, nullptr, q_f16, scale, d, stream, num_sms);
   return launch_quant_t<2>(x, T, H, q, q_f16, scale, d, stream, num_sms);
+}
+
+cudaError_t launch_quant_pack(const uint16_t* w, int64_t E, int64_t N, int64_t K, uint32_t flags, void* packed,
+                              float* scale, cudaStream_t stream, int num_sms) {
+  const PackLayout L = pack_layout(E, N, K, flags);
+  uint8_t* b = static_cast<uint8_t*>(packed);
+  const RowPack d{N, (flags & W8A8_PACK_GATE_UP) != 0u};
+  int8_t* q = reinterpret_cast<int8_t*>(b + L.i8_offset);
+  const cudaError_t e = L.f16_offset
+      ? launch_quant_t<2>(w, E * N, K, q, reinterpret_cast<uint16_t*>(b + L.f16_offset), scale, d, stream, num_sms)
+      : launch_quant_t<0>(w, E * N, K, q, nullptr, scale, d, stream, num_sms);
+  if (e != cudaSuccess) return e;
+  return launch_pack_header(E, N, K, flags, packed, stream);
 }
 
 }  // namespace w8a8

@@ -22,6 +22,10 @@ Recipe (one generator per case, seed 0 unless stated; draw order fixed):
          their token's payload and scale.  Token rows are kept too, with
          router weights drawn last: U[0.05,1] per chosen expert, divided by
          the token's sum, fp32.
+  bf16 weights (the source of the offline per-channel quantisation):
+         N(0,1) * 0.02 * 2^c per output channel, c uniform in {-4..2}, and one
+         element in every 64th channel multiplied by 8 (an outlier); drawn on
+         the target device with torch's seeded generator, rounded to BF16.
 BF16 rounding of the drawn fp32 values uses torch's conversion.
 """
 from __future__ import annotations
@@ -197,6 +201,20 @@ def make_moe(T: int, H: int, I: int, E: int, topk: int, routing: str = "uniform"
                      token_index=token_index, group_list=counts, x=np.ascontiguousarray(x),
                      x_scale=x_scale, w13=w13, s13=s13, w2=w2, s2=s2, extra=dict(p=p),
                      x_tok=x_tok, x_tok_scale=s_tok, topk_weights=topk_weights)
+
+
+def make_bf16_weight(E: int, N: int, K: int, seed: int = 0, device: str = "cpu") -> torch.Tensor:
+    """A BF16 weight stack [E,N,K] with per-channel ranges spread over 2^-4 .. 2^2 (and some outliers)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed * 7919 + 3)
+    w = torch.randn((E, N, K), generator=gen, device=device)
+    c = torch.randint(-4, 3, (E, N, 1), generator=gen, device=device).float()
+    w.mul_(torch.exp2(c) * 0.02)
+    rows = torch.arange(0, N, 64, device=device)  # every 64th channel gets one outlier
+    col = torch.randint(0, K, (E, rows.numel()), generator=gen, device=device)
+    e_idx = torch.arange(E, device=device)[:, None].expand_as(col)
+    w[e_idx, rows[None, :].expand_as(col), col] *= 8.0
+    return w.to(torch.bfloat16)
 
 
 def moe_config(cfg_id: int, seed: int = 0, device: str = "cpu") -> MoEInputs:
