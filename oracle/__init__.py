@@ -69,6 +69,9 @@ def _load(path: str) -> ctypes.CDLL:
     L.oracle_moe_w13_swiglu_requant_w2.argtypes = [
         _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp, _vp,
         _vp, _vp, _vp, _vp, _vp, _vp]
+    L.oracle_static_quant.argtypes = [_vp, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int32, _vp]
+    L.oracle_static_prepare.argtypes = [_vp, _c_i64, _c_i64, _vp, ctypes.c_float, ctypes.c_int32, _vp, _vp, _vp]
+    L.oracle_static_quant_matmul.argtypes = [_vp, _c_i64, _c_i64, _vp, _c_i64, _vp, _vp, _vp]
     L.oracle_quantize_weight.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
     L.oracle_moe_route.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
     L.oracle_moe_permute_quant.argtypes = [_vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp,
@@ -227,6 +230,43 @@ def moe_w13_swiglu_requant_w2(x, x_scale, group_list, w13, s13, w2, s2, intermed
                _p(inter.get("xq")), _p(inter.get("xs")), _p(inter.get("y13")),
                _p(inter.get("h")), _p(inter.get("hq")), _p(inter.get("hs"))))
     return (y, inter) if intermediates else y
+
+
+def static_quant(x, input_scale: float, input_offset: int):
+    """bf16 bits x [M,K] -> int8 q = clamp(rint(x / s) + o, -128, 127) (static, per-tensor s and o)."""
+    x = _c(x, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.int8)
+    _check("oracle_static_quant", lib().oracle_static_quant(_p(x), M, K, float(input_scale), int(input_offset),
+                                                            _p(q)))
+    return q
+
+
+def static_prepare(w, w_scale, input_scale: float, input_offset: int, bias=None):
+    """int8 W [N,K], fp32 weight scales [N] (+ bf16 bits bias [N]) -> (fp32 deq_scale [N], int32 quant_bias [N])."""
+    w = _c(w, np.int8)
+    ws = _c(w_scale, np.float32)
+    b = None if bias is None else _c(bias, np.uint16)
+    N, K = w.shape
+    deq = np.empty((N,), np.float32)
+    qb = np.empty((N,), np.int32)
+    _check("oracle_static_prepare", lib().oracle_static_prepare(_p(w), N, K, _p(ws), float(input_scale),
+                                                                int(input_offset), _p(b), _p(deq), _p(qb)))
+    return deq, qb
+
+
+def static_quant_matmul(q, w, deq_scale, quant_bias):
+    """int8 q [M,K] x int8 W [N,K] -> bf16 bits y = bf16(float(acc + quant_bias[n]) * deq_scale[n])."""
+    q = _c(q, np.int8)
+    w = _c(w, np.int8)
+    deq = _c(deq_scale, np.float32)
+    qb = _c(quant_bias, np.int32)
+    M, K = q.shape
+    N = w.shape[0]
+    y = np.empty((M, N), np.uint16)
+    _check("oracle_static_quant_matmul", lib().oracle_static_quant_matmul(_p(q), M, K, _p(w), N, _p(deq), _p(qb),
+                                                                          _p(y)))
+    return y
 
 
 def quantize_weight(w):

@@ -267,6 +267,75 @@ int oracle_quantize_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K, i
   return ORC_OK;
 }
 
+/* ------------------------------------------------------- static W8A8 -- */
+/*
+ * [P1] closing comparison of the static recipe: BF16 X is quantised by
+ * npu_quantize with a fixed (calibrated) input_scale / input_offset; at load
+ * time deq_scale = input_scale * weight_scale and
+ * quant_bias = round(fp_bias / deq_scale - sum_k(Qw[n,k]) * input_offset)
+ * (int32); npu_quant_matmul(x, W, deq_scale, bias=quant_bias) gives BF16 Y.
+ * The correction term is that of x = input_scale * (q - input_offset).
+ *
+ * READING (quantise): q = clamp(rint(x / s) + o, -128, 127): binary32 divide,
+ *   ties to even, the integer offset added to the integer code (exact), the
+ *   full int8 range (the code is no longer symmetric).  s, o per tensor.
+ * READING (prepare): a = float(bias[n]) / deq[n] (0 without a bias),
+ *   c = float(sum_k Qw[n,k]) * float(o) (the sum is exact), quant_bias =
+ *   rint(a - c) (binary32 steps, ties to even), saturated to int32.
+ *   deq[n] = s * weight_scale[n] (binary32).
+ * READING (matmul): y = bf16_rne(float(acc + quant_bias[n]) * deq[n]); the
+ *   integer bias is added to the accumulator before the one conversion.
+ */
+int oracle_static_quant(const uint16_t* x, int64_t M, int64_t K, float s, int32_t o, int8_t* q) {
+  if (M < 0 || K <= 0 || !(s > 0.0f)) return ORC_ERR_SHAPE;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m)
+    for (int64_t k = 0; k < K; ++k) {
+      const float t = oracle_bf16_to_f32(x[m * K + k]) / s;
+      double c = (double)rintf(t) + (double)o;
+      if (c > 127.0) c = 127.0;
+      if (c < -128.0) c = -128.0;
+      if (t != t) c = 0.0; /* NaN input: not produced by the generator */
+      q[m * K + k] = (int8_t)c;
+    }
+  return ORC_OK;
+}
+
+int oracle_static_prepare(const int8_t* w, int64_t N, int64_t K, const float* w_scale, float s, int32_t o,
+                          const uint16_t* bias, float* deq, int32_t* quant_bias) {
+  if (N <= 0 || K <= 0) return ORC_ERR_SHAPE;
+  for (int64_t n = 0; n < N; ++n) {
+    int64_t sum = 0;
+    for (int64_t k = 0; k < K; ++k) sum += w[n * K + k];
+    deq[n] = s * w_scale[n];
+    const float a = bias ? oracle_bf16_to_f32(bias[n]) / deq[n] : 0.0f;
+    const float c = (float)sum * (float)o;
+    const float t = rintf(a - c);
+    double v = (double)t;
+    if (v > 2147483647.0) v = 2147483647.0;
+    if (v < -2147483648.0) v = -2147483648.0;
+    quant_bias[n] = (int32_t)v;
+  }
+  return ORC_OK;
+}
+
+int oracle_static_quant_matmul(const int8_t* q, int64_t M, int64_t K, const int8_t* w, int64_t N,
+                               const float* deq, const int32_t* quant_bias, uint16_t* y) {
+  if (M < 0 || N <= 0 || K <= 0 || K > ORC_MAX_K) return ORC_ERR_SHAPE;
+  int32_t* acc = malloc((size_t)(M > 0 ? M : 1) * (size_t)N * sizeof(int32_t));
+  if (!acc) return ORC_ERR_ALLOC;
+  int rc = oracle_int8_gemm_acc(q, M, K, w, N, acc);
+  if (rc == ORC_OK)
+    for (int64_t m = 0; m < M; ++m)
+      for (int64_t n = 0; n < N; ++n) {
+        const float t = (float)((int64_t)acc[m * N + n] + (int64_t)quant_bias[n]);
+        y[m * N + n] = oracle_f32_to_bf16(t * deq[n]);
+      }
+  free(acc);
+  return rc;
+}
+
 /* ---------------------------------------------------------- grouped GEMM -- */
 
 int oracle_check_group_list(const int64_t* group_list, int64_t E, int64_t R) {

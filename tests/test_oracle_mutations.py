@@ -46,6 +46,12 @@ MUTATIONS = [
      "for (int64_t j = 0; j + 1 < k; ++j) {\n        const float v", "test_combine_against_float64", ()),
     ("weight channel read from the first expert", "oracle_dynamic_quant(w + row * K, 1, K, q + row * K, scale + row);",
      "oracle_dynamic_quant(w + n * K, 1, K, q + row * K, scale + row);", "test_weight_quant_is_per_output_channel", ()),
+    ("static correction added instead of subtracted", "const float t = rintf(a - c);", "const float t = rintf(a + c);",
+     "test_static_path_approximates_the_float_layer", (9,)),
+    ("static offset added before rounding", "double c = (double)rintf(t) + (double)o;",
+     "double c = (double)rintf(t + (float)o);", "test_static_quant_brute_force_and_closed_forms", ()),
+    ("static codes clamped at -127", "if (c < -128.0) c = -128.0;", "if (c < -127.0) c = -127.0;",
+     "test_static_quant_brute_force_and_closed_forms", ()),
     ("combine sums in double", "      float s = 0.0f;\n      for (int64_t j", "      double s = 0.0;\n      for (int64_t j",
      "test_combine_closed_forms_and_order", ()),
 ]

@@ -525,3 +525,68 @@ def test_weight_quant_is_per_output_channel():
     # a 2-D weight is one expert
     q2, s2 = oracle.quantize_weight(w[2])
     assert np.array_equal(q2, q[2]) and np.array_equal(s2, s[2])
+
+
+# ------------------------------------------------------------- static W8A8 ----
+
+def test_static_quant_brute_force_and_closed_forms():
+    """q = clamp(rint(x/s) + o, -128, 127): against the nearest code of the affine grid s*(c - o) found by
+    brute force (ties to the even rint(x/s)), exact grid points, and both clamps."""
+    rng = np.random.default_rng(31)
+    s, o = np.float32(0.0625), 5
+    x = S.to_bf16_bits((rng.standard_normal((6, 64)) * 4).astype(np.float32))
+    q = oracle.static_quant(x, s, o).astype(np.int64)
+    xf = f32(x).astype(np.float64)
+    grid = np.arange(-128, 128)
+    dist = np.abs(xf[..., None] - float(s) * (grid - o))          # [6,64,256]
+    best = dist.min(axis=-1)
+    # the chosen code is a nearest one, and where two are equally near it is the one with rint(x/s) even
+    chosen = np.take_along_axis(dist, (q + 128)[..., None], axis=-1)[..., 0]
+    assert np.all(chosen <= best + 1e-12)
+    tie = (np.sum(dist <= best[..., None] + 1e-12, axis=-1) > 1)
+    assert np.all(((q[tie] - o) % 2) == 0)
+    # exact grid points, and the clamps
+    pts = S.to_bf16_bits((np.float32(s) * np.array([[-3, 0, 7, 100, 5000, -5000]], np.float32)))
+    assert oracle.static_quant(pts, s, o).tolist() == [[2, 5, 12, 105, 127, -128]]
+
+
+def test_static_prepare_against_float64():
+    rng = np.random.default_rng(32)
+    N, K = 50, 96
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    ws = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    bias = S.to_bf16_bits(rng.normal(0, 0.5, N).astype(np.float32))
+    s, o = np.float32(0.03), -7
+    deq, qb = oracle.static_prepare(w, ws, s, o, bias)
+    assert np.array_equal(deq.view(np.uint32), (np.float32(s) * ws).view(np.uint32))
+    exact = f32(bias).astype(np.float64) / deq.astype(np.float64) - w.astype(np.int64).sum(axis=1) * o
+    assert np.all(np.abs(qb - exact) <= 0.5 + 1e-3 * np.abs(exact) / 2 ** 10 + 1e-6)
+    # no bias: just minus the correction, an exact integer
+    _, qb0 = oracle.static_prepare(w, ws, s, o, None)
+    assert np.array_equal(qb0.astype(np.int64), -w.astype(np.int64).sum(axis=1) * o)
+
+
+@pytest.mark.parametrize("o", [0, 9, -20])
+def test_static_path_approximates_the_float_layer(o):
+    """Static quant -> matmul with the prepared deq_scale / quant_bias approximates x @ W_deq^T + bias in
+    float64 within the input grid's rounding: the offset correction cancels the zero point (a sign slip
+    in it would leave an error of about s * o * sum|W|)."""
+    rng = np.random.default_rng(33 + o)
+    M, N, K = 12, 40, 256
+    s = np.float32(0.02)
+    x = S.to_bf16_bits((rng.standard_normal((M, K)) * 0.6).astype(np.float32))
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    ws = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    bias = S.to_bf16_bits(rng.normal(0, 0.3, N).astype(np.float32))
+    q = oracle.static_quant(x, s, o)
+    deq, qb = oracle.static_prepare(w, ws, s, o, bias)
+    y = f32(oracle.static_quant_matmul(q, w, deq, qb)).astype(np.float64)
+    wd = w.astype(np.float64) * ws[:, None].astype(np.float64)
+    ref = f32(x).astype(np.float64) @ wd.T + f32(bias).astype(np.float64)[None, :]
+    # per element: K input rounding errors of at most s/2 each times |W_deq|, the bias rounding, bf16
+    bound = 0.5 * float(s) * np.abs(wd).sum(axis=1)[None, :] + 0.5 * deq[None, :] + np.abs(ref) * 2.0 ** -8
+    assert np.all(np.abs(y - ref) <= bound)
+    # exact on the code grid: the same layer on the dequantised input is matched to the output rounding
+    xd = float(s) * (q.astype(np.float64) - o)
+    ref_q = xd @ wd.T + f32(bias).astype(np.float64)[None, :]
+    assert np.all(np.abs(y - ref_q) <= 0.5 * deq[None, :] + np.abs(ref_q) * 2.0 ** -8 * 1.01 + 1e-9)
