@@ -263,6 +263,53 @@ class Dense:
         return self.M
 
 
+class DenseStatic(Dense):
+    """The static W8A8 variant of a dense workload: quantisation with a fixed per-tensor input scale and
+    offset, then the matmul whose epilogue adds the load-time quant_bias and scales by deq_scale."""
+
+    def __init__(self, cfg_id: int, device):
+        super().__init__(cfg_id, device)
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        W, torch, d = self.W, self.torch, self.d
+        self.s_in, self.o_in = S.static_params(cfg_id)
+        self.name = d.name + "_static"
+        wd = torch.from_numpy(d.w).to(device)
+        for st in self.sets:  # load time, outside the timed step
+            st["deq"], st["qb"] = W.w8a8_static_prepare(wd, st["sw"], self.s_in, self.o_in, st["bias"])
+        M, N, K = self.M, self.N, self.K
+        self.kernels = ["static_quant", "static_quant_matmul"]
+        self.alg_bytes = {"static_quant": 2 * M * K + M * K,
+                          "static_quant_matmul": M * K + N * K + 8 * N + 2 * M * N}
+        self.alg_flops = {"static_quant_matmul": 2.0 * M * N * K}
+
+    def launch(self, kernel: str, i: int):
+        st = self.sets[i]
+        if kernel == "static_quant":
+            self.W.w8a8_static_quant(st["x"], self.s_in, self.o_in, st["q"])
+        else:
+            self.W.w8a8_static_quant_matmul(st["q"], st["wp"], st["deq"], st["qb"], st["ws"], st["y"])
+
+    def config(self):
+        c = super().config()
+        c.update(workload=self.name, input_scale=self.s_in, input_offset=self.o_in)
+        return c
+
+    def e2e_step(self):
+        st = self.sets[0]
+        st["x"].copy_(self.hx, non_blocking=True)
+        q = self.W.w8a8_static_quant(st["x"], self.s_in, self.o_in, st["q"])
+        y = self.W.w8a8_static_quant_matmul(q, st["wp"], st["deq"], st["qb"], st["ws"], st["y"])
+        self.hy.copy_(y, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    def oracle_step(self, rows):
+        import oracle
+        if not hasattr(self, "_prep"):
+            self._prep = oracle.static_prepare(self.d.w, self.d.w_scale, self.s_in, self.o_in, self.d.bias)
+        q = oracle.static_quant(self.d.x[:rows], self.s_in, self.o_in)
+        oracle.static_quant_matmul(q, self.d.w, *self._prep)
+
+
 class MoE:
     """MoE expert FFN: (quant) -> W13 grouped GEMM + SwiGLU -> requant -> W2 grouped GEMM."""
 
@@ -589,12 +636,12 @@ class WeightPrep:
         return self.channels
 
 
-def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False):
+def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False, static=False):
     from w8a8_dynamic_quant_gb300 import synthetic as S
     if prepare:
         return WeightPrep(cfg_id, device)
     if S.CONFIGS[cfg_id]["kind"] == "dense":
-        return Dense(cfg_id, device)
+        return DenseStatic(cfg_id, device) if static else Dense(cfg_id, device)
     return MoETokens(cfg_id, device, kernels) if from_tokens else MoE(cfg_id, device)
 
 
@@ -635,7 +682,7 @@ def run_reference(args):
     if args.prepare:
         wl = WeightPrep(args.workload, "cpu", host_only=True)
     elif S.CONFIGS[args.workload]["kind"] == "dense":
-        wl = _HostDense(args.workload)
+        wl = _HostDenseStatic(args.workload) if args.static else _HostDense(args.workload)
     else:
         wl = _HostMoETokens(args.workload) if args.from_tokens else _HostMoE(args.workload)
     for _ in range(args.warmup):
@@ -668,6 +715,14 @@ class _HostDense(Dense):
         self.input_note = "host arrays (CPU oracle)"
         # about 0.1-0.5 s of CPU per step on 16 cores
         self.step_rows = max(1, min(self.M, int(2e9 // (2 * self.N * self.K))))
+
+
+class _HostDenseStatic(DenseStatic):
+    def __init__(self, cfg_id):
+        from w8a8_dynamic_quant_gb300 import synthetic as S
+        _HostDense.__init__(self, cfg_id)
+        self.s_in, self.o_in = S.static_params(cfg_id)
+        self.name = self.d.name + "_static"
 
 
 class _HostMoE(MoE):
@@ -709,7 +764,7 @@ def run_gpu(args):
     __graft_entry__.build()
     peaks = load_peaks()
     kernels = args.kernels.split(",") if args.kernels else None
-    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare)
+    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare, args.static)
     step_kernels = getattr(wl, "step_kernels", wl.kernels)
     stream = torch.cuda.current_stream(device)
 
@@ -850,6 +905,9 @@ def main(argv=None):
     ap.add_argument("--from-tokens", action="store_true",
                     help="MoE workloads: the layer from token rows and router output (routing permute + quant, "
                          "expert chain, top-k weighted combine) instead of expert-sorted routed rows")
+    ap.add_argument("--static", action="store_true",
+                    help="dense workloads: the static W8A8 variant (fixed input scale and offset, load-time "
+                         "deq_scale and quant_bias)")
     ap.add_argument("--prepare", action="store_true",
                     help="time the load-time weight preparation instead: the workload's weights quantised per "
                          "channel from BF16 and packed in one pass (GB/s)")

@@ -191,6 +191,40 @@ W8A8_API w8a8_status w8a8_grouped_matmul_acc(const int8_t* q, const int64_t* gro
                                     int32_t* acc, void* ws, size_t ws_bytes, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Static W8A8 -- [P1] closing comparison of the static recipe: npu_quantize */
+/* with a fixed input_scale s and input_offset o; at load time               */
+/* deq_scale[n] = s * weight_scale[n] and                                    */
+/* quant_bias[n] = round(fp_bias[n] / deq_scale[n] - sum_k Qw[n,k] * o)      */
+/* (the correction of x = s * (q - o)); npu_quant_matmul(x, W, deq_scale,    */
+/* bias=quant_bias) -> BF16.                                                 */
+/*   quantise: q = clamp(rint(x / s) + o, -128, 127) (binary32 divide, ties  */
+/*             to even, the integer offset added after rounding)             */
+/*   prepare:  binary32 steps a = bias / deq (0 without a bias or where deq  */
+/*             is 0), c = float(sum_k Qw) * o, quant_bias = rint(a - c),     */
+/*             saturated to int32                                            */
+/*   matmul:   y = bf16_rne(float(acc + quant_bias[n]) * deq_scale[n])       */
+/* s > 0 and finite, o in [-128, 127]; both per tensor.                      */
+/* ------------------------------------------------------------------------ */
+
+/* x [M,K] bf16 -> q [M,K] int8.  K % 16 == 0, x and q 16-byte aligned. */
+W8A8_API w8a8_status w8a8_static_quant(const uint16_t* x, int64_t M, int64_t K, float input_scale,
+                                       int32_t input_offset, int8_t* q, w8a8_stream_t stream);
+
+/* Load time: w [N,K] int8 (checkpoint layout), weight_scale [N] fp32, bias
+ * [N] bf16 or NULL -> deq_scale [N] fp32 and quant_bias [N] int32 (device
+ * buffers).  K % 16 == 0, w 16-byte aligned. */
+W8A8_API w8a8_status w8a8_static_prepare(const int8_t* w, int64_t N, int64_t K, const float* weight_scale,
+                                         float input_scale, int32_t input_offset, const uint16_t* bias,
+                                         float* deq_scale, int32_t* quant_bias, w8a8_stream_t stream);
+
+/* q [M,K] int8 from w8a8_static_quant, w_packed as for w8a8_quant_matmul,
+ * deq_scale / quant_bias from w8a8_static_prepare -> y [M,N] bf16.  Workspace
+ * as w8a8_quant_matmul_workspace_bytes(M, N, K). */
+W8A8_API w8a8_status w8a8_static_quant_matmul(const int8_t* q, int64_t M, int64_t K, const void* w_packed,
+                                              const float* deq_scale, const int32_t* quant_bias, int64_t N,
+                                              uint16_t* y, void* ws, size_t ws_bytes, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* MoE expert FFN -- [P1] §三 runner chain: (quantise only if no per-token   */
 /* scale was supplied) -> W13 grouped matmul -> SwiGLU -> per-token INT8     */
 /* requant -> W2 grouped matmul -> BF16.                                     */

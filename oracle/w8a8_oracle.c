@@ -282,7 +282,8 @@ int oracle_quantize_weight(const uint16_t* w, int64_t E, int64_t N, int64_t K, i
  * READING (prepare): a = float(bias[n]) / deq[n] (0 without a bias),
  *   c = float(sum_k Qw[n,k]) * float(o) (the sum is exact), quant_bias =
  *   rint(a - c) (binary32 steps, ties to even), saturated to int32.
- *   deq[n] = s * weight_scale[n] (binary32).
+ *   deq[n] = s * weight_scale[n] (binary32).  Where deq is 0 (an all-zero
+ *   weight channel) the bias cannot be expressed: a = 0 (y is 0 there).
  * READING (matmul): y = bf16_rne(float(acc + quant_bias[n]) * deq[n]); the
  *   integer bias is added to the accumulator before the one conversion.
  */
@@ -309,7 +310,7 @@ int oracle_static_prepare(const int8_t* w, int64_t N, int64_t K, const float* w_
     int64_t sum = 0;
     for (int64_t k = 0; k < K; ++k) sum += w[n * K + k];
     deq[n] = s * w_scale[n];
-    const float a = bias ? oracle_bf16_to_f32(bias[n]) / deq[n] : 0.0f;
+    const float a = (bias && deq[n] != 0.0f) ? oracle_bf16_to_f32(bias[n]) / deq[n] : 0.0f;
     const float c = (float)sum * (float)o;
     const float t = rintf(a - c);
     double v = (double)t;

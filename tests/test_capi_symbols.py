@@ -84,6 +84,13 @@ def test_host_validation_rejects_before_launch(lib):
                                          fake, None) == 2  # I % 64 != 0
     assert lib.w8a8_prepack_weight(fake, 1, 130, 64, 1, ctypes.c_void_p(256), None) == 2  # gate/up needs I % 64 == 0
     assert lib.w8a8_prepack_weight(fake, 1, 128, 64, 8, ctypes.c_void_p(256), None) == 2  # unknown flag
+    # static W8A8: scale <= 0, offset out of int8, K % 16, missing quant_bias
+    assert lib.w8a8_static_quant(fake, 4, 32, 0.0, 0, fake, None) == 2
+    assert lib.w8a8_static_quant(fake, 4, 32, 0.1, 200, fake, None) == 2
+    assert lib.w8a8_static_quant(fake, 4, 24, 0.1, 0, fake, None) == 3
+    assert lib.w8a8_static_prepare(fake, 8, 32, fake, 0.1, 0, None, None, fake, None) == 1
+    assert lib.w8a8_static_quant_matmul(fake, 4, 64, ctypes.c_void_p(256), fake, None, 8, fake, fake, 1 << 20,
+                                        None) == 1
     # weight quantisation: K % 16, E out of range, unknown flag, gate/up needs (N/2) % 64, packed alignment
     assert lib.w8a8_quantize_weight(fake, 1, 8, 24, fake, fake, None) == 3
     assert lib.w8a8_quantize_weight(fake, 2000, 8, 32, fake, fake, None) == 2

@@ -25,7 +25,8 @@ __all__ = [
     "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
     "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
-    "w8a8_quantize_weight", "w8a8_quantize_prepack_weight", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
+    "w8a8_quantize_weight", "w8a8_quantize_prepack_weight", "w8a8_static_quant", "w8a8_static_prepare",
+    "w8a8_static_quant_matmul", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
     "moe_layer_workspace_offset", "moe_layer",
 ]
 
@@ -131,6 +132,58 @@ def w8a8_dynamic_quant(x: torch.Tensor, q: Optional[torch.Tensor] = None,
         _capi.check("w8a8_dynamic_quant", _capi.lib().w8a8_dynamic_quant(
             x.data_ptr(), M, K, q.data_ptr(), scale.data_ptr(), _stream(x.device)))
     return q, scale
+
+
+def w8a8_static_quant(x: torch.Tensor, input_scale: float, input_offset: int, q: Optional[torch.Tensor] = None):
+    """Static W8A8 quantisation: bf16 x [M,K] -> int8 q = clamp(rint(x / s) + o, -128, 127)."""
+    _need(x, "x", torch.bfloat16)
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device) if q is None else q
+    _need(q, "q", torch.int8, (M, K), x.device)
+    with torch.cuda.device(x.device):
+        _capi.check("w8a8_static_quant", _capi.lib().w8a8_static_quant(
+            x.data_ptr(), M, K, float(input_scale), int(input_offset), q.data_ptr(), _stream(x.device)))
+    return q
+
+
+def w8a8_static_prepare(w: torch.Tensor, weight_scale: torch.Tensor, input_scale: float, input_offset: int,
+                        bias: Optional[torch.Tensor] = None):
+    """Load time: int8 W [N,K], float32 weight scales [N] (+ bf16 bias [N]) -> (float32 deq_scale [N],
+    int32 quant_bias [N])."""
+    _need(w, "w", torch.int8)
+    N, K = w.shape
+    dev = w.device
+    _need(weight_scale, "weight_scale", torch.float32, (N,), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, (N,), dev)
+    deq = torch.empty((N,), dtype=torch.float32, device=dev)
+    qb = torch.empty((N,), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_static_prepare", _capi.lib().w8a8_static_prepare(
+            w.data_ptr(), N, K, weight_scale.data_ptr(), float(input_scale), int(input_offset), _ptr(bias),
+            deq.data_ptr(), qb.data_ptr(), _stream(dev)))
+    return deq, qb
+
+
+def w8a8_static_quant_matmul(q: torch.Tensor, w_packed: torch.Tensor, deq_scale: torch.Tensor,
+                             quant_bias: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                             y: Optional[torch.Tensor] = None):
+    """Static W8A8 matmul: int8 q [M,K] x packed W [N,K] -> bf16 y = bf16(float(acc + quant_bias) * deq_scale)."""
+    _need(q, "q", torch.int8)
+    M, K = q.shape
+    dev = q.device
+    _need(deq_scale, "deq_scale", torch.float32, None, dev)
+    N = deq_scale.shape[0]
+    _need(quant_bias, "quant_bias", torch.int32, (N,), dev)
+    _need(w_packed, "w_packed", torch.uint8, None, dev)
+    ws = workspace(quant_matmul_workspace_bytes(M, N, K), dev) if ws is None else ws
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if y is None else y
+    _need(y, "y", torch.bfloat16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_static_quant_matmul", _capi.lib().w8a8_static_quant_matmul(
+            q.data_ptr(), M, K, w_packed.data_ptr(), deq_scale.data_ptr(), quant_bias.data_ptr(), N, y.data_ptr(),
+            ws.data_ptr(), ws.numel(), _stream(dev)))
+    return y
 
 
 def quant_matmul_workspace_bytes(M: int, N: int, K: int) -> int:

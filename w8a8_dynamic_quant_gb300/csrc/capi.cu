@@ -411,12 +411,12 @@ size_t w8a8_quant_matmul_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 static w8a8_status dense_common(const int8_t* q, const float* x_scale, int64_t M, int64_t K, const void* w_packed,
                                 const float* w_scale, int64_t N, const uint16_t* bias, void* out, int mode,
-                                void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+                                void* ws, size_t ws_bytes, w8a8_stream_t stream, const int32_t* qbias = nullptr) {
   if (M < 0 || M > INT32_MAX || N <= 0 || N > INT32_MAX) return W8A8_ERR_SHAPE;
   if (w8a8_status s = check_k(K)) return s;
   if (M == 0) return W8A8_OK;
   if (!q || !w_packed || !out || !ws) return (!ws && q && w_packed && out) ? W8A8_ERR_WORKSPACE : W8A8_ERR_NULL;
-  if (mode == EPI_BF16 && (!x_scale || !w_scale)) return W8A8_ERR_NULL;
+  if (mode == EPI_BF16 && (!w_scale || (!x_scale && !qbias))) return W8A8_ERR_NULL;
   if (!aligned16(q) || (reinterpret_cast<uintptr_t>(w_packed) & 255u)) return W8A8_ERR_ALIGN;
   const GemmWs L = gemm_ws_layout(1, M, N, K);
   if (ws_bytes < L.total || !aligned16(ws)) return W8A8_ERR_WORKSPACE;
@@ -434,6 +434,7 @@ static w8a8_status dense_common(const int8_t* q, const float* x_scale, int64_t M
   a.pack_flags = 0u;
   a.w_scale = w_scale;
   a.bias = bias;
+  a.qbias = qbias;
   a.out = out;
   a.mode = mode;
   return run_gemm(a, ws, L, reinterpret_cast<cudaStream_t>(stream), sms);
@@ -448,6 +449,42 @@ w8a8_status w8a8_quant_matmul(const int8_t* q, const float* x_scale, int64_t M, 
 w8a8_status w8a8_int8_matmul_acc(const int8_t* q, int64_t M, int64_t K, const void* w_packed, int64_t N,
                                  int32_t* acc, void* ws, size_t ws_bytes, w8a8_stream_t stream) {
   return dense_common(q, nullptr, M, K, w_packed, nullptr, N, nullptr, acc, EPI_ACC, ws, ws_bytes, stream);
+}
+
+static bool static_params_ok(float s, int32_t o) { return s > 0.0f && s < 3.0e38f && o >= -128 && o <= 127; }
+
+w8a8_status w8a8_static_quant(const uint16_t* x, int64_t M, int64_t K, float input_scale, int32_t input_offset,
+                              int8_t* q, w8a8_stream_t stream) {
+  if (M < 0 || M > INT32_MAX || !static_params_ok(input_scale, input_offset)) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (M == 0) return W8A8_OK;
+  if (!x || !q) return W8A8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_static_quant(x, M, K, input_scale, input_offset, q, reinterpret_cast<cudaStream_t>(stream),
+                                         sms));
+}
+
+w8a8_status w8a8_static_prepare(const int8_t* w, int64_t N, int64_t K, const float* w_scale, float input_scale,
+                                int32_t input_offset, const uint16_t* bias, float* deq_scale, int32_t* quant_bias,
+                                w8a8_stream_t stream) {
+  if (N <= 0 || N > INT32_MAX || !static_params_ok(input_scale, input_offset)) return W8A8_ERR_SHAPE;
+  if (w8a8_status s = check_k(K)) return s;
+  if (!w || !w_scale || !deq_scale || !quant_bias) return W8A8_ERR_NULL;
+  if (!aligned16(w)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_static_prepare(w, N, K, w_scale, input_scale, input_offset, bias, deq_scale, quant_bias,
+                                           reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+w8a8_status w8a8_static_quant_matmul(const int8_t* q, int64_t M, int64_t K, const void* w_packed,
+                                     const float* deq_scale, const int32_t* quant_bias, int64_t N, uint16_t* y,
+                                     void* ws, size_t ws_bytes, w8a8_stream_t stream) {
+  if (M > 0 && !quant_bias) return W8A8_ERR_NULL;
+  return dense_common(q, nullptr, M, K, w_packed, deq_scale, N, nullptr, y, EPI_BF16, ws, ws_bytes, stream,
+                      quant_bias);
 }
 
 size_t w8a8_grouped_matmul_workspace_bytes(int64_t E, int64_t R, int64_t N, int64_t K) {

@@ -130,6 +130,17 @@ __device__ __forceinline__ float dequant(int32_t acc, float sx, float sw) {
   return __fmul_rn(__fmul_rn(__int2float_rn(acc), sx), sw);
 }
 
+// The same with an integer bias added to the accumulator first (static W8A8: quant_bias, with sx = 1
+// and sw = deq_scale): float(acc + qb) * sx * sw with the sum exact -- in 32 bits, or in 64 bits where
+// the 32-bit sum would wrap (rare: |acc| < 2^31 and |qb| < 2^31 both hold).
+__device__ __forceinline__ float dequant_q(int32_t acc, int32_t qb, float sx, float sw) {
+  const int32_t s = static_cast<int32_t>(static_cast<uint32_t>(acc) + static_cast<uint32_t>(qb));
+  float f;
+  if (__builtin_expect(((acc ^ s) & (qb ^ s)) < 0, 0)) f = __ll2float_rn(static_cast<long long>(acc) + qb);
+  else f = __int2float_rn(s);
+  return __fmul_rn(__fmul_rn(f, sx), sw);
+}
+
 // ------------------------------------------------------------- PTX helpers --
 
 // Programmatic dependent launch.  pdl_trigger: a kernel launched after this

@@ -191,6 +191,7 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
   // epilogue inputs of this row block, loaded by the converter warps before their first stage
   __shared__ float s_sw[DC_ROWS];
   __shared__ float s_bias[DC_ROWS];
+  __shared__ int32_t s_qb[DC_ROWS];
   __shared__ float s_sx[DC_TOK];
 
   const int tid = threadIdx.x;
@@ -275,6 +276,7 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
       const int64_t n = static_cast<int64_t>(rb) * DC_ROWS + ct;
       s_sw[ct] = n < N ? a.w_scale[n] : 0.0f;
       s_bias[ct] = (a.bias != nullptr && n < N) ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
+      s_qb[ct] = (a.qbias != nullptr && n < N) ? a.qbias[n] : 0;
     }
     // Weights: every stage of the slice is widened into its own tensor-memory A stage as it lands,
     // independent of the activations (which the previous grid may still be writing).
@@ -301,7 +303,7 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     asm volatile("bar.sync 1, %0;" ::"n"(32 * DC_CONV_WARPS) : "memory");
     if (MODE != EPI_ACC && ct >= DC_ROWS && ct < DC_ROWS + DC_TOK) {  // token scales: the previous grid's output
       pdl_wait();
-      s_sx[ct - DC_ROWS] = ct - DC_ROWS < M ? a.x_scale[ct - DC_ROWS] : 0.0f;
+      s_sx[ct - DC_ROWS] = ct - DC_ROWS < M ? (a.x_scale != nullptr ? a.x_scale[ct - DC_ROWS] : 1.0f) : 0.0f;
     }
     for (int i = 0; i < my && ok; ++i) {
       const int got = mbar_wait(smem_u32(&bar_x[i]), 0u, &s_abort, a.status, 16u) ? 1 : 0;
@@ -454,7 +456,8 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
         uint16_t o[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          float fv = dequant(sum[r], sx, s_sw[r0 + r]);
+          float fv = a.qbias != nullptr ? dequant_q(sum[r], s_qb[r0 + r], sx, s_sw[r0 + r])
+                                        : dequant(sum[r], sx, s_sw[r0 + r]);
           if (a.bias) fv = __fadd_rn(fv, s_bias[r0 + r]);
           o[r] = f32_to_bf16_bits(fv);
         }

@@ -382,7 +382,7 @@ reg_gemm_kernel(const GemmArgs a, const int ksplit) {
       for (int c = tid; c < T::BMT * (T::BNW / 8); c += NT) {
         const int m = c / (T::BNW / 8), n8 = (c % (T::BNW / 8)) * 8;
         if (m >= rows_t) continue;
-        const float sx = a.x_scale[r0 + m];
+        const float sx = a.x_scale != nullptr ? a.x_scale[r0 + m] : 1.0f;
         uint16_t* dst = out + (r0 + m) * N + n0 + n8;
         const int* src = S + m * T::kEpiStride + n8;
         uint16_t v[8];
@@ -391,7 +391,7 @@ reg_gemm_kernel(const GemmArgs a, const int ksplit) {
           const int64_t n = n0 + n8 + k;
           float f = 0.0f;
           if (n8 + k < rows_w) {
-            f = dequant(src[k], sx, sw[n]);
+            f = a.qbias != nullptr ? dequant_q(src[k], a.qbias[n], sx, sw[n]) : dequant(src[k], sx, sw[n]);
             if (a.bias) f = __fadd_rn(f, bf16_bits_to_f32(a.bias[n]));
           }
           v[k] = f32_to_bf16_bits(f);

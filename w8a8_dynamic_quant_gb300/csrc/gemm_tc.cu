@@ -114,10 +114,47 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int*
   return ti;
 }
 
+// Per-channel factors of a 128-column output segment, staged in shared memory by each epilogue warp for
+// the BF16 epilogue: weight scale, integer bias (static W8A8) and float bias (0 where absent).
+struct __align__(16) SegFactors {
+  float w[128];
+  int32_t qb[128];
+  float b[128];
+  int narrow;  // every |qb| <= 2^31 - 1 - 16384*K: acc + qb cannot leave int32 (|acc| <= 16384*K)
+  int pad[3];  // keeps every element of an array of these 16-byte aligned (16-byte shared loads)
+};
+static_assert(sizeof(SegFactors) % 16 == 0, "SegFactors must keep 16-byte alignment in arrays");
+
+// Warp-cooperative: the factors of columns [n_base, n_base + 128) of expert e into f (lane l takes
+// columns l, l+32, l+64, l+96).  The caller's __syncwarp() makes them visible to the warp.
+__device__ __forceinline__ void stage_factors(const GemmArgs& a, int e, int64_t n_base, int lane, SegFactors& f) {
+  const int64_t N = a.N;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;
+    const int64_t n = n_base + c;
+    const bool in = n < N;
+    f.w[c] = in ? a.w_scale[static_cast<int64_t>(e) * N + n] : 0.0f;
+    f.qb[c] = (in && a.qbias != nullptr) ? a.qbias[n] : 0;
+    f.b[c] = (in && a.bias != nullptr) ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
+  }
+  if (a.qbias != nullptr) {
+    const int64_t room = 2147483647LL - 16384LL * a.K;
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ok = ok && (f.qb[lane + 32 * i] <= room && -static_cast<int64_t>(f.qb[lane + 32 * i]) <= room);
+    const bool all = __all_sync(0xffffffffu, ok);
+    if (lane == 0) f.narrow = all ? 1 : 0;
+  }
+}
+
 // Stores one output row segment of a finished tile: global row gr, 128
 // columns from n_base (expert e's weight rows), from the exact int32 sums.
+// fac: the segment's factors staged in shared memory (BF16 epilogue), or nullptr to read them from
+// global memory.  A missing x_scale reads as 1 (static W8A8, with qbias).
 template <int MODE>
-__device__ __forceinline__ void store_row(const GemmArgs& a, int e, int64_t gr, int64_t n_base, const int (&sums)[128]) {
+__device__ __forceinline__ void store_row(const GemmArgs& a, int e, int64_t gr, int64_t n_base, const int (&sums)[128],
+                                          const SegFactors* fac = nullptr) {
   const int64_t N = a.N;
   if constexpr (MODE == EPI_ACC) {
     int32_t* dst = static_cast<int32_t*>(a.out) + gr * N + n_base;
@@ -134,22 +171,52 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, int e, int64_t gr, 
       }
     }
   } else if constexpr (MODE == EPI_BF16) {
-    const float sx = a.x_scale[gr];
+    const float sx = a.x_scale != nullptr ? a.x_scale[gr] : 1.0f;
     const float* sw = a.w_scale + static_cast<int64_t>(e) * N;
     uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * N + n_base;
     const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((N & 7) == 0) && (n_base + 128 <= N);
 #pragma unroll
     for (int c8 = 0; c8 < 16; ++c8) {
       uint16_t v[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int64_t n = n_base + 8 * c8 + k;
-        float f = 0.0f;
-        if (n < N) {
-          f = dequant(sums[8 * c8 + k], sx, sw[n]);
-          if (a.bias) f = __fadd_rn(f, bf16_bits_to_f32(a.bias[n]));
+      if (fac != nullptr) {  // staged factors: broadcast 16-byte shared loads
+        const float4 w0 = reinterpret_cast<const float4*>(fac->w)[2 * c8];
+        const float4 w1 = reinterpret_cast<const float4*>(fac->w)[2 * c8 + 1];
+        const float w8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        int32_t q8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        float b8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        if (a.qbias != nullptr) {
+          const int4 q0 = reinterpret_cast<const int4*>(fac->qb)[2 * c8];
+          const int4 q1 = reinterpret_cast<const int4*>(fac->qb)[2 * c8 + 1];
+          q8[0] = q0.x; q8[1] = q0.y; q8[2] = q0.z; q8[3] = q0.w;
+          q8[4] = q1.x; q8[5] = q1.y; q8[6] = q1.z; q8[7] = q1.w;
         }
-        v[k] = f32_to_bf16_bits(f);
+        if (a.bias != nullptr) {
+          const float4 b0 = reinterpret_cast<const float4*>(fac->b)[2 * c8];
+          const float4 b1 = reinterpret_cast<const float4*>(fac->b)[2 * c8 + 1];
+          b8[0] = b0.x; b8[1] = b0.y; b8[2] = b0.z; b8[3] = b0.w;
+          b8[4] = b1.x; b8[5] = b1.y; b8[6] = b1.z; b8[7] = b1.w;
+        }
+        const bool narrow = a.qbias != nullptr && fac->narrow;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float f;
+          if (narrow) f = __fmul_rn(__fmul_rn(__int2float_rn(sums[8 * c8 + k] + q8[k]), sx), w8[k]);
+          else if (a.qbias != nullptr) f = dequant_q(sums[8 * c8 + k], q8[k], sx, w8[k]);
+          else f = dequant(sums[8 * c8 + k], sx, w8[k]);
+          if (a.bias) f = __fadd_rn(f, b8[k]);
+          v[k] = f32_to_bf16_bits(f);  // columns past N (factors 0) are not stored
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int64_t n = n_base + 8 * c8 + k;
+          float f = 0.0f;
+          if (n < N) {
+            f = a.qbias != nullptr ? dequant_q(sums[8 * c8 + k], a.qbias[n], sx, sw[n]) : dequant(sums[8 * c8 + k], sx, sw[n]);
+            if (a.bias) f = __fadd_rn(f, bf16_bits_to_f32(a.bias[n]));
+          }
+          v[k] = f32_to_bf16_bits(f);
+        }
       }
       if (vec) {
         reinterpret_cast<uint4*>(dst)[c8] =
@@ -449,6 +516,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   __shared__ int s_unit_prefix[kMaxE + 1];
   __shared__ int s_row_off[kMaxE + 1];
   __shared__ int s_warp[TC_THREADS / 32];
+  __shared__ __align__(16) SegFactors s_fac[TC_EPI_WARPS];  // one per epilogue warp
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -604,6 +672,12 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int t = static_cast<int>(cluster_id); t < units && !s_abort; t += static_cast<int>(nclusters)) {
       int e, mb, nb;
       tile_of(t, e, mb, nb);
+      SegFactors& fac = s_fac[warp - 2];
+      if constexpr (MODE == EPI_BF16) {
+        // the segment's factors, loaded while the tile's MMAs run (read by this warp only)
+        stage_factors(a, e, static_cast<int64_t>(nb) * TC_BN + half * 128, lane, fac);
+        __syncwarp();
+      }
       int sums[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sums[i] = 0;
@@ -637,7 +711,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const int m0 = mb * P_BM + static_cast<int>(rank) * P_HALF;  // first row of this CTA inside the expert
       const int64_t n_base = static_cast<int64_t>(nb) * TC_BN + half * 128;
       if (m0 + r_loc < s_row_off[e + 1] - s_row_off[e] && n_base < N)
-        store_row<MODE>(a, e, static_cast<int64_t>(s_row_off[e]) + m0 + r_loc, n_base, sums);
+        store_row<MODE>(a, e, static_cast<int64_t>(s_row_off[e]) + m0 + r_loc, n_base, sums, &fac);
     }
   }
 

@@ -48,6 +48,12 @@ cudaError_t launch_scatter_rows_i8(const int8_t* xq_tok, const float* xs_tok, in
 cudaError_t launch_combine(const uint16_t* y_routed, const int32_t* pos, const float* w, int64_t T, int k,
                            int64_t H, uint16_t* y, DeviceStatus* status, cudaStream_t stream, int num_sms);
 
+// Static W8A8 (static.cu): q = clamp(rint(x / s) + o, -128, 127); load-time deq_scale / quant_bias.
+cudaError_t launch_static_quant(const uint16_t* x, int64_t M, int64_t K, float s, int o, int8_t* q,
+                                cudaStream_t stream, int num_sms);
+cudaError_t launch_static_prepare(const int8_t* w, int64_t N, int64_t K, const float* w_scale, float s, int o,
+                                  const uint16_t* bias, float* deq, int32_t* qb, cudaStream_t stream, int num_sms);
+
 // Epilogue of the contraction.
 enum EpiMode : int {
   EPI_BF16 = 0,    // y[r,n] = bf16(((float)acc * sx[r]) * sw[e,n] (+ bias[n]))
@@ -66,6 +72,8 @@ struct GemmArgs {
   int pack_known = 0;                 // 1: this process packed the buffer with these E, N, K (host record)
   const float* w_scale = nullptr;     // [E,N] in ORIGINAL channel order
   const uint16_t* bias = nullptr;     // [N] bf16 or nullptr (dense only)
+  const int32_t* qbias = nullptr;     // [N] int32 added to the accumulator before dequant, or nullptr (dense,
+                                      // static W8A8; x_scale is then nullptr and reads as 1)
   void* out = nullptr;                // bf16 [R,N] | int32 [R,N] | bf16 h [R,N/2]
   int mode = EPI_BF16;
   DeviceStatus* status = nullptr;

@@ -26,6 +26,9 @@ Recipe (one generator per case, seed 0 unless stated; draw order fixed):
          N(0,1) * 0.02 * 2^c per output channel, c uniform in {-4..2}, and one
          element in every 64th channel multiplied by 8 (an outlier); drawn on
          the target device with torch's seeded generator, rounded to BF16.
+  static W8A8: per-tensor input scale U[0.02, 0.04] (binary32) and input
+         offset uniform in {-8..8}, stand-ins for calibrated values, drawn
+         per workload from their own generator.
 BF16 rounding of the drawn fp32 values uses torch's conversion.
 """
 from __future__ import annotations
@@ -201,6 +204,12 @@ def make_moe(T: int, H: int, I: int, E: int, topk: int, routing: str = "uniform"
                      token_index=token_index, group_list=counts, x=np.ascontiguousarray(x),
                      x_scale=x_scale, w13=w13, s13=s13, w2=w2, s2=s2, extra=dict(p=p),
                      x_tok=x_tok, x_tok_scale=s_tok, topk_weights=topk_weights)
+
+
+def static_params(cfg_id: int, seed: int = 0):
+    """(input_scale, input_offset) of the static variant for a workload."""
+    rng = rng_for(seed * 31 + cfg_id + 1000)
+    return float(np.float32(rng.uniform(0.02, 0.04))), int(rng.integers(-8, 9))
 
 
 def make_bf16_weight(E: int, N: int, K: int, seed: int = 0, device: str = "cpu") -> torch.Tensor:
