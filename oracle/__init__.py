@@ -72,6 +72,12 @@ def _load(path: str) -> ctypes.CDLL:
     L.oracle_static_quant.argtypes = [_vp, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int32, _vp]
     L.oracle_static_prepare.argtypes = [_vp, _c_i64, _c_i64, _vp, ctypes.c_float, ctypes.c_int32, _vp, _vp, _vp]
     L.oracle_static_quant_matmul.argtypes = [_vp, _c_i64, _c_i64, _vp, _c_i64, _vp, _vp, _vp]
+    L.oracle_e4m3_from_f32.argtypes = [ctypes.c_float]
+    L.oracle_e4m3_from_f32.restype = ctypes.c_uint8
+    L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_to_f32.restype = ctypes.c_float
+    L.oracle_mx_quant.argtypes = [_vp, _c_i64, _c_i64, _vp, _vp]
+    L.oracle_mx_matmul.argtypes = [_vp, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _vp]
     L.oracle_quantize_weight.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
     L.oracle_moe_route.argtypes = [_vp, _c_i64, _c_i64, _c_i64, _vp, _vp]
     L.oracle_moe_permute_quant.argtypes = [_vp, _vp, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _vp,
@@ -353,3 +359,31 @@ def moe_layer(x, x_scale, topk_ids, topk_weights, w13, s13, w2, s2, want_routed=
         _p(x), _p(xs_in), _p(ids), _p(w), T, k, E, H, I, _p(w13), _p(s13), _p(w2), _p(s2), _p(y),
         _p(yr)))
     return (y, yr) if want_routed else y
+
+
+def e4m3_from_f32(v: float) -> int:
+    return int(lib().oracle_e4m3_from_f32(float(v)))
+
+
+def e4m3_to_f32(b: int) -> float:
+    return float(lib().oracle_e4m3_to_f32(int(b)))
+
+
+def mx_quant(x):
+    """bf16 bits x [M,K] (K % 32 == 0) -> (uint8 E4M3 codes [M,K], uint8 E8M0 scales [M,K/32])."""
+    x = _c(x, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((M, K // 32), np.uint8)
+    _check("oracle_mx_quant", lib().oracle_mx_quant(_p(x), M, K, _p(q), _p(s)))
+    return q, s
+
+
+def mx_matmul(qa, sa, qw, sw):
+    """MXFP8 operands (E4M3 codes + E8M0 scales per 32 along K) -> bf16 bits y [M,N] (float64 sum)."""
+    qa, sa, qw, sw = (_c(t, np.uint8) for t in (qa, sa, qw, sw))
+    M, K = qa.shape
+    N = qw.shape[0]
+    y = np.empty((M, N), np.uint16)
+    _check("oracle_mx_matmul", lib().oracle_mx_matmul(_p(qa), _p(sa), M, K, _p(qw), _p(sw), N, _p(y)))
+    return y

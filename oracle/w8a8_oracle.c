@@ -587,3 +587,124 @@ done:
   free(yr);
   return rc;
 }
+
+/* ------------------------------------------------------------ MXFP8 -- */
+/*
+ * [P2] "Qwen3.8-FP8 on Ascend 950: Why Weights Become MXFP8 at Load Time",
+ * sections 3 and 5: the MXFP8 contract -- an E4M3 payload with one E8M0
+ * (power-of-two) scale per 32 values along the reduction axis K, for the
+ * weights (re-quantised at load) and for each activation row (quantised at
+ * run time, group sizes [1,1,32]); the matmul consumes both scales.
+ *
+ * READING (scale): the pages name the scale algorithm only as "0, the normal
+ * case".  Taken as the OCP Microscaling rule: for each group of 32 values,
+ * shared = floor(log2(max |v|)) - 8 (8 = the largest E4M3 exponent),
+ * clamped to [-127, 127]; the E8M0 byte is shared + 127; a group of zeros
+ * gets byte 0.  Elements: v / 2^shared (exact) rounded to E4M3 to nearest,
+ * ties to even, saturating at +-448 (the E4M3 "fn" variant: no infinities,
+ * NaN = S.1111.111).
+ * READING (matmul): y[m,n] = bf16_rne( sum_g Sa[m,g] * Sw[n,g] *
+ * sum_{k in g} a[m,k] * w[n,k] ) with the sum taken in float64 here (the
+ * products of E4M3 values and powers of two are exact); a tensor-core
+ * implementation accumulates in binary32, so parity is within a bound.
+ */
+static double pow2d(int e) { return ldexp(1.0, e); }
+
+/* E4M3 (fn) byte of a binary32 value: round to nearest even, saturate. */
+uint8_t oracle_e4m3_from_f32(float v) {
+  if (v != v) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;             /* largest finite: 1.75 * 2^8 */
+  if (a < pow2d(-6)) {                            /* subnormal steps of 2^-9 */
+    const double m = nearbyint(a / pow2d(-9));    /* 0..8; 8 is the smallest normal */
+    return sign | (uint8_t)m;
+  }
+  int e;
+  (void)frexp(a, &e);
+  e -= 1;                                         /* a in [2^e, 2^(e+1)) */
+  double m = nearbyint((a / pow2d(e) - 1.0) * 8.0);  /* 3 mantissa bits */
+  if (m == 8.0) {
+    m = 0.0;
+    e += 1;
+  }
+  if (e > 8) return sign | 0x7E;
+  return sign | (uint8_t)(((e + 7) << 3) | (int)m);
+}
+
+float oracle_e4m3_to_f32(uint8_t b) {
+  const int sign = b & 0x80;
+  const int ex = (b >> 3) & 0xF;
+  const int man = b & 0x7;
+  if (ex == 0xF && man == 0x7) return NAN;
+  double v = ex == 0 ? man * pow2d(-9) : (1.0 + man / 8.0) * pow2d(ex - 7);
+  return (float)(sign ? -v : v);
+}
+
+/* x bf16 [M,K] (K % 32 == 0) -> q E4M3 [M,K], scale E8M0 [M,K/32]. */
+int oracle_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale) {
+  if (M < 0 || K <= 0 || K % 32 != 0) return ORC_ERR_SHAPE;
+  const int64_t G = K / 32;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m)
+    for (int64_t g = 0; g < G; ++g) {
+      const uint16_t* xs = x + m * K + g * 32;
+      float amax = 0.0f;
+      int nan = 0;
+      for (int i = 0; i < 32; ++i) {
+        const float v = oracle_bf16_to_f32(xs[i]);
+        if (v != v) nan = 1;
+        else if (fabsf(v) > amax) amax = fabsf(v);
+      }
+      int shared = -127;
+      if (amax > 0.0f) {
+        int e;
+        (void)frexp((double)amax, &e);
+        shared = (e - 1) - 8;
+        if (shared < -127) shared = -127;
+        if (shared > 127) shared = 127;
+      }
+      scale[m * G + g] = nan ? 0xFF : (uint8_t)(shared + 127);
+      for (int i = 0; i < 32; ++i) {
+        const double v = (double)oracle_bf16_to_f32(xs[i]) / pow2d(shared);
+        q[m * K + g * 32 + i] = oracle_e4m3_from_f32((float)v);
+      }
+    }
+  return ORC_OK;
+}
+
+/* bf16 bits of a double, rounded to nearest even (normal range). */
+static uint16_t bf16_from_f64(double x) {
+  if (x == 0.0) return signbit(x) ? 0x8000 : 0x0000;
+  int e;
+  (void)frexp(fabs(x), &e);
+  const double ulp = pow2d((e - 1) - 7);
+  const double r = nearbyint(x / ulp) * ulp;      /* exact: a bf16 value */
+  const float f = (float)r;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+/* qa E4M3 [M,K] + sa E8M0 [M,K/32], qw E4M3 [N,K] + sw E8M0 [N,K/32] -> y bf16 [M,N]. */
+int oracle_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
+                     const uint8_t* sw, int64_t N, uint16_t* y) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 32 != 0) return ORC_ERR_SHAPE;
+  const int64_t G = K / 32;
+  int64_t m;
+#pragma omp parallel for schedule(static)
+  for (m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t g = 0; g < G; ++g) {
+        double part = 0.0;
+        for (int i = 0; i < 32; ++i)
+          part += (double)oracle_e4m3_to_f32(qa[m * K + g * 32 + i]) *
+                  (double)oracle_e4m3_to_f32(qw[n * K + g * 32 + i]);
+        acc += part * pow2d((int)sa[m * G + g] - 127) * pow2d((int)sw[n * G + g] - 127);
+      }
+      y[m * N + n] = bf16_from_f64(acc);
+    }
+  return ORC_OK;
+}

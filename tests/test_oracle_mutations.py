@@ -52,6 +52,12 @@ MUTATIONS = [
      "double c = (double)rintf(t + (float)o);", "test_static_quant_brute_force_and_closed_forms", ()),
     ("static codes clamped at -127", "if (c < -128.0) c = -128.0;", "if (c < -127.0) c = -127.0;",
      "test_static_quant_brute_force_and_closed_forms", ()),
+    ("MX shared exponent one too high", "shared = (e - 1) - 8;", "shared = e - 8;",
+     "test_mx_quant_closed_forms_and_bounds", ()),
+    ("E4M3 without saturation", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 464.0) return sign | 0x7F;",
+     "test_e4m3_encode_decode_against_torch", ()),
+    ("MX matmul drops the weight scale", "acc += part * pow2d((int)sa[m * G + g] - 127) * pow2d((int)sw[n * G + g] - 127);",
+     "acc += part * pow2d((int)sa[m * G + g] - 127);", "test_mx_matmul_against_float64", ()),
     ("combine sums in double", "      float s = 0.0f;\n      for (int64_t j", "      double s = 0.0;\n      for (int64_t j",
      "test_combine_closed_forms_and_order", ()),
 ]

@@ -590,3 +590,75 @@ def test_static_path_approximates_the_float_layer(o):
     xd = float(s) * (q.astype(np.float64) - o)
     ref_q = xd @ wd.T + f32(bias).astype(np.float64)[None, :]
     assert np.all(np.abs(y - ref_q) <= 0.5 * deq[None, :] + np.abs(ref_q) * 2.0 ** -8 * 1.01 + 1e-9)
+
+
+# -------------------------------------------------------------------- MXFP8 ----
+
+def test_e4m3_encode_decode_against_torch():
+    """The E4M3 codes of every BF16 value up to 448 in magnitude equal torch's float8_e4m3fn conversion
+    (round to nearest even); every code decodes as torch decodes it; beyond 448 the codes saturate."""
+    bits = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    v = f32(bits)
+    fin = np.isfinite(v) & (np.abs(v) <= 448)
+    vals = v[fin][::7]  # a spread subset keeps the test quick
+    ours = np.array([oracle.e4m3_from_f32(x) for x in vals], np.uint8)
+    ref = torch.from_numpy(vals.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    codes = np.arange(256, dtype=np.uint8)
+    dec = np.array([oracle.e4m3_to_f32(int(c)) for c in codes], np.float32)
+    tdec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    same = (dec == tdec) | (np.isnan(dec) & np.isnan(tdec))
+    assert same.all()
+    for x, b in [(448.0, 0x7E), (449.0, 0x7E), (1e30, 0x7E), (-600.0, 0xFE), (2.0 ** -10, 0x00),
+                 (3 * 2.0 ** -10, 0x02), (2.0 ** -6, 0x08)]:
+        assert oracle.e4m3_from_f32(x) == b, x
+
+
+def test_mx_quant_closed_forms_and_bounds():
+    rng = np.random.default_rng(41)
+    M, K = 6, 128
+    x = (rng.standard_normal((M, K)) * 2.0 ** rng.integers(-20, 20, (M, 1))).astype(np.float32)
+    x[0, :32] = 1.0                  # all ones: shared exponent 0 - 8, codes 256 = 2^8
+    x[1, 32:64] = 0.0                # zeros: scale byte 0, codes 0
+    x[2, 64:96] = 0.0
+    x[2, 70] = -3.0                  # one value: 3 = 1.5 * 2^1 -> shared -7, element 384
+    xb = S.to_bf16_bits(x)
+    q, s = oracle.mx_quant(xb)
+    assert s[0, 0] == 127 - 8 and np.all(q[0, :32] == 0x78)
+    assert s[1, 1] == 0 and np.all(q[1, 32:64] == 0)
+    assert s[2, 2] == 127 - 7 and q[2, 70] == oracle.e4m3_from_f32(-384.0)
+    # shared = floor(log2 amax) - 8 for every group
+    xf = f32(xb).astype(np.float64).reshape(M, K // 32, 32)
+    amax = np.abs(xf).max(axis=2)
+    live = amax > 0
+    want = np.floor(np.log2(amax[live])) - 8 + 127
+    assert np.array_equal(s[live].astype(np.float64), want)
+    # reconstruction: within half a step of the 3-bit mantissa, or the saturation at 448 for the top values
+    dec = np.vectorize(oracle.e4m3_to_f32)(q).astype(np.float64).reshape(M, K // 32, 32)
+    scale = 2.0 ** (s.astype(np.float64) - 127)[..., None]
+    rec = dec * scale
+    y = xf / scale
+    step = np.where(np.abs(y) >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))) - 3), 2.0 ** -9)
+    ok = np.abs(rec - xf) <= 0.5 * step * scale + 1e-300
+    sat = np.abs(y) > 448
+    assert np.all(ok | sat)
+    assert np.all(np.abs(dec[sat]) == 448)
+
+
+def test_mx_matmul_against_float64():
+    rng = np.random.default_rng(42)
+    M, N, K = 9, 13, 96
+    xa = S.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    xw = S.to_bf16_bits((rng.standard_normal((N, K)) * 0.05).astype(np.float32))
+    qa, sa = oracle.mx_quant(xa)
+    qw, sw = oracle.mx_quant(xw)
+    y = f32(oracle.mx_matmul(qa, sa, qw, sw)).astype(np.float64)
+    dec = np.vectorize(oracle.e4m3_to_f32)
+    A = dec(qa).astype(np.float64) * np.repeat(2.0 ** (sa.astype(np.float64) - 127), 32, axis=1)
+    B = dec(qw).astype(np.float64) * np.repeat(2.0 ** (sw.astype(np.float64) - 127), 32, axis=1)
+    ref = A @ B.T
+    assert np.all(np.abs(y - ref) <= bf16_ulp(ref) * 0.5 * 1.001 + 1e-30)
+    # and the MX product approximates the BF16 product within the E4M3 rounding of both operands
+    full = f32(xa).astype(np.float64) @ f32(xw).astype(np.float64).T
+    mag = np.abs(f32(xa)).astype(np.float64) @ np.abs(f32(xw)).astype(np.float64).T
+    assert np.all(np.abs(y - full) <= 2 * 2.0 ** -4 * mag + bf16_ulp(full))
