@@ -310,6 +310,53 @@ class DenseStatic(Dense):
         oracle.static_quant_matmul(q, self.d.w, *self._prep)
 
 
+class DenseMX(Dense):
+    """MXFP8 quantisation of a dense workload's activations (E4M3 + one E8M0 scale per 32 along K); the
+    MXFP8 contraction is not built yet, so the step is the quantiser alone (GB/s)."""
+
+    def __init__(self, cfg_id: int, device):
+        super().__init__(cfg_id, device)
+        torch, M, K = self.torch, self.M, self.K
+        self.name = self.d.name + "_mx_quant"
+        for st in self.sets:
+            st["mq"] = torch.empty((M, K), dtype=torch.uint8, device=device)
+            st["ms"] = torch.empty((M, K // 32), dtype=torch.uint8, device=device)
+        self.kernels = ["mx_quant"]
+        nbytes = 2 * M * K + M * K + M * K // 32
+        self.alg_bytes = {"mx_quant": nbytes}
+        self.alg_flops = {}
+        self.units_per_step = float(nbytes)
+        self.unit = "GB/s"
+        self.bound = "hbm"
+        self.launches_per_step = 1
+
+    def launch(self, kernel: str, i: int):
+        st = self.sets[i]
+        self.W.w8a8_mx_quant(st["x"], st["mq"], st["ms"])
+
+    def value(self, units, seconds):
+        return units / seconds / 1e9
+
+    def e2e_setup(self, device):
+        super().e2e_setup(device)
+        self.hq = self.torch.empty((self.M, self.K), dtype=self.torch.uint8).pin_memory()
+        self.d2h = self.hq.numel() + self.M * self.K // 32
+
+    def e2e_step(self):
+        st = self.sets[0]
+        st["x"].copy_(self.hx, non_blocking=True)
+        q, s = self.W.w8a8_mx_quant(st["x"], st["mq"], st["ms"])
+        self.hq.copy_(q, non_blocking=True)
+        self.torch.cuda.current_stream().synchronize()
+
+    def oracle_units(self, rows):
+        return float(rows * (3 * self.K + self.K // 32))
+
+    def oracle_step(self, rows):
+        import oracle
+        oracle.mx_quant(self.d.x[:rows])
+
+
 class MoE:
     """MoE expert FFN: (quant) -> W13 grouped GEMM + SwiGLU -> requant -> W2 grouped GEMM."""
 
@@ -636,10 +683,12 @@ class WeightPrep:
         return self.channels
 
 
-def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False, static=False):
+def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False, static=False, mx=False):
     from w8a8_dynamic_quant_gb300 import synthetic as S
     if prepare:
         return WeightPrep(cfg_id, device)
+    if mx:
+        return DenseMX(cfg_id, device)
     if S.CONFIGS[cfg_id]["kind"] == "dense":
         return DenseStatic(cfg_id, device) if static else Dense(cfg_id, device)
     return MoETokens(cfg_id, device, kernels) if from_tokens else MoE(cfg_id, device)
@@ -764,7 +813,7 @@ def run_gpu(args):
     __graft_entry__.build()
     peaks = load_peaks()
     kernels = args.kernels.split(",") if args.kernels else None
-    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare, args.static)
+    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare, args.static, args.mx)
     step_kernels = getattr(wl, "step_kernels", wl.kernels)
     stream = torch.cuda.current_stream(device)
 
@@ -908,6 +957,8 @@ def main(argv=None):
     ap.add_argument("--static", action="store_true",
                     help="dense workloads: the static W8A8 variant (fixed input scale and offset, load-time "
                          "deq_scale and quant_bias)")
+    ap.add_argument("--mx", action="store_true",
+                    help="dense workloads: the MXFP8 quantiser of the activations alone (GB/s)")
     ap.add_argument("--prepare", action="store_true",
                     help="time the load-time weight preparation instead: the workload's weights quantised per "
                          "channel from BF16 and packed in one pass (GB/s)")

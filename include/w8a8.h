@@ -225,6 +225,21 @@ W8A8_API w8a8_status w8a8_static_quant_matmul(const int8_t* q, int64_t M, int64_
                                               uint16_t* y, void* ws, size_t ws_bytes, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8 quantisation -- [P2] sections 3 and 5: weights re-quantised to      */
+/* MXFP8 at load, activation rows at run time (group sizes [1,1,32]): an E4M3 */
+/* payload with one E8M0 (power-of-two) scale per 32 values along K, the     */
+/* normal scale algorithm: per group shared = floor(log2 max|v|) - 8,        */
+/* clamped to [-127, 127], scale byte = shared + 127 (0 for a group of zeros, */
+/* 0xFF for a group holding a NaN); elements v / 2^shared rounded to E4M3,   */
+/* nearest even, saturating at +-448.                                        */
+/* ------------------------------------------------------------------------ */
+
+/* x [M,K] bf16 -> q [M,K] E4M3 bytes, scale [M,K/32] E8M0 bytes.  K % 32 == 0,
+ * x and q 16-byte aligned.  Weights [N,K] (or [E*N,K]) take the same call. */
+W8A8_API w8a8_status w8a8_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale,
+                                   w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* MoE expert FFN -- [P1] §三 runner chain: (quantise only if no per-token   */
 /* scale was supplied) -> W13 grouped matmul -> SwiGLU -> per-token INT8     */
 /* requant -> W2 grouped matmul -> BF16.                                     */

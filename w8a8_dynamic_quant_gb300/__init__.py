@@ -26,7 +26,7 @@ __all__ = [
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
     "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
     "w8a8_quantize_weight", "w8a8_quantize_prepack_weight", "w8a8_static_quant", "w8a8_static_prepare",
-    "w8a8_static_quant_matmul", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
+    "w8a8_static_quant_matmul", "w8a8_mx_quant", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
     "moe_layer_workspace_offset", "moe_layer",
 ]
 
@@ -130,6 +130,20 @@ def w8a8_dynamic_quant(x: torch.Tensor, q: Optional[torch.Tensor] = None,
     _need(scale, "scale", torch.float32, (M,), x.device)
     with torch.cuda.device(x.device):
         _capi.check("w8a8_dynamic_quant", _capi.lib().w8a8_dynamic_quant(
+            x.data_ptr(), M, K, q.data_ptr(), scale.data_ptr(), _stream(x.device)))
+    return q, scale
+
+
+def w8a8_mx_quant(x: torch.Tensor, q: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None):
+    """MXFP8: bf16 x [M,K] (K % 32 == 0) -> (uint8 E4M3 codes [M,K], uint8 E8M0 scales [M,K/32])."""
+    _need(x, "x", torch.bfloat16)
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    scale = torch.empty((M, K // 32), dtype=torch.uint8, device=x.device) if scale is None else scale
+    _need(q, "q", torch.uint8, (M, K), x.device)
+    _need(scale, "scale", torch.uint8, (M, K // 32), x.device)
+    with torch.cuda.device(x.device):
+        _capi.check("w8a8_mx_quant", _capi.lib().w8a8_mx_quant(
             x.data_ptr(), M, K, q.data_ptr(), scale.data_ptr(), _stream(x.device)))
     return q, scale
 

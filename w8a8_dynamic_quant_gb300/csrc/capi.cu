@@ -451,6 +451,18 @@ w8a8_status w8a8_int8_matmul_acc(const int8_t* q, int64_t M, int64_t K, const vo
   return dense_common(q, nullptr, M, K, w_packed, nullptr, N, nullptr, acc, EPI_ACC, ws, ws_bytes, stream);
 }
 
+w8a8_status w8a8_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale,
+                          w8a8_stream_t stream) {
+  if (M < 0 || M > INT32_MAX || K <= 0 || K > W8A8_MAX_K) return W8A8_ERR_SHAPE;
+  if (K % 32 != 0) return W8A8_ERR_ALIGN;
+  if (M == 0) return W8A8_OK;
+  if (!x || !q || !scale) return W8A8_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_mx_quant(x, M, K, q, scale, reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
 static bool static_params_ok(float s, int32_t o) { return s > 0.0f && s < 3.0e38f && o >= -128 && o <= 127; }
 
 w8a8_status w8a8_static_quant(const uint16_t* x, int64_t M, int64_t K, float input_scale, int32_t input_offset,

@@ -54,6 +54,10 @@ cudaError_t launch_static_quant(const uint16_t* x, int64_t M, int64_t K, float s
 cudaError_t launch_static_prepare(const int8_t* w, int64_t N, int64_t K, const float* w_scale, float s, int o,
                                   const uint16_t* bias, float* deq, int32_t* qb, cudaStream_t stream, int num_sms);
 
+// MXFP8 quantisation (mx.cu): x [M,K] bf16 -> E4M3 q [M,K] + E8M0 scale [M,K/32].
+cudaError_t launch_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale, cudaStream_t stream,
+                            int num_sms);
+
 // Epilogue of the contraction.
 enum EpiMode : int {
   EPI_BF16 = 0,    // y[r,n] = bf16(((float)acc * sx[r]) * sw[e,n] (+ bias[n]))
