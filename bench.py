@@ -311,50 +311,51 @@ class DenseStatic(Dense):
 
 
 class DenseMX(Dense):
-    """MXFP8 quantisation of a dense workload's activations (E4M3 + one E8M0 scale per 32 along K); the
-    MXFP8 contraction is not built yet, so the step is the quantiser alone (GB/s)."""
+    """The MXFP8 variant of a dense workload: the activations quantised to E4M3 + one E8M0 scale per 32
+    along K, then the MXFP8 contraction against weights quantised the same way at load (TOPS)."""
 
     def __init__(self, cfg_id: int, device):
         super().__init__(cfg_id, device)
         torch, M, K = self.torch, self.M, self.K
-        self.name = self.d.name + "_mx_quant"
+        self.name = self.d.name + "_mxfp8"
+        N = self.N
+        # load time: the weights (the workload's INT8 weight times its channel scale, as BF16) to MXFP8
+        wbf = (torch.from_numpy(self.d.w).to(device).float() * torch.from_numpy(self.d.w_scale).to(device)[:, None])
+        wq, wsc = self.W.w8a8_mx_quant(wbf.to(torch.bfloat16))
         for st in self.sets:
             st["mq"] = torch.empty((M, K), dtype=torch.uint8, device=device)
             st["ms"] = torch.empty((M, K // 32), dtype=torch.uint8, device=device)
-        self.kernels = ["mx_quant"]
-        nbytes = 2 * M * K + M * K + M * K // 32
-        self.alg_bytes = {"mx_quant": nbytes}
-        self.alg_flops = {}
-        self.units_per_step = float(nbytes)
-        self.unit = "GB/s"
-        self.bound = "hbm"
-        self.launches_per_step = 1
+            st["wq"], st["wsc"] = wq.clone(), wsc.clone()
+        self.kernels = ["mx_quant", "mx_matmul"]
+        self.alg_bytes = {"mx_quant": 2 * M * K + M * K + M * K // 32,
+                          "mx_matmul": M * K + N * K + (M + N) * K // 32 + 2 * M * N}
+        self.alg_flops = {"mx_matmul": 2.0 * M * N * K}
+        self.launches_per_step = 2
+        self.tensor_peak_ratio = 2.0  # FP8 tensor rate: the measured bf16 peak x the nominal 2x
 
     def launch(self, kernel: str, i: int):
         st = self.sets[i]
-        self.W.w8a8_mx_quant(st["x"], st["mq"], st["ms"])
-
-    def value(self, units, seconds):
-        return units / seconds / 1e9
-
-    def e2e_setup(self, device):
-        super().e2e_setup(device)
-        self.hq = self.torch.empty((self.M, self.K), dtype=self.torch.uint8).pin_memory()
-        self.d2h = self.hq.numel() + self.M * self.K // 32
+        if kernel == "mx_quant":
+            self.W.w8a8_mx_quant(st["x"], st["mq"], st["ms"])
+        else:
+            self.W.w8a8_mx_matmul(st["mq"], st["ms"], st["wq"], st["wsc"], st["y"])
 
     def e2e_step(self):
         st = self.sets[0]
         st["x"].copy_(self.hx, non_blocking=True)
         q, s = self.W.w8a8_mx_quant(st["x"], st["mq"], st["ms"])
-        self.hq.copy_(q, non_blocking=True)
+        y = self.W.w8a8_mx_matmul(q, s, st["wq"], st["wsc"], st["y"])
+        self.hy.copy_(y, non_blocking=True)
         self.torch.cuda.current_stream().synchronize()
-
-    def oracle_units(self, rows):
-        return float(rows * (3 * self.K + self.K // 32))
 
     def oracle_step(self, rows):
         import oracle
-        oracle.mx_quant(self.d.x[:rows])
+        if not hasattr(self, "_wmx"):
+            wbf = (self.d.w.astype("float32") * self.d.w_scale[:, None])
+            from w8a8_dynamic_quant_gb300 import synthetic as S
+            self._wmx = oracle.mx_quant(S.to_bf16_bits(wbf))
+        qa, sa = oracle.mx_quant(self.d.x[:rows])
+        oracle.mx_matmul(qa, sa, *self._wmx)
 
 
 class MoE:
@@ -904,11 +905,13 @@ def run_gpu(args):
         peak, unit = peaks["hbm_gbs"], "GB/s"
     else:
         achieved = wl.alg_flops[dom] / dur_s / 1e12
-        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        peak, unit = peaks["bf16_tflops"] * getattr(wl, "tensor_peak_ratio", 1.0), "TFLOP/s"
     traffic = recorded_traffic(dom, wl.name)
     roofline = {"bound": wl.bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": traffic, "kernel": dom, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
-                if peaks["source"] == "measured" else "fallback",
+                "traffic": traffic, "kernel": dom, "peak_source": (f"{peaks['source']} (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback") +
+                (f" x {wl.tensor_peak_ratio:g} (nominal FP8/BF16 ratio)" if getattr(wl, "tensor_peak_ratio", 1.0) != 1.0
+                 and wl.bound == "tensor" else ""),
                 "alg_bytes_per_launch": wl.alg_bytes[dom],
                 "per_kernel_us": {k: v * 1e3 for k, v in per_kernel_ms.items()},
                 "sum_of_kernels_us": sum(per_kernel_ms[k] for k in step_kernels) * 1e3}
@@ -958,7 +961,7 @@ def main(argv=None):
                     help="dense workloads: the static W8A8 variant (fixed input scale and offset, load-time "
                          "deq_scale and quant_bias)")
     ap.add_argument("--mx", action="store_true",
-                    help="dense workloads: the MXFP8 quantiser of the activations alone (GB/s)")
+                    help="dense workloads: the MXFP8 variant (E4M3 + E8M0 per 32 along K, weights converted at load)")
     ap.add_argument("--prepare", action="store_true",
                     help="time the load-time weight preparation instead: the workload's weights quantised per "
                          "channel from BF16 and packed in one pass (GB/s)")

@@ -239,6 +239,15 @@ W8A8_API w8a8_status w8a8_static_quant_matmul(const int8_t* q, int64_t M, int64_
 W8A8_API w8a8_status w8a8_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale,
                                    w8a8_stream_t stream);
 
+/* MXFP8 contraction ([P2] section 5, npu_quant_matmul with both E8M0
+ * scales): qa [M,K] E4M3 + sa [M,K/32] E8M0 (from w8a8_mx_quant of the
+ * activations), qw [N,K] E4M3 + sw [N,K/32] (of the weights) ->
+ * y[m,n] = bf16( sum_g 2^(sa[m,g]-127) 2^(sw[n,g]-127) sum_{k in g} qa[m,k] qw[n,k] ),
+ * accumulated in binary32 (so within a bound of the exact sum, not bit-exact).
+ * K % 128 == 0; all pointers 16-byte aligned. */
+W8A8_API w8a8_status w8a8_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
+                                    const uint8_t* sw, int64_t N, uint16_t* y, w8a8_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* MoE expert FFN -- [P1] §三 runner chain: (quantise only if no per-token   */
 /* scale was supplied) -> W13 grouped matmul -> SwiGLU -> per-token INT8     */

@@ -84,7 +84,8 @@ def test_host_validation_rejects_before_launch(lib):
                                          fake, None) == 2  # I % 64 != 0
     assert lib.w8a8_prepack_weight(fake, 1, 130, 64, 1, ctypes.c_void_p(256), None) == 2  # gate/up needs I % 64 == 0
     assert lib.w8a8_prepack_weight(fake, 1, 128, 64, 8, ctypes.c_void_p(256), None) == 2  # unknown flag
-    # MXFP8: K % 32, negative M
+    # MXFP8: K % 32, negative M; contraction K % 128
+    assert lib.w8a8_mx_matmul(fake, fake, 4, 96, fake, fake, 8, fake, None) == 3
     assert lib.w8a8_mx_quant(fake, 4, 48, fake, fake, None) == 3
     assert lib.w8a8_mx_quant(fake, -1, 64, fake, fake, None) == 2
     # static W8A8: scale <= 0, offset out of int8, K % 16, missing quant_bias

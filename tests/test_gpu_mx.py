@@ -47,3 +47,35 @@ def test_mx_quant_every_finite_bf16_value():
 def test_mx_quant_dense_decode_input():
     d = S.dense_config(2)
     check(d.x)
+
+
+def mx_bound(qa, sa, qw, sw, y_ref):
+    """1 bf16 ulp of the exact result plus the binary32 accumulation: (32 + K/32) roundings of at most
+    2^-24 of the running magnitude, bounded by the sum of |terms|."""
+    dec = np.vectorize(oracle.e4m3_to_f32, otypes=[np.float32])
+    A = np.abs(dec(qa).astype(np.float64)) * np.repeat(2.0 ** (sa.astype(np.float64) - 127), 32, axis=1)
+    B = np.abs(dec(qw).astype(np.float64)) * np.repeat(2.0 ** (sw.astype(np.float64) - 127), 32, axis=1)
+    mag = A @ B.T
+    K = qa.shape[1]
+    ref = S.bf16_bits_to_f32(y_ref).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+    return ref, ulp + (32 + K // 32) * 2.0 ** -24 * mag
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (37, 200, 512), (128, 256, 1024), (300, 130, 384),
+                                   (64, 2048, 7168)])
+def test_mx_matmul_within_bound(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    xa = S.to_bf16_bits((rng.standard_normal((M, K)) * 2.0 ** rng.integers(-6, 6, (M, 1))).astype(np.float32))
+    xw = S.to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    qa, sa = oracle.mx_quant(xa)
+    qw, sw = oracle.mx_quant(xw)
+    from gpu_helpers import dev
+    y = W.w8a8_mx_matmul(dev(qa), dev(sa), dev(qw), dev(sw))
+    torch.cuda.synchronize()
+    got = S.bf16_bits_to_f32(y.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+    y_ref = oracle.mx_matmul(qa, sa, qw, sw)
+    ref, bound = mx_bound(qa, sa, qw, sw, y_ref)
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), f"max excess {np.max(err - bound)}"
+    assert np.mean(err == 0) > 0.9  # nearly all outputs are the exactly rounded ones

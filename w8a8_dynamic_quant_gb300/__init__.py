@@ -26,7 +26,7 @@ __all__ = [
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
     "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
     "w8a8_quantize_weight", "w8a8_quantize_prepack_weight", "w8a8_static_quant", "w8a8_static_prepare",
-    "w8a8_static_quant_matmul", "w8a8_mx_quant", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
+    "w8a8_static_quant_matmul", "w8a8_mx_quant", "w8a8_mx_matmul", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
     "moe_layer_workspace_offset", "moe_layer",
 ]
 
@@ -146,6 +146,24 @@ def w8a8_mx_quant(x: torch.Tensor, q: Optional[torch.Tensor] = None, scale: Opti
         _capi.check("w8a8_mx_quant", _capi.lib().w8a8_mx_quant(
             x.data_ptr(), M, K, q.data_ptr(), scale.data_ptr(), _stream(x.device)))
     return q, scale
+
+
+def w8a8_mx_matmul(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
+                   y: Optional[torch.Tensor] = None):
+    """MXFP8 contraction: E4M3 qa [M,K] + E8M0 sa [M,K/32], E4M3 qw [N,K] + E8M0 sw [N,K/32] -> bf16 y [M,N]."""
+    _need(qa, "qa", torch.uint8)
+    M, K = qa.shape
+    dev = qa.device
+    _need(sa, "sa", torch.uint8, (M, K // 32), dev)
+    _need(qw, "qw", torch.uint8, None, dev)
+    N = qw.shape[0]
+    _need(sw, "sw", torch.uint8, (N, K // 32), dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if y is None else y
+    _need(y, "y", torch.bfloat16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _capi.check("w8a8_mx_matmul", _capi.lib().w8a8_mx_matmul(
+            qa.data_ptr(), sa.data_ptr(), M, K, qw.data_ptr(), sw.data_ptr(), N, y.data_ptr(), _stream(dev)))
+    return y
 
 
 def w8a8_static_quant(x: torch.Tensor, input_scale: float, input_offset: int, q: Optional[torch.Tensor] = None):

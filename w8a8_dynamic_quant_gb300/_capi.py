@@ -27,6 +27,7 @@ SIGNATURES = {
     "w8a8_quantize_prepack_weight": (_int, [_vp, _i64, _i64, _i64, _u32, _vp, _vp, _vp]),
     "w8a8_dynamic_quant": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "w8a8_mx_quant": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "w8a8_mx_matmul": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp]),
     "w8a8_static_quant": (_int, [_vp, _i64, _i64, ctypes.c_float, ctypes.c_int32, _vp, _vp]),
     "w8a8_static_prepare": (_int, [_vp, _i64, _i64, _vp, ctypes.c_float, ctypes.c_int32, _vp, _vp, _vp, _vp]),
     "w8a8_static_quant_matmul": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),

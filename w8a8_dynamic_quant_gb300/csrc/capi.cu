@@ -463,6 +463,18 @@ w8a8_status w8a8_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, u
   return cuda_status(launch_mx_quant(x, M, K, q, scale, reinterpret_cast<cudaStream_t>(stream), sms));
 }
 
+w8a8_status w8a8_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
+                           const uint8_t* sw, int64_t N, uint16_t* y, w8a8_stream_t stream) {
+  if (M < 0 || M > INT32_MAX || N <= 0 || N > INT32_MAX || K <= 0 || K > W8A8_MAX_K) return W8A8_ERR_SHAPE;
+  if (K % 128 != 0) return W8A8_ERR_ALIGN;
+  if (M == 0) return W8A8_OK;
+  if (!qa || !sa || !qw || !sw || !y) return W8A8_ERR_NULL;
+  if (!aligned16(qa) || !aligned16(qw) || !aligned16(sa) || !aligned16(sw)) return W8A8_ERR_ALIGN;
+  int sms = 0;
+  if (w8a8_status s = device_info(sms)) return s;
+  return cuda_status(launch_mx_matmul(qa, sa, M, K, qw, sw, N, y, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static bool static_params_ok(float s, int32_t o) { return s > 0.0f && s < 3.0e38f && o >= -128 && o <= 127; }
 
 w8a8_status w8a8_static_quant(const uint16_t* x, int64_t M, int64_t K, float input_scale, int32_t input_offset,

@@ -58,6 +58,10 @@ cudaError_t launch_static_prepare(const int8_t* w, int64_t N, int64_t K, const f
 cudaError_t launch_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale, cudaStream_t stream,
                             int num_sms);
 
+// MXFP8 contraction (mx.cu): E4M3 a [M,K] + E8M0 [M,K/32], E4M3 w [N,K] + E8M0 [N,K/32] -> bf16 y [M,N].
+cudaError_t launch_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
+                             const uint8_t* sw, int64_t N, uint16_t* y, cudaStream_t stream);
+
 // Epilogue of the contraction.
 enum EpiMode : int {
   EPI_BF16 = 0,    // y[r,n] = bf16(((float)acc * sx[r]) * sw[e,n] (+ bias[n]))
