@@ -732,7 +732,8 @@ def run_reference(args):
     if args.prepare:
         wl = WeightPrep(args.workload, "cpu", host_only=True)
     elif S.CONFIGS[args.workload]["kind"] == "dense":
-        wl = _HostDenseStatic(args.workload) if args.static else _HostDense(args.workload)
+        wl = (_HostDenseStatic(args.workload) if args.static else
+              _HostDenseMX(args.workload) if args.mx else _HostDense(args.workload))
     else:
         wl = _HostMoETokens(args.workload) if args.from_tokens else _HostMoE(args.workload)
     for _ in range(args.warmup):
@@ -773,6 +774,13 @@ class _HostDenseStatic(DenseStatic):
         _HostDense.__init__(self, cfg_id)
         self.s_in, self.o_in = S.static_params(cfg_id)
         self.name = self.d.name + "_static"
+
+
+class _HostDenseMX(DenseMX):
+    def __init__(self, cfg_id):
+        _HostDense.__init__(self, cfg_id)
+        self.name = self.d.name + "_mxfp8"
+        self.step_rows = max(1, self.step_rows // 8)  # the float64 MX oracle is slower per row
 
 
 class _HostMoE(MoE):
