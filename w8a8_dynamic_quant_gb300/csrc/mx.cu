@@ -243,13 +243,10 @@ cudaError_t launch_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q,
 cudaError_t launch_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
                              const uint8_t* sw, int64_t N, uint16_t* y, cudaStream_t stream) {
   if (M == 0) return cudaSuccess;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(mx_matmul_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(MXM_SMEM));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // per device: set on every call, like the other engines
+  const cudaError_t e = cudaFuncSetAttribute(mx_matmul_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(MXM_SMEM));
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((N + MXM_BN - 1) / MXM_BN), static_cast<unsigned>((M + MXM_BM - 1) / MXM_BM));
   return launch_pdl(mx_matmul_kernel, grid, dim3(MXM_THREADS), MXM_SMEM, stream, qa, sa, static_cast<int>(M),
                     static_cast<int>(K), qw, sw, static_cast<int>(N), y);

@@ -489,14 +489,13 @@ __global__ void __launch_bounds__(kCbThreads) combine_kernel(const uint16_t* __r
   }
 }
 
-// CTAs of combine_kernel resident per SM (queried once).
+// CTAs of combine_kernel resident per SM (queried once; every device of the part is alike).  The
+// shared-memory attribute is set before each launch.
 int combine_per_sm() {
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kCbSmem)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel, kCbThreads, kCbSmem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel, kCbThreads, kCbSmem) != cudaSuccess ||
         n < 1) {
       cudaGetLastError();
       n = 1;
@@ -517,13 +516,9 @@ cudaError_t launch_route(const int64_t* topk_ids, int64_t n, int E, int32_t* cou
   while ((1 << nbits) < E) ++nbits;
   const size_t ssmem = small_smem(n, E);
   if (n <= kSmallMaxPairs && ssmem <= kSmallMaxSmem) {
-    static bool attr_set = false;
-    if (!attr_set) {
-      const cudaError_t ea = cudaFuncSetAttribute(route_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(kSmallMaxSmem));
-      if (ea != cudaSuccess) return ea;
-      attr_set = true;
-    }
+    const cudaError_t ea = cudaFuncSetAttribute(route_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(kSmallMaxSmem));
+    if (ea != cudaSuccess) return ea;
     return launch_pdl(route_small, dim3(1), dim3(kSmallThreads), ssmem, stream, topk_ids, n, E, nbits,
                       static_cast<int>(small_seg(n)), group_list, pos, status);
   }
@@ -552,6 +547,9 @@ cudaError_t launch_combine(const uint16_t* y_routed, const int32_t* pos, const f
   const int64_t nslice = (H + kCbCols - 1) / kCbCols;
   const int64_t items = T * nslice;
   if (items == 0) return cudaSuccess;
+  const cudaError_t ea = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(kCbSmem));
+  if (ea != cudaSuccess) return ea;
   const int64_t blocks = std::min<int64_t>(items, static_cast<int64_t>(num_sms) * combine_per_sm());
   return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCbThreads), kCbSmem, stream,
                     y_routed, pos, w, static_cast<int>(T), k, static_cast<int>(H), y, status);
