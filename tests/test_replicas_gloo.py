@@ -37,7 +37,7 @@ def test_aggregate_sums_units_and_takes_the_slowest_rank():
     world = 2
     units = [1000.0, 3000.0]
     seconds = [0.5, 2.0]
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:  # no fork of this (threaded) process
         out = mgr.dict()
         mp.spawn(_rank, args=(world, free_port(), units, seconds, out), nprocs=world, join=True)
         res = dict(out)
