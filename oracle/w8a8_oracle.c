@@ -15,13 +15,18 @@
  *              npu_quant_matmul(q, W, weight_scale, pertoken_scale, bias,
  *              output_dtype=bf16) -> BF16 [M,N])
  *        §三  (MoE: npu_grouped_matmul over group_list = rows per expert;
- *              Routed Hidden -> W13 GMM -> SwiGLU -> Requant -> W2 GMM -> BF16;
- *              "if pertoken_scale is None: quantise", i.e. no double quant)
+ *              routed rows -> W13 grouped matmul -> SwiGLU -> requant -> W2
+ *              grouped matmul -> BF16; an input that already carries a
+ *              per-token scale is not quantised again)
  *        §四  (Atlas A3 operator contract: INT8 x1, INT8 x2, FLOAT32 per-token
  *              scale, BF16 output)
+ *   [P2] "Qwen3.8-FP8 on Ascend 950: Why Weights Become MXFP8 at Load Time",
+ *        sections 3 (re-quantisation to MXFP8) and 5 (MXFP8 activations and
+ *        weights in the quantized matmul).
  *   [P3] "超大 MoE 的低比特推理：INT4、FP4 与量化感知训练", section
- *        "为什么要量化感知训练" (fake_int4: scale = group absmax / qmax, then
- *        divide, round half-to-even, clamp).
+ *        on why quantisation-aware training is needed (its fake-quant
+ *        helper takes the group absmax over qmax as the scale, divides by
+ *        it, rounds half to even and clamps).
  *
  * Arithmetic (readings where the pages are silent are marked READING):
  *   quant    amax = max_k |x|, s = amax / 127 (binary32 divide),
@@ -43,7 +48,12 @@
  *   skip     a non-NULL x_scale means x is already INT8 + per-token scale and
  *            is not quantised again.
  *   route / permute / combine (token rows in, token rows out): see the
- *            readings above oracle_moe_route at the end of this file.
+ *            readings above oracle_moe_route.
+ *   per-channel weight quantisation from BF16: above oracle_quantize_weight.
+ *   static W8A8 (fixed input scale and offset, deq_scale, quant_bias):
+ *            above oracle_static_quant.
+ *   MXFP8 (E4M3 + one E8M0 scale per 32 along K, [P2] sections 3 and 5):
+ *            above oracle_e4m3_from_f32.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared
  * (contraction off: no hidden FMA may change a rounding).
