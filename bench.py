@@ -1,19 +1,23 @@
 #!/usr/bin/env python3
 """Benchmark of the W8A8_DYNAMIC hot path on GB300 (one JSON line on stdout).
 
-Default workload: the dense decode linear X BF16 [64,7168] x W INT8
-[2048,7168] (per-channel scales, no bias); one step = dynamic per-token quant
-+ INT8 GEMM with the fused dequant epilogue.  `--workload N` selects one of
-the five workloads (1 tiny dense, 2 dense decode, 3 dense prefill, 4 MoE
-prefill, 5 MoE decode with pre-quantised input).
+Default workload: the MoE prefill layer, T=4096 tokens, H=4096, I=2048,
+E=64 experts, top-8 routing with Zipf(1.1) popularity (R = 32768 routed rows,
+4 experts empty); one step = per-token INT8 quant of the routed BF16 rows ->
+W13 grouped GEMM with SwiGLU fused into its epilogue -> per-token INT8
+requant -> W2 grouped GEMM -> BF16.  `--workload N` selects one of the five
+workloads (1 tiny dense, 2 dense decode, 3 dense prefill, 4 MoE prefill,
+5 MoE decode with pre-quantised input).
 
 Timing: W warm-up steps, then exactly K steps between a barrier +
 synchronize on both sides.  The step (every kernel of the path, in order, on
-one input set) is captured into a CUDA graph over rotating input sets whose
+one input set) is captured into CUDA graphs over rotating input sets whose
 total size exceeds the 129 MB L2 (or a single set when one set already
-exceeds it) and timed with CUDA events on the stream it runs on; kernels of a
-step may overlap where the library lets them (the decode contraction starts
-its weight stream while the quantisation still runs).  Each kernel type is
+exceeds it): one graph of a step on each set and one of a whole rotation, so
+that exactly W and K steps run; the K steps are timed with CUDA events on
+the stream they run on.  Kernels of a step may overlap where the library
+lets them (the decode contraction starts its weight stream while the
+quantisation still runs).  Each kernel type is
 also captured on its own over the same sets for the per-kernel breakdown and
 the roofline of the dominant kernel.  The
 `e2e` leg runs the same step through the public Python API with the inputs
@@ -177,7 +181,7 @@ def aggregate(units: float, seconds: float, group=None):
 class Dense:
     """Dense W8A8_DYNAMIC linear: quant + quantised matmul."""
 
-    def __init__(self, cfg_id: int, device):
+    def __init__(self, cfg_id: int, device, pack: str = "auto"):
         import torch
         import w8a8_dynamic_quant_gb300 as W
         from w8a8_dynamic_quant_gb300 import synthetic as S
@@ -187,13 +191,16 @@ class Dense:
         self.name = d.name
         M, N, K = d.M, d.N, d.K
         self.M, self.N, self.K = M, N, K
-        set_bytes = 2 * M * K + M * K + N * K * (3 if M >= 128 else 1) + 2 * M * N
+        if pack == "auto":
+            pack = "i8+f16" if M >= 128 else "i8"
+        self.pack = pack
+        set_bytes = 2 * M * K + M * K + N * K * (3 if pack == "i8+f16" else 1) + 2 * M * N
         self.n_sets = max(1, -(-int(1.2 * L2_BYTES) // set_bytes))
         self.n_sets = min(self.n_sets, 16)
         xd = torch.from_numpy(d.x.view("int16")).to(device).view(torch.bfloat16)
         wd = torch.from_numpy(d.w).to(device)
-        # large M runs on the tcgen05 engine, which reads the fp16 copy of the weight
-        self.pack_flags = W.PACK_F16 if M >= 128 else 0
+        # large M runs on a tcgen05 engine: on the fp16 copy of the weight when the pack holds it
+        self.pack_flags = W.PACK_F16 if pack == "i8+f16" else 0
         sw = torch.from_numpy(d.w_scale).to(device)
         bias = None if d.bias is None else torch.from_numpy(d.bias.view("int16")).to(device).view(torch.bfloat16)
         self.sets = []
@@ -227,6 +234,7 @@ class Dense:
 
     def config(self):
         return {"workload": self.name, "M": self.M, "N": self.N, "K": self.K, "bias": self.d.bias is not None,
+                "packed_weights": {"i8": "int8 only", "i8+f16": "int8 + integer-valued fp16 copy"}[self.pack],
                 "seed": 0, "inputs": self.input_note}
 
     def value(self, units, seconds):
@@ -361,7 +369,7 @@ class DenseMX(Dense):
 class MoE:
     """MoE expert FFN: (quant) -> W13 grouped GEMM + SwiGLU -> requant -> W2 grouped GEMM."""
 
-    def __init__(self, cfg_id: int, device, pack_weights: bool = True):
+    def __init__(self, cfg_id: int, device, pack_weights: bool = True, pack: str = "auto"):
         import numpy as np
         import torch
         import w8a8_dynamic_quant_gb300 as W
@@ -371,7 +379,12 @@ class MoE:
         self.m = m
         self.name = m.name
         self.n_sets = 1
-        f16 = W.PACK_F16 if m.R >= 64 * m.E else 0  # prefill-sized groups: tcgen05 engine
+        # prefill-sized groups run on a tcgen05 engine: with the packed FP16 weight copy ("i8+f16") or
+        # on the INT8 payload widened in tensor memory ("i8")
+        if pack == "auto":
+            pack = "i8+f16" if m.R >= 64 * m.E else "i8"
+        f16 = W.PACK_F16 if pack == "i8+f16" else 0
+        self.pack = pack
         self.w13p = W.w8a8_prepack_weight(m.w13, W.PACK_GATE_UP | f16) if pack_weights else None
         self.w2p = W.w8a8_prepack_weight(m.w2, f16) if pack_weights else None
         self.gl = torch.from_numpy(m.group_list).to(device)
@@ -408,6 +421,7 @@ class MoE:
         m = self.m
         return {"workload": self.name, "T": m.T, "R": m.R, "H": m.H, "I": m.I, "E": m.E, "topk": m.topk,
                 "active_experts": int((m.group_list > 0).sum()), "prequantised_input": m.x_scale is not None,
+                "packed_weights": {"i8": "int8 only", "i8+f16": "int8 + integer-valued fp16 copy"}[self.pack],
                 "seed": 0, "inputs": self.input_note}
 
     def value(self, units, seconds):
@@ -474,9 +488,9 @@ class MoETokens(MoE):
     top-k weighted combine (one moe_layer call).  The permute and the combine are also timed alone,
     through their own calls, for their HBM rooflines."""
 
-    def __init__(self, cfg_id: int, device, kernels=None):
+    def __init__(self, cfg_id: int, device, kernels=None, pack: str = "auto"):
         # the routing kernels alone (profiling) need no packed weights
-        super().__init__(cfg_id, device, pack_weights=kernels is None or "moe_layer" in kernels)
+        super().__init__(cfg_id, device, pack_weights=kernels is None or "moe_layer" in kernels, pack=pack)
         W, torch, m = self.W, self.torch, self.m
         T, k, H, I, E, R = m.T, m.topk, m.H, m.I, m.E, m.R
         self.name = m.name + "_from_tokens"
@@ -684,15 +698,16 @@ class WeightPrep:
         return self.channels
 
 
-def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False, static=False, mx=False):
+def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False, static=False, mx=False,
+                  pack="auto"):
     from w8a8_dynamic_quant_gb300 import synthetic as S
     if prepare:
         return WeightPrep(cfg_id, device)
     if mx:
         return DenseMX(cfg_id, device)
     if S.CONFIGS[cfg_id]["kind"] == "dense":
-        return DenseStatic(cfg_id, device) if static else Dense(cfg_id, device)
-    return MoETokens(cfg_id, device, kernels) if from_tokens else MoE(cfg_id, device)
+        return DenseStatic(cfg_id, device) if static else Dense(cfg_id, device, pack)
+    return MoETokens(cfg_id, device, kernels, pack) if from_tokens else MoE(cfg_id, device, pack=pack)
 
 
 # -------------------------------------------------------------- the arms --
@@ -762,6 +777,7 @@ class _HostDense(Dense):
         self.d = S.dense_config(cfg_id)
         self.name = self.d.name
         self.M, self.N, self.K = self.d.M, self.d.N, self.d.K
+        self.pack = "i8+f16" if self.M >= 128 else "i8"  # the GPU arm's default layout, named in config
         self.unit = "TOPS"
         self.input_note = "host arrays (CPU oracle)"
         # about 0.1-0.5 s of CPU per step on 16 cores
@@ -791,6 +807,7 @@ class _HostMoE(MoE):
         self.np, self.torch = np, torch
         self.m = S.moe_config(cfg_id, device="cpu")
         self.name = self.m.name
+        self.pack = "i8+f16" if self.m.R >= 64 * self.m.E else "i8"  # the GPU arm's default layout
         self.unit = "tokens/s"
         self.input_note = "host arrays (CPU oracle)"
         self.step_rows = 8
@@ -804,6 +821,7 @@ class _HostMoETokens(MoETokens):
         self.np, self.torch = np, torch
         self.m = S.moe_config(cfg_id, device="cpu")
         self.name = self.m.name + "_from_tokens"
+        self.pack = "i8+f16" if self.m.R >= 64 * self.m.E else "i8"  # the GPU arm's default layout
         self.unit = "tokens/s"
         self.input_note = "host arrays (CPU oracle)"
         self.step_rows = 1  # tokens (each with topk routed rows)
@@ -822,7 +840,8 @@ def run_gpu(args):
     __graft_entry__.build()
     peaks = load_peaks()
     kernels = args.kernels.split(",") if args.kernels else None
-    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare, args.static, args.mx)
+    wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare, args.static, args.mx,
+                       args.pack)
     step_kernels = getattr(wl, "step_kernels", wl.kernels)
     stream = torch.cuda.current_stream(device)
 
@@ -846,28 +865,40 @@ def run_gpu(args):
                 for i in range(wl.n_sets):
                     wl.launch(k, i)
         graphs[k] = g
+    # a whole rotation over the input sets in one graph, and one graph per set for a single step
     step_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(step_graph):
         for i in range(wl.n_sets):
             for k in step_kernels:
                 wl.launch(k, i)
+    one_graphs = []
+    if wl.n_sets > 1:
+        for i in range(wl.n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for k in step_kernels:
+                    wl.launch(k, i)
+            one_graphs.append(g)
     torch.cuda.synchronize()
 
-    rounds_w = max(1, -(-args.warmup // wl.n_sets))
-    for _ in range(rounds_w):
-        step_graph.replay()
-    rounds = max(1, -(-args.steps // wl.n_sets))
-    steps = rounds * wl.n_sets
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(rounds + 1)]
+    def run_steps(n):
+        """Exactly n steps: whole rotations, then single steps on the next sets."""
+        for _ in range(n // wl.n_sets):
+            step_graph.replay()
+        for i in range(n % wl.n_sets):
+            one_graphs[i].replay()
+
+    run_steps(args.warmup)
+    steps = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         t_wall0 = time.perf_counter()
-        ev[0].record(stream)
-        for r in range(rounds):
-            step_graph.replay()
-            ev[r + 1].record(stream)
+        ev0.record(stream)
+        run_steps(steps)
+        ev1.record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
         # keep the GPU loaded long enough for the clock sampler to see it
@@ -879,7 +910,8 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clocks = clk.summary()
-    step_ms = sum(ev[r].elapsed_time(ev[r + 1]) for r in range(rounds)) / steps
+    step_ms = ev0.elapsed_time(ev1) / steps
+    rounds = max(1, -(-steps // wl.n_sets))
 
     # per-kernel breakdown: each kernel type alone over the same sets (outside the timed region)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(wl.kernels) + 1)] for _ in range(rounds)]
@@ -936,7 +968,7 @@ def run_gpu(args):
                                                 "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
 
     line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": steps,
-            "warmup": rounds_w * wl.n_sets, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": wl.config(),
             "roofline": roofline, "clocks": clocks, "gpu_launches": steps * wl.launches_per_step,
             "e2e": {"value": wl.value(e_units, e_seconds), "unit": wl.unit, "h2d_bytes_per_step": wl.h2d,
@@ -958,7 +990,10 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--pack", default="auto", choices=["auto", "i8", "i8+f16"],
+                    help="packed weight layout: INT8 only, or INT8 plus the integer-valued FP16 copy the fastest "
+                         "large-M engines read (auto: the copy for prefill-sized shapes)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")

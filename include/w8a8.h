@@ -351,12 +351,21 @@ W8A8_API int64_t moe_layer_workspace_offset(int64_t T, int64_t k, int64_t H, int
  * scratch lives in a fixed 8 MiB device array inside the library (held by every
  * GPU that loads it until exit); problems that need more (roughly M*N > 2M)
  * return W8A8_ERR_WORKSPACE before any launch.  The first call on a device
- * looks up the array's address and should come before any stream capture.
- * All calls share the array: calls that overlap on the GPU race.  Allocates
- * nothing. */
+ * looks up the array's address, clears its status word, and should come
+ * before any stream capture.  All calls share the array: calls that overlap
+ * on the GPU race.  Errors found on the device go to the array's status
+ * word (the first one stays); read them with
+ * w8a8_quant_matmul_noalloc_status().  Allocates nothing. */
 W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const float* x_scale, int64_t M, int64_t K,
                                                const void* w_packed, const float* w_scale, int64_t N,
                                                const uint16_t* bias, uint16_t* y, w8a8_stream_t stream);
+
+/* Synchronises `stream`, returns the status word that w8a8_quant_matmul_noalloc
+ * calls on the current device wrote (W8A8_OK if none, else the first device
+ * error since the last read, e.g. W8A8_ERR_PACKED for a packed weight whose
+ * header does not match the call) and clears it.  Copies through the array's
+ * symbol into a host local: allocates nothing. */
+W8A8_API w8a8_status w8a8_quant_matmul_noalloc_status(w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Device status                                                             */
@@ -366,6 +375,17 @@ W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const float* x_s
  * workspace `ws` (W8A8_OK if none) and clears it.  `ws` is any workspace
  * passed to the calls above. */
 W8A8_API w8a8_status w8a8_read_device_status(void* ws, w8a8_stream_t stream);
+
+/* Self-check of the device-side failure path (the failure table at the end
+ * of [P2], "Where It Breaks or Falls Back": a condition the operation cannot
+ * meet comes back as an error code, not a crash).  Launches one CTA that waits
+ * on an mbarrier nobody arrives on, with the bounded-wait helper of the
+ * tensor-core kernels and a limit of `limit_us` microseconds (1 .. 2,000,000).
+ * When the wait gives up the kernel writes W8A8_ERR_DEVICE_TIMEOUT to the status
+ * word of `ws` (a zero-filled workspace of at least W8A8_STATUS_BYTES) and
+ * returns; nothing else is in flight, so the context stays usable.  Read the
+ * outcome with w8a8_read_device_status(). */
+W8A8_API w8a8_status w8a8_selftest_bounded_wait(void* ws, uint32_t limit_us, w8a8_stream_t stream);
 
 /* Engines a contraction can run on. */
 enum {

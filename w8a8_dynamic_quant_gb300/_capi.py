@@ -49,7 +49,9 @@ SIGNATURES = {
                          _vp]),
     "moe_layer_workspace_offset": (_i64, [_i64, _i64, _i64, _i64, _i64, _int]),
     "w8a8_quant_matmul_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _vp]),
+    "w8a8_quant_matmul_noalloc_status": (_int, [_vp]),
     "w8a8_read_device_status": (_int, [_vp, _vp]),
+    "w8a8_selftest_bounded_wait": (_int, [_vp, _u32, _vp]),
     "w8a8_last_engine": (_int, []),
 }
 
@@ -57,6 +59,7 @@ STATUS = {0: "W8A8_OK", 1: "W8A8_ERR_NULL", 2: "W8A8_ERR_SHAPE", 3: "W8A8_ERR_AL
           4: "W8A8_ERR_WORKSPACE", 5: "W8A8_ERR_GROUP_LIST", 6: "W8A8_ERR_DEVICE_TIMEOUT",
           7: "W8A8_ERR_CUDA", 8: "W8A8_ERR_UNSUPPORTED", 9: "W8A8_ERR_PACKED", 10: "W8A8_ERR_TOPK_IDS"}
 STATUS_BYTES = 256
+W8A8_OK, W8A8_ERR_WORKSPACE, W8A8_ERR_DEVICE_TIMEOUT, W8A8_ERR_PACKED = 0, 4, 6, 9
 PACK_GATE_UP = 1
 PACK_F16 = 2
 

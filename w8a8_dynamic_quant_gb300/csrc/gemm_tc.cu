@@ -21,16 +21,15 @@
 // activation rows x 64 K, B = 256 weight rows x 64 K (48 KB per stage).  One
 // elected thread issues tcgen05.mma M=128 N=256 K=16 four times per stage.
 //
-// Clusters of two CTAs.  The CTAs of a cluster work on neighbouring tiles
-// that share one operand and fetch that operand once for both: each loads
-// half of it and multicasts the half into the same stage of both CTAs.  For
-// m-blocks 2p and 2p+1 of an expert at one n-block the shared operand is the
-// 256-row weight block; an expert with an odd number of m-blocks leaves its
-// last m-block, and for it the pair takes n-blocks 2j and 2j+1 and shares
-// the 128-row activation block.  Either way each SM requests 256 rows of 128
-// bytes per stage instead of 384.  A stage is free again only when both
-// CTAs' MMAs are done with it, so each MMA commit arrives on the empty
-// barrier of both CTAs (count 2).
+// Clusters of two CTAs.  The CTAs of a cluster are scheduled together and
+// work on neighbouring tiles that share one operand: for m-blocks 2p and
+// 2p+1 of an expert at one n-block the shared operand is the 256-row weight
+// block; an expert with an odd number of m-blocks leaves its last m-block,
+// and for it the pair takes n-blocks 2j and 2j+1 and shares the 128-row
+// activation block.  Each CTA loads its whole stage itself with plain tensor
+// copies; the copy of the shared operand that lands second is served from L2,
+// because both CTAs request it at about the same time.  The CTAs exchange
+// nothing: each stage is freed by its own CTA's MMA commit.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over output tiles):
 //   warp 0     TMA producer
@@ -72,7 +71,6 @@ __device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f
 
 struct TileInfo {
   int e, mb, nb, cnt;
-  int share_a;   // 0: the pair shares the weight block, 1: it shares the activation block
   int64_t row0;  // first global row of the tile (into the [R,K] activation matrix)
 };
 
@@ -102,11 +100,9 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int*
     const int g = local / (mpairs * TC_GROUP_N);
     const int rem = local - g * mpairs * TC_GROUP_N;
     const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
-    ti.share_a = 0;
     ti.mb = 2 * (rem / gn) + rank;
     ti.nb = g * TC_GROUP_N + rem % gn;
   } else {
-    ti.share_a = 1;
     ti.mb = mblocks - 1;
     ti.nb = 2 * (local - mpairs * NB) + rank;
   }
@@ -298,7 +294,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       s_bad = W8A8_ERR_PACKED;
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), TC_CLUSTER);  // one commit from each CTA's MMA
+      mbar_init(smem_u32(&bar_empty[s]), 1);  // this CTA's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_accf[b]), 1);
@@ -319,7 +315,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   int tiles_total;
   const int rows_total = scan_groups<TC_THREADS, kMaxE>(
       a, E, [NB](int c) { return pair_units(c, NB); }, s_row_off, s_tile_prefix, s_warp, &s_bad, &tiles_total);
-  // Both CTAs' barriers are initialised before either sends the other a copy or an arrival.
   tc_fence_before();
   cluster_sync_all();
   tc_fence_after();
@@ -341,28 +336,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
           const uint32_t full = smem_u32(&bar_full[stage]);
-          mbar_expect_tx(full, TC_STAGE_BYTES);  // own loads plus the peer's multicast half
+          mbar_expect_tx(full, TC_STAGE_BYTES);
           const uint32_t sa = stage_base + stage * TC_STAGE_BYTES;
           const int x = kb * TC_BK;
-          if (ti.share_a) {
-            tma_load_2d_mc(sa + rank * (TC_A_BYTES / 2), &tmA, x, ya + static_cast<int>(rank) * (TC_BM / 2), full,
-                           TC_PAIR_MASK);
-            tma_load_2d(sa + TC_A_BYTES, &tmB, x, yb, full);
-            tma_load_2d(sa + TC_A_BYTES + TC_B_BYTES / 2, &tmB, x, yb + TC_BN / 2, full);
-          } else {
-            tma_load_2d(sa, &tmA, x, ya, full);
-            tma_load_2d(sa + TC_A_BYTES / 2, &tmA, x, ya + TC_BM / 2, full);
-            tma_load_2d_mc(sa + TC_A_BYTES + rank * (TC_B_BYTES / 2), &tmB, x, yb + static_cast<int>(rank) * (TC_BN / 2),
-                           full, TC_PAIR_MASK);
-          }
+          tma_load_2d(sa, &tmA, x, ya, full);
+          tma_load_2d(sa + TC_A_BYTES, &tmB, x, yb, full);
           if (++stage == TC_STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Drain: every stage's last fill has been consumed by both CTAs, so no copy into either CTA and no
-      // arrival on this CTA's barriers is still in flight when the cluster leaves.
+      // Drain: every stage's last fill has been consumed, so no copy into this CTA is still in flight
+      // when it leaves.
       for (int i = 0; i < TC_STAGES && !s_abort; ++i) {
         if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 5u)) break;
         if (++stage == TC_STAGES) {
@@ -401,7 +387,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc,
                      (kb > c * TC_KB_PER_CHUNK || k > 0) ? 1u : 0u);
             }
-            tc_commit_mc(smem_u32(&bar_empty[stage]), TC_PAIR_MASK);  // frees the stage in both CTAs
+            tc_commit(smem_u32(&bar_empty[stage]));  // frees the stage
             if (++stage == TC_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -473,7 +459,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     while (globaltimer_ns() - t0 < 20000000ull) {
     }
   }
-  cluster_sync_all();  // neither CTA leaves while the other may still write into it
+  cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -792,9 +778,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f
     if (a.mode == EPI_ACC) return launch_tc_mode<EPI_ACC, true>(ma, mb, a, grid, smem, stream);
     return launch_tc_mode<EPI_BF16, true>(ma, mb, a, grid, smem, stream);
   }
-  // Half-tile boxes: one operand of a tile pair is fetched as two halves, one by each CTA.
-  if (!make_map(&ma, a_f16, a.R, a.K, TC_BM / 2)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b_f16, a.E * a.N, a.K, TC_BN / 2)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, a_f16, a.R, a.K, TC_BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, b_f16, a.E * a.N, a.K, TC_BN)) return cudaErrorInvalidValue;
   const int64_t units = tc_upper_units(a.E, a.R, a.N, a.group_list != nullptr);
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / TC_CLUSTER));
   const int grid = static_cast<int>(clusters * TC_CLUSTER);

@@ -22,10 +22,10 @@
 // 1024-deep chunk.  Shared memory: four stages of a 128-token x 128-K FP16
 // activation tile (two 64-K sub-tiles, 128-byte swizzle) and a 128-row x
 // 128-byte INT8 weight tile (128-byte swizzle), brought in by TMA.  The two
-// CTAs of a cluster take weight blocks 2p and 2p+1 of the same tokens and
-// fetch the activation tile once: each loads half of its rows and multicasts
-// them into both CTAs, so a stage is free again only when both CTAs' MMAs are
-// done with it (their commits arrive on both CTAs' empty barriers).
+// CTAs of a cluster are scheduled together and take weight blocks 2p and 2p+1
+// of the same tokens; each loads the activation tile itself with plain tensor
+// copies (the second request is served from L2) and the CTAs exchange
+// nothing, so each stage is freed by its own CTA's MMA commit.
 //
 // Warp roles (448 threads, one CTA per SM, persistent over tiles):
 //   warp 0       TMA producer
@@ -67,7 +67,6 @@ static_assert(W_BK == 128, "a stage is one 128-byte weight row and two 64-K acti
 constexpr uint32_t W_TMEM_COLS = 512;
 constexpr int W_GROUP_N = 16;  // n-blocks per rasterisation group (8 pairs)
 constexpr int W_CLUSTER = 2;
-constexpr uint16_t W_PAIR_MASK = 0x3;
 constexpr int kMaxE = 1024;
 constexpr uint32_t W_UP_BYTES = 2 * 2 * 64 * 32 * 2;  // up values: [gate warp pair][half][64 tokens][32 lanes] bf16
 // kind::f16 instruction descriptor: D = F32, A = B = F16, both K-major, N = 128, M = 128.
@@ -160,7 +159,7 @@ tcw_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     for (int s = 0; s < W_STAGES; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
       mbar_init(smem_u32(&bar_conv[s]), W_CONV_WARPS);
-      mbar_init(smem_u32(&bar_empty[s]), W_CLUSTER);  // both CTAs' MMAs (the peer's copy lands here too)
+      mbar_init(smem_u32(&bar_empty[s]), 1);  // this CTA's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_accf[b]), 1);
@@ -186,7 +185,7 @@ tcw_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
       a, E, [NB](int c) { return ((c + W_BT - 1) / W_BT) * ((NB + 1) / 2); }, s_row_off, s_unit_prefix, s_warp, &s_bad,
       &units_total);
   tc_fence_before();
-  cluster_sync_all();  // both CTAs' barriers exist before either sends the other a copy or an arrival
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   int bad = s_bad;
@@ -208,11 +207,9 @@ tcw_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
           const uint32_t full = smem_u32(&bar_full[stage]);
           mbar_expect_tx(full, W_STAGE_BYTES);
           const uint32_t sa = stage_base + stage * W_STAGE_BYTES;
-          // this CTA's half of the token rows, multicast into both CTAs; its own weight rows
-          const uint32_t xo = rank * (W_X_SUB / 2);
-          const int yxh = yx + static_cast<int>(rank) * (W_BT / 2);
-          tma_load_2d_mc(sa + xo, &tmX, kb * W_BK, yxh, full, W_PAIR_MASK);
-          tma_load_2d_mc(sa + W_X_SUB + xo, &tmX, kb * W_BK + 64, yxh, full, W_PAIR_MASK);
+          // the tile's token rows (two 64-K sub-tiles) and its weight rows
+          tma_load_2d(sa, &tmX, kb * W_BK, yx, full);
+          tma_load_2d(sa + W_X_SUB, &tmX, kb * W_BK + 64, yx, full);
           tma_load_2d(sa + W_X_BYTES, &tmW, kb * W_BK, yw, full);
           if (++stage == W_STAGES) {
             stage = 0;
@@ -220,8 +217,8 @@ tcw_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
           }
         }
       }
-      // Drain: every stage's last fill has been consumed by both CTAs, so no copy into either CTA and no
-      // arrival on this CTA's barriers is still in flight when the cluster leaves.
+      // Drain: every stage's last fill has been consumed, so no copy into this CTA is still in flight
+      // when it leaves.
       for (int i = 0; i < W_STAGES && !s_abort; ++i) {
         if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 5u)) break;
         if (++stage == W_STAGES) {
@@ -257,7 +254,7 @@ tcw_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
               tc_mma_tmem_a(d_tmem, tmem_base + stage * W_A_COLS + 8u * k,
                             smem_desc_sw128(sx + (k >> 2) * W_X_SUB) + 2u * (k & 3), kIdescW,
                             (kb > c * W_KB_PER_CHUNK || k > 0) ? 1u : 0u);
-            tc_commit_mc(smem_u32(&bar_empty[stage]), W_PAIR_MASK);  // frees the stage in both CTAs
+            tc_commit(smem_u32(&bar_empty[stage]));  // frees the stage
             if (++stage == W_STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -424,7 +421,7 @@ tcw_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     while (globaltimer_ns() - t0 < 20000000ull) {
     }
   }
-  cluster_sync_all();  // neither CTA leaves while the other may still write into it
+  cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -450,7 +447,7 @@ cudaError_t launch_tcw_gemm(const GemmArgs& a, const void* a_f16, int num_sms, c
   // fp16 activations [R, K] and the int8 weight payload [E*N, K]; rows past the ends read as zero
   CUtensorMap mx, mw;
   const uint8_t* w_i8 = static_cast<const uint8_t*>(a.packed) + pack_layout(a.E, a.N, a.K, 0).i8_offset;
-  if (!encode_map_2d(&mx, a_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.R, a.K, 64, W_BT / 2,
+  if (!encode_map_2d(&mx, a_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.R, a.K, 64, W_BT,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map_2d(&mw, w_i8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.E * a.N, a.K, W_BK, W_BN,
                      CU_TENSOR_MAP_SWIZZLE_128B))

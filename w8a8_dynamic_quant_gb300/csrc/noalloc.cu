@@ -16,12 +16,16 @@
 //     fit (roughly M * N > 2 million) are rejected with W8A8_ERR_WORKSPACE
 //     before anything is launched;
 //   - the first call on a device looks up the array's device address
-//     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture;
+//     (cudaGetSymbolAddress) with that device current and clears the status
+//     word; make that first call before any stream capture;
 //   - all calls share the one array and it keeps the last call's contents:
-//     each call zeroes the status word and the arrival counters on its stream
-//     first, and the partial sums are zero again after every call; calls that
-//     overlap on the GPU (different streams, no ordering) race on the array;
+//     each call zeroes the arrival counters on its stream first, and the
+//     partial sums are zero again after every call; calls that overlap on
+//     the GPU (different streams, no ordering) race on the array;
+//   - errors found on the device (a packed header that does not match the
+//     call, an exhausted bounded wait) go to the array's status word, where
+//     the first one stays until w8a8_quant_matmul_noalloc_status() reads and
+//     clears it -- the same contract as a workspace's status word;
 //   - nothing here allocates: no cudaMalloc, cudaFree or allocating library
 //     routine is called.
 #include <mutex>
@@ -37,7 +41,8 @@ constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the array on the current device (looked up once per device).
+// Device address of the array on the current device (looked up once per device, when the status word
+// is also cleared).
 w8a8_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W8A8_ERR_CUDA;
@@ -45,6 +50,7 @@ w8a8_status scratch_address(void** out) {
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return W8A8_ERR_CUDA;
+    if (cudaMemset(p, 0, w8a8::kStatusBytes) != cudaSuccess) return W8A8_ERR_CUDA;
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -87,9 +93,8 @@ extern "C" W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const
   if (w8a8_status s = scratch_address(&base)) return s;
   uint8_t* b = static_cast<uint8_t*>(base);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // what must start at zero: the status word and the arrival counters
-  if (cudaMemsetAsync(b, 0, kStatusBytes, st) != cudaSuccess ||
-      cudaMemsetAsync(b + count_off, 0, static_cast<size_t>(count_len) * 4, st) != cudaSuccess)
+  // what must start at zero: the arrival counters (the status word keeps the first error until it is read)
+  if (cudaMemsetAsync(b + count_off, 0, static_cast<size_t>(count_len) * 4, st) != cudaSuccess)
     return W8A8_ERR_CUDA;
 
   GemmArgs a;
@@ -112,4 +117,17 @@ extern "C" W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const
   a.ws_count_len = count_len;
   const GemmPlan p = plan_reg_gemm(a, sms);
   return launch_reg_gemm(a, p, st) == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
+}
+
+extern "C" W8A8_API w8a8_status w8a8_quant_matmul_noalloc_status(w8a8_stream_t stream) {
+  void* base = nullptr;
+  if (w8a8_status s = scratch_address(&base)) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return W8A8_ERR_CUDA;
+  DeviceStatus s;
+  if (cudaMemcpyFromSymbol(&s, g_noalloc_scratch, sizeof(s)) != cudaSuccess) return W8A8_ERR_CUDA;
+  if (s.code != 0u) {
+    const DeviceStatus zero = {};
+    if (cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(zero)) != cudaSuccess) return W8A8_ERR_CUDA;
+  }
+  return static_cast<w8a8_status>(s.code);
 }

@@ -40,13 +40,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // when the CTA is aborting (this wait gave up, or another one did).  The
 // first probe is inline; only a phase still open calls the polling loop.
+// limit_ns: how long the wait may take (the kernels use kWaitLimitNs).
 static __device__ __noinline__ bool mbar_wait_poll(uint32_t a, uint32_t parity, volatile int* abort_flag,
-                                                   DeviceStatus* st, uint32_t where) {
+                                                   DeviceStatus* st, uint32_t where,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       set_status(st, W8A8_ERR_DEVICE_TIMEOUT, where);
       return false;
@@ -54,24 +56,14 @@ static __device__ __noinline__ bool mbar_wait_poll(uint32_t a, uint32_t parity, 
   }
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, volatile int* abort_flag, DeviceStatus* st,
-                                          uint32_t where) {
-  return mbar_try_wait(a, parity) || mbar_wait_poll(a, parity, abort_flag, st, where);
+                                          uint32_t where, uint64_t limit_ns = kWaitLimitNs) {
+  return mbar_try_wait(a, parity) || mbar_wait_poll(a, parity, abort_flag, st, where, limit_ns);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
-      : "memory");
-}
-// The same box into the same shared-memory offset of every CTA in `mask` (this cluster); each
-// destination's mbarrier at offset `mbar` receives the bytes that land in that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -102,12 +94,6 @@ __device__ __forceinline__ void tc_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
 }
 
-// As tc_commit, but the arrival goes to the mbarrier at offset `mbar` in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t mbar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(mbar), "h"(mask)
-               : "memory");
-}
 // Address, in the cluster window, of the same shared-memory offset in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t smem_cluster_addr(uint32_t addr, uint32_t rank) {
   uint32_t r;
