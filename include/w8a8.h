@@ -94,11 +94,10 @@ W8A8_API int w8a8_version(void);
 #define W8A8_PACK_GATE_UP 1u /* W13 [E,2I,K]: interleave gate rows [0,I) and up rows [I,2I)
                                 in blocks of 64 so one tile holds matching gate/up channels;
                                 requires N even and (N/2) % 64 == 0 */
-#define W8A8_PACK_F16 2u     /* also store an integer-valued FP16 copy of the weights: the
-                                operand the tensor-core engines read for large M (dense needs
-                                it for that engine; grouped calls without it widen the INT8
-                                weights in tensor memory instead, slower, a third of the
-                                memory) */
+#define W8A8_PACK_F16 2u     /* also store an integer-valued FP16 copy of the weights, which
+                                one large-M tensor-core engine reads; without it large-M
+                                calls run on the CTA-pair engine that widens the INT8 weights
+                                in tensor memory (a third of the memory) */
 
 /* Bytes of the packed buffer for E experts of [N,K] INT8 weights (E = 1 for a dense layer). */
 W8A8_API size_t w8a8_prepacked_bytes(int64_t E, int64_t N, int64_t K, uint32_t flags);
@@ -392,8 +391,9 @@ enum {
   W8A8_ENGINE_NONE = 0,    /* no contraction launched yet on this thread (or M == 0) */
   W8A8_ENGINE_WARP = 1,    /* warp-level mma.sync engine (any shape) */
   W8A8_ENGINE_DECODE = 2,  /* tcgen05 decode engine: dense, M <= 64, int8 weights widened in tensor memory */
-  W8A8_ENGINE_TC = 3       /* tcgen05 engine for large M: fp16 weight copy (W8A8_PACK_F16), or for grouped
-                              calls without it the INT8 weights widened in tensor memory */
+  W8A8_ENGINE_TC = 3,      /* tcgen05 engine for large M reading the fp16 weight copy (W8A8_PACK_F16) */
+  W8A8_ENGINE_TC_I8 = 4    /* tcgen05 engine for large M on CTA pairs reading the INT8 weights, widened in
+                              tensor memory (packs without the fp16 copy) */
 };
 
 /* The engine the last contraction launched by the calling host thread ran on

@@ -168,7 +168,7 @@ def test_moe_layer_exact(T, H, I, E, k, prequant, f16_copy):
     assert np.array_equal(yr, yr_ref)
     assert np.array_equal(y, y_ref)
     if T * k >= 64 * E:  # shapes the tensor-core engines take: the routed codes are kept as fp16
-        assert W.last_engine() == W.ENGINE_TC
+        assert W.last_engine() == (W.ENGINE_TC if f16_copy else W.ENGINE_TC_I8)
         o16 = W.moe_layer_workspace_offset(T, k, H, I, E, 5)
         xq16 = ws[o16:o16 + T * k * H * 2].view(torch.float16).cpu().numpy().reshape(T * k, H)
         xq_ref, _, _, _ = oracle.moe_permute_quant(m.x_tok, m.x_tok_scale, m.topk_ids, E)

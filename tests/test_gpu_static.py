@@ -55,13 +55,13 @@ def static_case(M, N, K, f16, bias, seed):
 
 
 @pytest.mark.parametrize("M,N,K,f16,engine", [(1, 256, 512, False, "decode"), (64, 2048, 7168, False, "decode"),
-                                              (17, 200, 80, False, "decode"), (300, 384, 1040, False, "warp"),
-                                              (130, 200, 64, False, "warp"), (512, 512, 2048, True, "tc"),
-                                              (1000, 768, 2064, True, "tc")])
+                                              (17, 200, 80, False, "decode"), (100, 384, 1040, False, "warp"),
+                                              (300, 384, 1040, False, "tc_i8"), (130, 200, 64, False, "tc_i8"),
+                                              (512, 512, 2048, True, "tc"), (1000, 768, 2064, True, "tc")])
 @pytest.mark.parametrize("bias", [False, True])
 def test_static_quant_matmul_exact(M, N, K, f16, engine, bias):
     d, q, deq, qb, y = static_case(M, N, K, f16, bias, seed=M + N)
-    want = {"decode": W.ENGINE_DECODE, "warp": W.ENGINE_WARP, "tc": W.ENGINE_TC}[engine]
+    want = {"decode": W.ENGINE_DECODE, "warp": W.ENGINE_WARP, "tc": W.ENGINE_TC, "tc_i8": W.ENGINE_TC_I8}[engine]
     assert W.last_engine() == want
     assert np.array_equal(y, oracle.static_quant_matmul(q, d.w, deq, qb))
 
@@ -98,8 +98,8 @@ def test_static_quant_every_bf16_value_in_range(s, o):
     assert np.array_equal(q.cpu().numpy(), oracle.static_quant(xb, np.float32(s), o))
 
 
-@pytest.mark.parametrize("M,f16,engine", [(1, False, W.ENGINE_DECODE), (130, False, W.ENGINE_WARP),
-                                          (256, True, W.ENGINE_TC)])
+@pytest.mark.parametrize("M,f16,engine", [(1, False, W.ENGINE_DECODE), (100, False, W.ENGINE_WARP),
+                                          (130, False, W.ENGINE_TC_I8), (256, True, W.ENGINE_TC)])
 def test_static_matmul_sum_past_int32(M, f16, engine):
     """acc + quant_bias beyond the int32 range (codes of +-127 against weights of 127, so |acc| is about
     1.2e8, and a quant_bias within 100 of +-2^31): the epilogue takes the exact 64-bit sum."""

@@ -1,9 +1,9 @@
 """GPU parity of the tcgen05 engines (large-M shapes; weights packed with their
-fp16 copy, and for grouped calls also without it, when the int8 weights are
-widened in tensor memory): INT32 accumulators, BF16 outputs and the MoE
+fp16 copy, and without it, when the CTA-pair engine widens the INT8 weights
+in tensor memory): INT32 accumulators, BF16 outputs and the MoE
 intermediates must be bit-exact against the oracle.  Each test also checks
-that a tcgen05 engine really ran, through the fp16 activation copy it leaves in
-the workspace."""
+that the expected tcgen05 engine really ran (the host's engine record and the
+fp16 activation copy it leaves in the workspace)."""
 import numpy as np
 import pytest
 import torch
@@ -25,14 +25,18 @@ def a16_region(ws, rows, K):
     return ws[start:start + nbytes].view(torch.float16).view(rows, K)
 
 
-def tc_dense(q, xs, w, wsc, bias=None):
+def tc_dense(q, xs, w, wsc, bias=None, f16_copy=True):
+    """Dense contraction on a tcgen05 engine: the fp16-copy engine, or without the copy the CTA-pair
+    engine on the INT8 weights."""
     M, K = q.shape
     N = w.shape[0]
-    wp = W.w8a8_prepack_weight(dev(w), F16)
+    wp = W.w8a8_prepack_weight(dev(w), F16 if f16_copy else 0)
     ws = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
     y = W.w8a8_quant_matmul(dev(q), dev(xs), wp, dev(wsc), N, None if bias is None else dev_bf16(bias), ws=ws)
+    assert W.last_engine() == (W.ENGINE_TC if f16_copy else W.ENGINE_TC_I8)
     ws2 = W.workspace(W.quant_matmul_workspace_bytes(M, N, K))
     acc = W.w8a8_int8_matmul_acc(dev(q), wp, N, ws=ws2)
+    assert W.last_engine() == (W.ENGINE_TC if f16_copy else W.ENGINE_TC_I8)
     torch.cuda.synchronize()
     # the tcgen05 engine widens q to fp16 at the end of the workspace
     assert torch.equal(a16_region(ws, M, K).cpu(), torch.from_numpy(q.astype(np.float16))), \
@@ -42,16 +46,18 @@ def tc_dense(q, xs, w, wsc, bias=None):
 
 @pytest.mark.parametrize("M,N,K,bias", [(128, 256, 64, False), (130, 200, 80, True), (300, 512, 1040, True),
                                         (256, 384, 4096, False), (1000, 768, 2064, True), (129, 2048, 7168, False),
-                                        (600, 1280, 576, True)])
-def test_tc_dense_exact(M, N, K, bias):
+                                        (600, 1280, 576, True), (385, 300, 144, False)])
+@pytest.mark.parametrize("f16_copy", [True, False])
+def test_tc_dense_exact(M, N, K, bias, f16_copy):
     d = S.make_dense(M, K, N, n_outlier=min(4, K), outlier_mult=20.0, bias=bias, seed=M * 3 + N + K)
     q, xs = oracle.dynamic_quant(d.x)
-    y, acc = tc_dense(q, xs, d.w, d.w_scale, d.bias)
+    y, acc = tc_dense(q, xs, d.w, d.w_scale, d.bias, f16_copy)
     assert np.array_equal(acc, oracle.int8_gemm_acc(q, d.w))
     assert np.array_equal(y, oracle.quant_matmul(q, xs, d.w, d.w_scale, d.bias))
 
 
-def test_tc_accumulation_exact_at_extremes():
+@pytest.mark.parametrize("f16_copy", [True, False])
+def test_tc_accumulation_exact_at_extremes(f16_copy):
     K = 65536
     M = 128
     q = np.full((M, K), 127, np.int8)
@@ -64,18 +70,20 @@ def test_tc_accumulation_exact_at_extremes():
     w[2, : K // 2] = 1
     w[3, ::3] = -127
     w[4:] = np.random.default_rng(1).integers(-128, 128, (252, K), dtype=np.int8)
-    _, acc = tc_dense(q, np.ones(M, np.float32), w, np.ones(256, np.float32))
+    _, acc = tc_dense(q, np.ones(M, np.float32), w, np.ones(256, np.float32), f16_copy=f16_copy)
     ref = q.astype(np.int64) @ w.astype(np.int64).T
     assert np.array_equal(acc.astype(np.int64), ref)
 
 
-def test_tc_dense_prefill_config_sampled_rows():
+@pytest.mark.parametrize("f16_copy", [True, False])
+def test_tc_dense_prefill_config_sampled_rows(f16_copy):
     d = S.dense_config(3)
     q, xs = oracle.dynamic_quant(d.x)
-    wp = W.w8a8_prepack_weight(dev(d.w), F16)
+    wp = W.w8a8_prepack_weight(dev(d.w), F16 if f16_copy else 0)
     qd = dev(q)
     ws = W.workspace(W.quant_matmul_workspace_bytes(d.M, d.N, d.K))
     y = W.w8a8_quant_matmul(qd, dev(xs), wp, dev(d.w_scale), d.N, ws=ws)
+    assert W.last_engine() == (W.ENGINE_TC if f16_copy else W.ENGINE_TC_I8)
     acc = W.w8a8_int8_matmul_acc(qd, wp, d.N)
     rows = sample_rows(d.M, 40, seed=5)
     idx = torch.as_tensor(rows, device="cuda")
@@ -103,6 +111,7 @@ def test_tc_grouped_exact(gl, K, N, f16_copy):
     ws = W.workspace(W.grouped_matmul_workspace_bytes(E, R, N, K))
     y = torch.full((R, N), 3.0, dtype=torch.bfloat16, device="cuda")
     y = W.w8a8_grouped_matmul(dev(q), dev(xs), dev(glnp), wp, dev(wsc), ws=ws, y=y)
+    assert W.last_engine() == (W.ENGINE_TC if f16_copy else W.ENGINE_TC_I8)
     acc = W.w8a8_grouped_matmul_acc(dev(q), dev(glnp), wp, N)
     torch.cuda.synchronize()
     assert torch.equal(a16_region(ws, R, K).cpu(), torch.from_numpy(q.astype(np.float16))), \
@@ -119,6 +128,7 @@ def tc_moe(m, f16_copy=True):
     x, xs = (dev_bf16(m.x), None) if m.x_scale is None else (dev(m.x), dev(m.x_scale))
     ws = W.workspace(W.moe_workspace_bytes(m.R, m.H, m.I, m.E))
     y = W.moe_w13_swiglu_requant_w2(x, xs, dev(m.group_list), w13p, dev(m.s13), w2p, dev(m.s2), ws=ws)
+    assert W.last_engine() == (W.ENGINE_TC if f16_copy else W.ENGINE_TC_I8)
     torch.cuda.synchronize()
     off16 = W.moe_workspace_offset(m.R, m.H, m.I, m.E, 5)
     assert off16 > 0

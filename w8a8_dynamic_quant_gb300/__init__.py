@@ -24,7 +24,7 @@ __all__ = [
     "w8a8_int8_matmul_acc", "grouped_matmul_workspace_bytes", "w8a8_grouped_matmul",
     "w8a8_grouped_matmul_acc", "moe_workspace_bytes", "moe_workspace_offset",
     "moe_w13_swiglu_requant_w2", "read_device_status", "workspace", "w8a8_quant_matmul_noalloc",
-    "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC",
+    "last_engine", "ENGINE_NONE", "ENGINE_WARP", "ENGINE_DECODE", "ENGINE_TC", "ENGINE_TC_I8",
     "w8a8_quantize_weight", "w8a8_quantize_prepack_weight", "w8a8_static_quant", "w8a8_static_prepare",
     "w8a8_static_quant_matmul", "w8a8_mx_quant", "w8a8_mx_matmul", "moe_route_workspace_bytes", "moe_permute_quant", "moe_unpermute_combine", "moe_layer_workspace_bytes",
     "moe_layer_workspace_offset", "moe_layer",
@@ -471,9 +471,10 @@ def read_device_status(ws: torch.Tensor) -> int:
         return int(_capi.lib().w8a8_read_device_status(ws.data_ptr(), _stream(ws.device)))
 
 
-ENGINE_NONE, ENGINE_WARP, ENGINE_DECODE, ENGINE_TC = 0, 1, 2, 3
+ENGINE_NONE, ENGINE_WARP, ENGINE_DECODE, ENGINE_TC, ENGINE_TC_I8 = 0, 1, 2, 3, 4
 
 
 def last_engine() -> int:
-    """Engine the calling thread's last contraction ran on (ENGINE_WARP / ENGINE_DECODE / ENGINE_TC)."""
+    """Engine the calling thread's last contraction ran on (ENGINE_WARP / ENGINE_DECODE / ENGINE_TC /
+    ENGINE_TC_I8)."""
     return int(_capi.lib().w8a8_last_engine())

@@ -218,17 +218,17 @@ w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream,
     t_last_engine = W8A8_ENGINE_TC;
     return cuda_status(launch_tc_gemm(a, a16, b16, sms, stream));
   }
-  if (tc_rows && a.group_list != nullptr) {  // grouped without the fp16 copy: int8 weights widened in TMEM
+  if (tc_rows) {  // without the fp16 copy: CTA pairs with the int8 weights widened in TMEM (dense or grouped)
     if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
-    t_last_engine = W8A8_ENGINE_TC;
-    return cuda_status(launch_tcw_gemm(a, a16, sms, stream));
+    t_last_engine = W8A8_ENGINE_TC_I8;
+    return cuda_status(launch_tcp_gemm(a, a16, sms, stream));
   }
   if (a.group_list == nullptr && a.mode != EPI_SWIGLU && L.dec < L.total) {
-    const int ks = dec_plan_ksplit(a.R, a.N, a.K, sms);  // dense decode: int8 weights widened in TMEM
-    if (ks > 0) {
+    const DecPlan dp = dec_plan(a.R, a.N, a.K, sms);  // dense decode: int8 weights widened in TMEM
+    if (dp.ksplit > 0) {
       a.pack_known = pack_recorded(a.packed, a.E, a.N, a.K, a.pack_flags) ? 1 : 0;
       t_last_engine = W8A8_ENGINE_DECODE;
-      return cuda_status(launch_dec_gemm(a, ks, static_cast<uint8_t*>(ws) + L.dec, stream));
+      return cuda_status(launch_dec_gemm(a, dp, static_cast<uint8_t*>(ws) + L.dec, stream));
     }
   }
   t_last_engine = W8A8_ENGINE_WARP;
@@ -290,7 +290,7 @@ w8a8_status moe_chain(const void* x, const float* x_scale, bool x16_ready, const
   bind_ws(a13, gws, L.g);
   a13.status = static_cast<DeviceStatus*>(ws);
   const cudaError_t e13 = f16w ? launch_tc_gemm(a13, xq16, w13_16, sms, st)
-                         : tc ? launch_tcw_gemm(a13, xq16, sms, st)
+                         : tc ? launch_tcp_gemm(a13, xq16, sms, st)
                              : launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st);
   if (e13 != cudaSuccess) return W8A8_ERR_CUDA;
 
@@ -314,9 +314,9 @@ w8a8_status moe_chain(const void* x, const float* x_scale, bool x16_ready, const
   bind_ws(a2, gws, L.g);
   a2.status = static_cast<DeviceStatus*>(ws);
   const cudaError_t e2 = f16w ? launch_tc_gemm(a2, hq16, w2_16, sms, st)
-                        : tc ? launch_tcw_gemm(a2, hq16, sms, st)
+                        : tc ? launch_tcp_gemm(a2, hq16, sms, st)
                             : launch_reg_gemm(a2, plan_reg_gemm(a2, sms), st);
-  t_last_engine = tc ? W8A8_ENGINE_TC : W8A8_ENGINE_WARP;
+  t_last_engine = f16w ? W8A8_ENGINE_TC : tc ? W8A8_ENGINE_TC_I8 : W8A8_ENGINE_WARP;
   return e2 == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
 }
 

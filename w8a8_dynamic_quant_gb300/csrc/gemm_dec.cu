@@ -30,14 +30,16 @@
 // into an FP32 TMEM accumulator; the CTA's K slice is at most 896, so the
 // accumulator holds an exact integer (|partial| <= 896 * 128^2 < 2^24).
 //
-// Split-K reduction in two steps, neither of which waits on another CTA's
-// progress beyond the cluster barrier: the K splits of a row block form
-// clusters of up to four CTAs; after a cluster barrier each CTA sums, for its
-// quarter of the tokens, the cluster's partial tiles straight out of the other
-// CTAs' shared memory (distributed shared memory).  With more than four
-// splits, each CTA then stores its quarter in its own workspace slot and bumps
-// the arrival counter of that quarter (release); the CTA that arrives last
-// adds the other clusters' slots.  The CTA holding the complete sums applies
+// Split-K reduction, which waits on no other CTA's progress beyond the
+// cluster barrier: the K splits of a row block form clusters of up to eight
+// CTAs; after a cluster barrier each CTA sums, for its share of the tokens
+// (64 / cluster size), the cluster's partial tiles straight out of the other
+// CTAs' shared memory (distributed shared memory), every remote load of a
+// thread in flight at once.  Only when a row block has more K splits than one
+// cluster holds (clusters of at least four then) does a second step follow:
+// each CTA stores its share in its own workspace slot and bumps the arrival
+// counter of that share (release); the CTA that arrives last adds the other
+// clusters' slots.  The CTA holding the complete sums applies
 // the dequant epilogue and writes BF16 (or the INT32 sums) and resets the
 // counter.  Integer addition is exact in any order.
 //
@@ -79,8 +81,9 @@ constexpr uint32_t DC_W_STAGE = DC_ROWS * DC_BK;  // int8 weight tile (16 KB)
 constexpr uint32_t DC_X_STAGE = DC_TOK * DC_BK;   // int8 activation tile (8 KB)
 constexpr uint32_t DC_TILE_I32 = DC_TOK * DC_ROWS * 4;  // int32 partial tile (32 KB)
 constexpr int DC_MAX_KSPLIT = 16;
-constexpr int DC_CLUSTER = 4;                            // CTAs per cluster (consecutive K splits)
-constexpr int DC_SLOT_I32 = DC_TOK / DC_CLUSTER * DC_ROWS;  // int32 per workspace slot
+constexpr int DC_CLUSTER = 8;       // most CTAs per cluster (consecutive K splits)
+constexpr int DC_MIN_SLOT_CLUSTER = 4;  // clusters that meet through workspace slots hold at least 4 CTAs
+constexpr int DC_SLOT_I32 = DC_TOK / DC_MIN_SLOT_CLUSTER * DC_ROWS;  // int32 per workspace slot
 constexpr uint32_t kIdescDec = (1u << 4) | (uint32_t(DC_TOK >> 3) << 17) | (uint32_t(DC_ROWS >> 4) << 24);
 static_assert(DC_B_BYTES % 1024 == 0 && DC_W_STAGE % 1024 == 0 && DC_X_STAGE % 1024 == 0, "1024-byte aligned tiles");
 static_assert(DC_D_COL + DC_TOK <= DC_TMEM_COLS, "tensor memory budget");
@@ -153,7 +156,7 @@ __device__ __forceinline__ void issue_activations(const CUtensorMap* xmap, uint6
 
 // Workspace of the decode engine: per row block and K split a slot for the
 // cluster-summed int32 piece [tokens of the CTA][DC_ROWS], and per row block
-// four arrival counters (one per cluster rank), zero between calls.
+// eight arrival counters (one per cluster rank), zero between calls.
 struct DecWs {
   int32_t* slots;
   uint32_t* cnt;
@@ -169,10 +172,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// Remote load without a memory clobber, so that a thread's loads of several CTAs' tiles are all in
+// flight before the first result is used (volatile keeps them after the cluster barrier before them).
 __device__ __forceinline__ int4 ld_dsmem_v4(uint32_t addr) {
   int4 v;
-  asm volatile("ld.shared::cluster.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
+  asm volatile("ld.shared::cluster.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
 
@@ -321,8 +325,13 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
         widen16(*reinterpret_cast<const uint4*>(xst + t * DC_BK + ((c ^ (t & 7)) << 4)), hh);
         uint8_t* brow = bt + (c >> 2) * DC_B_SUB + t * 128;
         const int cc = (c & 3) * 2;
-        *reinterpret_cast<uint4*>(brow + ((cc ^ (t & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-        *reinterpret_cast<uint4*>(brow + (((cc + 1) ^ (t & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+        // The eight threads of a token write 16-byte chunks cc and cc+1 of its row in both 64-K sub-tiles
+        // (which sit on the same banks); threads c >= 4 store the odd chunk first, so each store
+        // instruction covers all eight chunk positions of the row: no bank conflict.
+        const int first = cc + (c >> 2), second = cc + 1 - (c >> 2);
+        const uint4 lo = make_uint4(hh[0], hh[1], hh[2], hh[3]), hi = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+        *reinterpret_cast<uint4*>(brow + ((first ^ (t & 7)) << 4)) = (c >> 2) ? hi : lo;
+        *reinterpret_cast<uint4*>(brow + ((second ^ (t & 7)) << 4)) = (c >> 2) ? lo : hi;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -401,11 +410,11 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     __syncthreads();
     if (tid == 0) {
       asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      const uint32_t prev = atomicAdd(&ws.cnt[rb * 4 + cr], 1u);
+      const uint32_t prev = atomicAdd(&ws.cnt[rb * DC_CLUSTER + cr], 1u);
       if (prev == static_cast<uint32_t>(ncl - 1)) {
         asm volatile("fence.acq_rel.gpu;" ::: "memory");
         s_last = 1;
-        ws.cnt[rb * 4 + cr] = 0u;  // for the next call
+        ws.cnt[rb * DC_CLUSTER + cr] = 0u;  // for the next call
       }
     }
   } else if (tid == 0) {
@@ -530,16 +539,16 @@ int dec_resident_clusters(int cs) {
 
 template <int MODE>
 cudaError_t launch_dec_mode(const GemmArgs& a, const DecWs& ws, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                            int ksplit, int nblk, cudaStream_t stream) {
+                            const DecPlan& plan, int nblk, cudaStream_t stream) {
   dec_set_attributes();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ksplit), static_cast<unsigned>(nblk), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.ksplit), static_cast<unsigned>(nblk), 1);
   cfg.blockDim = dim3(DC_THREADS, 1, 1);
   cfg.dynamicSmemBytes = kDecSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit < DC_CLUSTER ? ksplit : DC_CLUSTER);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   // may start before the previous kernel on the stream ends, if that kernel allows it (the activation
@@ -559,35 +568,47 @@ size_t dec_ws_bytes(int64_t N) {
          align_up(static_cast<uint64_t>(nblk) * DC_CLUSTER * 4, 256);
 }
 
-// K split for the decode engine: 1, 2, 4 (one cluster per row block) or a
-// multiple of 4 up to 16 (clusters of 4); every CTA covers at most DC_MAX_KB
-// stages of K and all clusters fit in one wave.  Among those, the split with
-// the fewest stages per CTA, and of equal ones the smallest.  0 = shape
+// K split and cluster size for the decode engine.  Every CTA covers at most DC_MAX_KB stages of K and all
+// clusters fit in one wave.  Splits 1, 2, 4 and 8 form one cluster per row block (the reduction is one
+// distributed-shared-memory step); 16 splits form two clusters of 8 that meet through workspace slots.
+// When clusters of 8 cannot all be resident, 8 or 16 splits fall back to clusters of 4.  Among the
+// candidates: the fewest stages per CTA, then the fewest clusters per row block.  ksplit 0 = shape
 // unsuited.
-int dec_plan_ksplit(int64_t M, int64_t N, int64_t K, int num_sms) {
+DecPlan dec_plan(int64_t M, int64_t N, int64_t K, int num_sms) {
   (void)num_sms;
-  if (M < 1 || M > DC_TOK) return 0;
+  DecPlan best;
+  if (M < 1 || M > DC_TOK) return best;
   const int64_t nkb = (K + DC_BK - 1) / DC_BK;
   const int64_t nblk = (N + DC_ROWS - 1) / DC_ROWS;
-  static const int kSplits[] = {1, 2, 4, 8, 12, 16};
-  int best = 0;
   int64_t best_stages = DC_MAX_KB + 1;
+  int best_ncl = 1 << 30;
+  static const int kSplits[] = {1, 2, 4, 8, 16};
   for (int ks : kSplits) {
     if (ks > nkb) break;
-    const int cs = ks < DC_CLUSTER ? ks : DC_CLUSTER;
-    if (nblk * (ks / cs) > dec_resident_clusters(cs)) break;
     const int64_t stages = (nkb + ks - 1) / ks;
-    if (stages < best_stages) {
-      best_stages = stages;
-      best = ks;
+    for (int cs : {8, 4, 2, 1}) {
+      if (cs > ks || ks % cs != 0) continue;
+      if (ks > cs && cs < DC_MIN_SLOT_CLUSTER) continue;
+      if (nblk * (ks / cs) > dec_resident_clusters(cs)) continue;
+      const int ncl = ks / cs;
+      if (stages < best_stages || (stages == best_stages && ncl < best_ncl)) {
+        best_stages = stages;
+        best_ncl = ncl;
+        best.ksplit = ks;
+        best.cluster = cs;
+      }
+      break;  // the largest cluster that fits for this split
     }
   }
-  return best_stages <= DC_MAX_KB ? best : 0;
+  if (best_stages > DC_MAX_KB) best = DecPlan{};
+  return best;
 }
 
-cudaError_t launch_dec_gemm(const GemmArgs& a, int ksplit, void* dec_ws, cudaStream_t stream) {
+cudaError_t launch_dec_gemm(const GemmArgs& a, const DecPlan& plan, void* dec_ws, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
-  if (ksplit < 1 || ksplit > DC_MAX_KSPLIT || (ksplit > DC_CLUSTER && ksplit % DC_CLUSTER != 0) || ksplit == 3)
+  const int ks = plan.ksplit, cs = plan.cluster;
+  if (ks < 1 || ks > DC_MAX_KSPLIT || cs < 1 || cs > DC_CLUSTER || (cs & (cs - 1)) != 0 || ks % cs != 0 ||
+      (ks > cs && cs < DC_MIN_SLOT_CLUSTER))
     return cudaErrorInvalidValue;
   const int nblk = static_cast<int>((a.N + DC_ROWS - 1) / DC_ROWS);
   DecWs ws;
@@ -602,8 +623,8 @@ cudaError_t launch_dec_gemm(const GemmArgs& a, int ksplit, void* dec_ws, cudaStr
       !encode_map_2d(&xmap, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.R, a.K, DC_BK, DC_TOK,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (a.mode == EPI_ACC) return launch_dec_mode<EPI_ACC>(a, ws, wmap, xmap, ksplit, nblk, stream);
-  return launch_dec_mode<EPI_BF16>(a, ws, wmap, xmap, ksplit, nblk, stream);
+  if (a.mode == EPI_ACC) return launch_dec_mode<EPI_ACC>(a, ws, wmap, xmap, plan, nblk, stream);
+  return launch_dec_mode<EPI_BF16>(a, ws, wmap, xmap, plan, nblk, stream);
 }
 
 }  // namespace w8a8

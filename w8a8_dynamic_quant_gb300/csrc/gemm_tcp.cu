@@ -1,0 +1,562 @@
+// gemm_tcp.cu -- exact INT8 contraction on CTA pairs of the 5th-generation
+// tensor cores with the weights read as INT8: the dense prefill linear and
+// the grouped expert GEMMs of MoE prefill (W13 + SwiGLU, W2), for packed
+// weights with or without an FP16 copy (only the INT8 payload is read).
+//
+// Page "DeepSeek-V4 W8A8 执行链从量化权重到 Ascend INT8 算子": §二
+// npu_quant_matmul (INT8 x INT8 -> INT32, then * x_scale * w_scale (+bias) ->
+// BF16; the weight stays INT8 after loading), §三 npu_grouped_matmul over
+// group_list and the W13 -> SwiGLU step, §四 (prefill, large M, gets its own
+// tiling).
+//
+// Engine.  sm_103a has no integer tcgen05.mma kind, so the codes are fed as
+// integer-valued FP16 (exact) to tcgen05.mma.kind::f16 with FP32 accumulators
+// in tensor memory; products |a*b| <= 2^14 are exact and a fresh accumulator
+// is started every 1024 of K, so every accumulator holds an exact integer.
+//
+// Tile.  The weights are the MMA's M side: a CTA pair (tcgen05 cta_group::2)
+// owns 256 weight rows of one expert, 128 in each CTA, and a block of up to
+// 192 of the expert's tokens as N -- the even CTA holds the first half of the
+// block's tokens, the odd CTA the second.  N is the block's token count
+// rounded up to 16, so an expert's ragged last block costs at most 15 rows of
+// work.  Per CTA and 128 of K a stage holds the 128 x 128-byte INT8 weight
+// tile and the two 64-K FP16 sub-tiles of its token rows (128-byte swizzle),
+// 40 KB, brought by TMA into a ring of five stages (four for W13 + SwiGLU,
+// whose epilogue needs 24 KB of shared memory to exchange values).  Four converter warps widen
+// the weight tile -- lane r takes row r -- to integer-valued FP16 and store it
+// into tensor memory, where the MMA reads its A operand, so the large operand
+// is never written back to shared memory.  Per SM and 128 of K this moves
+// 16 KB of weights and 24 KB of tokens through shared memory for 6.3 MFLOP,
+// about 100 bytes per clock at the full tensor rate.
+//
+// Tensor memory (512 columns per CTA): two accumulators of 192 columns at 0
+// and 256, and two A buffers of 128 K (64 columns of FP16 pairs) at 192 and
+// 448.  The accumulators alternate per 1024-deep chunk of K, so the epilogue
+// drains one while the MMAs fill the other.  Stage g of the ring (counted over
+// the whole run) is widened into A buffer g%2, so the commit that frees stage
+// g-2 of the shared-memory ring also frees the buffer stage g reuses: one
+// commit per stage frees both.
+//
+// Synchronisation.  TMA: each CTA's weight tile completes on its own barrier
+// (its converters wait for it); both CTAs' token tiles complete on the even
+// CTA's barrier.  Converters of both CTAs arrive on the even CTA's A-buffer
+// barrier once per stage; the even CTA's MMA thread issues tcgen05.mma.cta_group::2
+// M = 256 N = 16..192 K = 16 and frees shared-memory stages (with their A
+// slots) and accumulators in both CTAs by multicast commits.  Both CTAs'
+// epilogue warps release an accumulator on the even CTA's barrier.
+//
+// Warp roles (448 threads, one CTA per SM, persistent over tiles):
+//   warp 0       TMA producer
+//   warp 1       TMEM owner; the even CTA's lane 0 issues the MMAs
+//   warps 2-5    converters: lane r of warp w widens weight row 32*(w%4)+r
+//   warps 6-13   epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows)
+//                and one half (96 tokens) of the accumulator's columns
+// W13 + SwiGLU: the gate/up interleave puts gate channel j in tile row j%64
+// and up channel j in row 64 + j%64 of a CTA's 128 rows, so a gate warp and
+// its up warp meet through shared memory: the gate warp passes its BF16 gate
+// values of the second 48 tokens of its half, the up warp its BF16 up values
+// of the first 48, and each computes SwiGLU for 48 tokens (the SwiGLU math is
+// spread over all four SM sub-partitions).
+// Every mbarrier wait is bounded (2 s): on expiry the CTA sets
+// W8A8_ERR_DEVICE_TIMEOUT, lets in-flight copies land, frees TMEM and returns.
+#include "kernels.cuh"
+#include "tc_common.cuh"
+
+namespace w8a8 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int P_WROWS = 256;  // weight rows per pair tile (MMA M)
+constexpr int P_WHALF = 128;  // weight rows per CTA
+constexpr int P_NT = 192;     // most tokens per tile (MMA N)
+constexpr int P_NHALF = 96;   // token rows per CTA
+constexpr int P_BK = 128;     // K per shared-memory stage
+constexpr int P_MAX_STAGES = 5;
+constexpr int p_stages(int mode) { return mode == EPI_SWIGLU ? 4 : 5; }
+constexpr int P_KB_PER_CHUNK = kChunkK / P_BK;  // 8
+constexpr uint32_t P_X_SUB = P_NHALF * 64 * 2;  // 64-K fp16 token sub-tile (12 KB)
+constexpr uint32_t P_X_BYTES = 2 * P_X_SUB;     // 24 KB
+constexpr uint32_t P_W_BYTES = P_WHALF * P_BK;  // 16 KB
+constexpr uint32_t P_STAGE_BYTES = P_W_BYTES + P_X_BYTES;
+constexpr int P_THREADS = 448;
+constexpr int P_CONV_WARPS = 4;
+constexpr int P_EPI0 = 6;
+constexpr int P_EPI_WARPS = 8;
+constexpr int P_CLUSTER = 2;
+constexpr uint16_t P_PAIR_MASK = 0x3;
+constexpr uint32_t P_TMEM_COLS = 512;
+// accumulator b at column 256*b; A buffer p (128 K, 64 columns) at 192 + 256*p
+__host__ __device__ constexpr uint32_t p_acc_col(uint32_t b) { return 256u * b; }
+__host__ __device__ constexpr uint32_t p_abuf_col(uint32_t p) { return 192u + 256u * p; }
+static_assert(p_abuf_col(1) + 64u <= 512u && p_acc_col(1) + 192u <= p_abuf_col(1) && p_acc_col(0) + 192u <= p_abuf_col(0),
+              "tensor memory budget");
+constexpr int kMaxE = 1024;
+constexpr int P_XCH = P_NHALF / 2;  // SwiGLU tokens each warp of a gate/up pair hands to the other
+// SwiGLU exchange: [gate warp pair][token half][direction gate->up, up->gate][48 tokens][32 lanes] bf16
+constexpr uint32_t P_XCH_BYTES = 2 * 2 * 2 * P_XCH * 32 * 2;
+static_assert(P_STAGE_BYTES % 1024 == 0 && P_W_BYTES % 1024 == 0 && P_X_SUB % 1024 == 0, "1024-byte tiles");
+static_assert(P_NHALF % 8 == 0, "whole 8-row swizzle atoms per CTA");
+
+// kind::f16 instruction descriptor: D = F32, A = B = F16, both K-major, M = 256, N = n (multiple of 16).
+__device__ __forceinline__ uint32_t idesc_pair(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(P_WROWS >> 4) << 24);
+}
+
+// D(tmem, both CTAs) (+)= A(tmem, both CTAs) * B(smem desc, both CTAs), kind::f16 on a CTA pair: each CTA's
+// tensor memory holds its 128 rows of A (K packed two fp16 per column) and of D; B rows [0,N/2) in the even
+// CTA, [N/2,N) in the odd one.  Issued by one thread of the even CTA.
+__device__ __forceinline__ void tc_mma_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
+
+// 16 int8 (one 16-byte chunk) -> 8 words of fp16 pairs.
+__device__ __forceinline__ void widen16(const uint4& x, uint32_t* h) {
+  s8x4_to_f16x4(x.x, h[0], h[1]);
+  s8x4_to_f16x4(x.y, h[2], h[3]);
+  s8x4_to_f16x4(x.z, h[4], h[5]);
+  s8x4_to_f16x4(x.w, h[6], h[7]);
+}
+
+struct PTile {
+  int e, tb, wb, cnt;
+  int n_eff;     // MMA N: the block's token count rounded up to 16
+  int tvalid;    // tokens of the block that belong to the expert
+  int64_t row0;  // first routed row of the block
+};
+
+// Work unit t -> (expert, 256-row weight block, token block); the token block varies fastest, so the pairs
+// in flight share a weight block and the expert's token rows stay in L2 while the weight blocks sweep past.
+__device__ __forceinline__ PTile p_decode(int t, int E, int WB, const int* s_unit_prefix, const int* s_row_off) {
+  PTile ti;
+  ti.e = expert_of(t, E, s_unit_prefix);
+  const int local = t - s_unit_prefix[ti.e];
+  ti.cnt = s_row_off[ti.e + 1] - s_row_off[ti.e];
+  const int TB = (ti.cnt + P_NT - 1) / P_NT;
+  ti.wb = local / TB;
+  ti.tb = local - ti.wb * TB;
+  ti.tvalid = min(P_NT, ti.cnt - ti.tb * P_NT);
+  ti.n_eff = (ti.tvalid + 15) & ~15;
+  ti.row0 = static_cast<int64_t>(s_row_off[ti.e]) + static_cast<int64_t>(ti.tb) * P_NT;
+  (void)WB;
+  return ti;
+}
+
+// 14 warps: the register file is split over the four SM sub-partitions, one of which holds four of the
+// warps, so 128 registers a thread is the most the launch allows.
+template <int MODE>
+__global__ void __cluster_dims__(P_CLUSTER, 1, 1) __launch_bounds__(P_THREADS, 1)
+tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs a) {
+  constexpr int STAGES = p_stages(MODE);
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_wfull[P_MAX_STAGES];  // this CTA's weight tile landed
+  __shared__ __align__(8) uint64_t bar_xfull[P_MAX_STAGES];  // even CTA: both CTAs' token tiles landed
+  __shared__ __align__(8) uint64_t bar_empty[P_MAX_STAGES];  // the MMAs reading the stage (and its A buffer) are done
+  __shared__ __align__(8) uint64_t bar_aready[2];             // even CTA: both CTAs widened the stage into A buffer
+  __shared__ __align__(8) uint64_t bar_accf[2];
+  __shared__ __align__(8) uint64_t bar_acce[2];          // even CTA: both CTAs drained the accumulator
+  // SwiGLU exchange, per (warp pair, token half): gate values written / read, up values written / read
+  __shared__ __align__(8) uint64_t bar_gfull[4];
+  __shared__ __align__(8) uint64_t bar_gfree[4];
+  __shared__ __align__(8) uint64_t bar_ufull[4];
+  __shared__ __align__(8) uint64_t bar_ufree[4];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+  __shared__ int s_bad;
+  __shared__ int s_unit_prefix[kMaxE + 1];
+  __shared__ int s_row_off[kMaxE + 1];
+  __shared__ int s_warp[P_THREADS / 32];
+  __shared__ float s_sx[P_EPI_WARPS][P_NHALF];           // token scales of each epilogue warp's tile half
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = static_cast<int>(a.E);
+  const int64_t N = a.N;
+  const int64_t K = a.K;
+  const int WB = static_cast<int>((N + P_WROWS - 1) / P_WROWS);
+  const int nkb = static_cast<int>((K + P_BK - 1) / P_BK);
+  const int nchunk = (nkb + P_KB_PER_CHUNK - 1) / P_KB_PER_CHUNK;
+
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_base = smem_u32(stages);
+  uint16_t* xchbuf = reinterpret_cast<uint16_t*>(stages + STAGES * P_STAGE_BYTES);
+  uint32_t rank, cluster_id, nclusters;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cluster_id));
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(nclusters));
+  const int c0 = static_cast<int>(cluster_id), cstep = static_cast<int>(nclusters);
+
+  if (tid == 0) {
+    s_abort = 0;
+    s_bad = 0;
+    const PackedHeader* h = static_cast<const PackedHeader*>(a.packed);
+    if (h->magic != kPackMagic || h->version != kPackVersion || h->E != a.E || h->N != a.N || h->K != a.K ||
+        ((h->flags ^ a.pack_flags) & W8A8_PACK_GATE_UP) != 0u)
+      s_bad = W8A8_ERR_PACKED;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&bar_wfull[s]), 1);
+      mbar_init(smem_u32(&bar_xfull[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&bar_aready[s]), P_CLUSTER * P_CONV_WARPS);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_accf[b]), 1);
+      mbar_init(smem_u32(&bar_acce[b]), P_CLUSTER * P_EPI_WARPS);
+    }
+    for (int p = 0; p < 4; ++p) {
+      mbar_init(smem_u32(&bar_gfull[p]), 1);
+      mbar_init(smem_u32(&bar_gfree[p]), 1);
+      mbar_init(smem_u32(&bar_ufull[p]), 1);
+      mbar_init(smem_u32(&bar_ufree[p]), 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
+                 "r"(P_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  // ---- per-expert rows and work units (token blocks x 256-row weight blocks)
+  int units_total;
+  const int rows_total = scan_groups<P_THREADS, kMaxE>(
+      a, E, [WB](int c) { return ((c + P_NT - 1) / P_NT) * WB; }, s_row_off, s_unit_prefix, s_warp, &s_bad,
+      &units_total);
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers and tensor memory exist before either touches the other's
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  int bad = s_bad;
+  if (rows_total != a.R) bad |= W8A8_ERR_GROUP_LIST << 8;
+  if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, (bad & 0xff) ? (bad & 0xff) : (bad >> 8), 0u);
+  const int units = bad ? 0 : units_total;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = c0; t < units && !s_abort; t += cstep) {
+        const PTile ti = p_decode(t, E, WB, s_unit_prefix, s_row_off);
+        // this CTA's token rows: the first or the second half of the block's n_eff tokens
+        const int yx = static_cast<int>(ti.row0) + static_cast<int>(rank) * (ti.n_eff >> 1);
+        const int yw = static_cast<int>(static_cast<int64_t>(ti.e) * N + static_cast<int64_t>(ti.wb) * P_WROWS) +
+                       static_cast<int>(rank) * P_WHALF;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
+          const uint32_t sa = stage_base + stage * P_STAGE_BYTES;
+          const uint32_t wf = smem_u32(&bar_wfull[stage]);
+          mbar_expect_tx(wf, P_W_BYTES);
+          tma_load_2d(sa, &tmW, kb * P_BK, yw, wf);
+          const uint32_t xf = smem_u32(&bar_xfull[stage]);
+          if (rank == 0) mbar_expect_tx(xf, P_CLUSTER * P_X_BYTES);
+          const uint32_t xf_even = smem_cluster_addr(xf, 0);
+          tma_load_2d_pair(sa + P_W_BYTES, &tmX, kb * P_BK, yx, xf_even);
+          tma_load_2d_pair(sa + P_W_BYTES + P_X_SUB, &tmX, kb * P_BK + 64, yx, xf_even);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: the last fill of every stage has been consumed, so no copy into this CTA and no arrival on
+      // the even CTA's barriers from this CTA's copies is still in flight when the pair leaves.
+      for (int i = 0; i < STAGES && !s_abort; ++i) {
+        if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 5u)) break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      uint32_t g = 0;  // stages consumed so far: ring index g % STAGES, A buffer g % 2
+      uint32_t acc_count = 0;
+      for (int t = c0; t < units && !s_abort; t += cstep) {
+        const PTile ti = p_decode(t, E, WB, s_unit_prefix, s_row_off);
+        const uint32_t idesc = idesc_pair(ti.n_eff);
+        bool ok = true;
+        for (int c = 0; c < nchunk && ok; ++c) {
+          const uint32_t b = acc_count & 1u;
+          const uint32_t use = acc_count >> 1;
+          if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + p_acc_col(b);
+          const int kb_end = min(nkb, (c + 1) * P_KB_PER_CHUNK);
+          for (int kb = c * P_KB_PER_CHUNK; kb < kb_end && ok; ++kb, ++g) {
+            const int stage = static_cast<int>(g % STAGES);
+            if (!mbar_wait(smem_u32(&bar_xfull[stage]), (g / STAGES) & 1u, &s_abort, a.status, 3u) ||
+                !mbar_wait(smem_u32(&bar_aready[g & 1u]), (g >> 1) & 1u, &s_abort, a.status, 6u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sx = stage_base + stage * P_STAGE_BYTES + P_W_BYTES;
+            const uint32_t abuf = tmem_base + p_abuf_col(g & 1u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // the two 64-K token sub-tiles of the stage
+              const uint64_t bdesc = smem_desc_sw128(sx + h * P_X_SUB);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                tc_mma_pair_tmem_a(d_tmem, abuf + 32u * h + 8u * k, bdesc + 2u * k, idesc,
+                                   (kb > c * P_KB_PER_CHUNK || h > 0 || k > 0) ? 1u : 0u);
+            }
+            // frees the stage and its two A slots in both CTAs
+            tc_commit_pair_mc(smem_u32(&bar_empty[stage]), P_PAIR_MASK);
+          }
+          tc_commit_pair_mc(smem_u32(&bar_accf[b]), P_PAIR_MASK);
+          ++acc_count;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp < P_EPI0) {
+    // ------------------------------------------------------------- converters (both CTAs)
+    const int q = warp & 3;
+    const int row = 32 * q + lane;  // weight row of this CTA's half == TMEM lane
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    const uint32_t aready_even0 = smem_cluster_addr(smem_u32(&bar_aready[0]), 0);
+    uint32_t g = 0;  // stages widened so far (as in the MMA issuer)
+    bool ok = true;
+    for (int t = c0; t < units && ok; t += cstep) {
+      for (int kb = 0; kb < nkb && ok; ++kb, ++g) {
+        const int stage = static_cast<int>(g % STAGES);
+        // every lane observes the completed weight copy itself
+        const int got = mbar_wait(smem_u32(&bar_wfull[stage]), (g / STAGES) & 1u, &s_abort, a.status, 7u) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        // weight row `row`: 128 bytes, 16-byte chunk c stored at chunk c ^ (row & 7) (128-byte swizzle)
+        const uint8_t* wrow = stages + stage * P_STAGE_BYTES + row * P_BK;
+        uint32_t v[64];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          widen16(*reinterpret_cast<const uint4*>(wrow + ((c ^ (row & 7)) << 4)), &v[8 * c]);
+        if (g >= 2) {
+          // A buffer g % 2 was last read by stage g - 2: wait for the commit that freed that stage
+          const uint32_t gp = g - 2;
+          const int free_ok =
+              mbar_wait(smem_u32(&bar_empty[gp % STAGES]), (gp / STAGES) & 1u, &s_abort, a.status, 8u) ? 1 : 0;
+          if (!__all_sync(0xffffffffu, free_ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st64(lane_addr + p_abuf_col(g & 1u), v);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(aready_even0 + 8u * (g & 1u));
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int ew = warp - P_EPI0;
+    const int q = warp & 3;
+    const int h = ew >> 2;              // token half of the tile: columns [96h, 96h + 96)
+    const int n_loc = 32 * q + lane;    // weight row of this CTA's half
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    const uint32_t acce_even = smem_cluster_addr(smem_u32(&bar_acce[0]), 0);
+    float* sxw = s_sx[ew];
+    uint32_t acc_count = 0, ntile = 0;
+    for (int t = c0; t < units && !s_abort; t += cstep) {
+      const PTile ti = p_decode(t, E, WB, s_unit_prefix, s_row_off);
+      const int64_t rowh = ti.row0 + P_NHALF * h;                    // routed row of column 96h
+      const int tv = min(P_NHALF, ti.tvalid - P_NHALF * h);         // tokens of the half that have rows
+      if (MODE != EPI_ACC) {  // the half's token scales, loaded while the tile's MMAs run
+        for (int i = lane; i < P_NHALF; i += 32)
+          sxw[i] = i < tv ? (a.x_scale != nullptr ? a.x_scale[rowh + i] : 1.0f) : 0.0f;
+        __syncwarp();
+      }
+      int sums[P_NHALF];
+#pragma unroll
+      for (int i = 0; i < P_NHALF; ++i) sums[i] = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunk; ++c) {
+        const uint32_t b = acc_count & 1u;
+        const uint32_t use = acc_count >> 1;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(smem_u32(&bar_accf[b]), use & 1u, &s_abort, a.status, 4u) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col0 = p_acc_col(b) + P_NHALF * h;
+#pragma unroll
+        for (int j = 0; j < P_NHALF / 16; ++j) {
+          uint32_t v[16];
+          tmem_ld16(lane_addr + col0 + 16 * j, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sums[16 * j + i] += __float2int_rn(__uint_as_float(v[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_even + 8u * b);
+        ++acc_count;
+      }
+      if (!ok) break;
+
+      const int64_t n = static_cast<int64_t>(ti.wb) * P_WROWS + static_cast<int64_t>(rank) * P_WHALF + n_loc;
+      if constexpr (MODE == EPI_ACC) {
+        if (n < N) {
+          int32_t* dst = static_cast<int32_t*>(a.out) + rowh * N + n;
+#pragma unroll
+          for (int i = 0; i < P_NHALF; ++i)
+            if (i < tv) dst[i * N] = sums[i];
+        }
+      } else if constexpr (MODE == EPI_BF16) {
+        if (n < N) {
+          const float sw = a.w_scale[static_cast<int64_t>(ti.e) * N + n];
+          const float bias = a.bias ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
+          const int32_t qb = a.qbias ? a.qbias[n] : 0;
+          uint16_t* dst = static_cast<uint16_t*>(a.out) + rowh * N + n;
+#pragma unroll
+          for (int i = 0; i < P_NHALF; ++i) {
+            if (i < tv) {
+              float f = a.qbias != nullptr ? dequant_q(sums[i], qb, sxw[i], sw) : dequant(sums[i], sxw[i], sw);
+              if (a.bias) f = __fadd_rn(f, bias);
+              dst[i * N] = f32_to_bf16_bits(f);
+            }
+          }
+        }
+      } else {  // EPI_SWIGLU: rows [0,64) of this CTA's half are gate channels, [64,128) the matching up channels
+        const int p = q & 1;
+        const bool up = q >= 2;
+        const int64_t I = N / 2;
+        const int64_t j = (static_cast<int64_t>(ti.wb) * 2 + rank) * kGateUpBlock + 32 * p + lane;
+        const float swv = j < I ? a.w_scale[static_cast<int64_t>(ti.e) * N + (up ? I : 0) + j] : 0.0f;
+        const int pi = p * 2 + h;
+        uint16_t* gbuf = xchbuf + (pi * 2 + 0) * P_XCH * 32 + lane;  // gate -> up: gate of tokens [48, 96)
+        uint16_t* ubuf = xchbuf + (pi * 2 + 1) * P_XCH * 32 + lane;  // up -> gate: up of tokens [0, 48)
+        const uint32_t par = ntile & 1u;
+        // my BF16 values of the tokens the other warp computes
+        const uint32_t b_free = smem_u32(up ? &bar_ufree[pi] : &bar_gfree[pi]);
+        const uint32_t b_full = smem_u32(up ? &bar_ufull[pi] : &bar_gfull[pi]);
+        int got = 0;
+        if (lane == 0) got = mbar_wait(b_free, par ^ 1u, &s_abort, a.status, 9u) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;
+        // (the token offsets are compile-time constants in each branch, so sums[] stays in registers)
+        if (up) {
+#pragma unroll
+          for (int i = 0; i < P_XCH; ++i) {
+            float v = 0.0f;
+            if (i < tv && j < I) v = dequant(sums[i], sxw[i], swv);
+            ubuf[i * 32] = f32_to_bf16_bits(v);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < P_XCH; ++i) {
+            float v = 0.0f;
+            if (P_XCH + i < tv && j < I) v = dequant(sums[P_XCH + i], sxw[P_XCH + i], swv);
+            gbuf[i * 32] = f32_to_bf16_bits(v);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_full);
+        // the other warp's values of my tokens, then SwiGLU and the store
+        const uint32_t o_full = smem_u32(up ? &bar_gfull[pi] : &bar_ufull[pi]);
+        const uint32_t o_free = smem_u32(up ? &bar_gfree[pi] : &bar_ufree[pi]);
+        if (lane == 0) got = mbar_wait(o_full, par, &s_abort, a.status, 10u) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;
+        if (j < I) {
+          if (up) {  // tokens [48, 96): gate from the gate warp, my up
+            uint16_t* dst = static_cast<uint16_t*>(a.out) + (rowh + P_XCH) * I + j;
+#pragma unroll
+            for (int i = 0; i < P_XCH; ++i) {
+              if (P_XCH + i < tv) {
+                const float u = bf16_round(dequant(sums[P_XCH + i], sxw[P_XCH + i], swv));
+                dst[static_cast<int64_t>(i) * I] = swiglu_bf16(bf16_bits_to_f32(gbuf[i * 32]), u);
+              }
+            }
+          } else {  // tokens [0, 48): my gate, up from the up warp
+            uint16_t* dst = static_cast<uint16_t*>(a.out) + rowh * I + j;
+#pragma unroll
+            for (int i = 0; i < P_XCH; ++i) {
+              if (i < tv) {
+                const float gt = bf16_round(dequant(sums[i], sxw[i], swv));
+                dst[static_cast<int64_t>(i) * I] = swiglu_bf16(gt, bf16_bits_to_f32(ubuf[i * 32]));
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        ++ntile;
+      }
+      __syncwarp();  // the scales of this tile are read before the next tile overwrites them
+    }
+  }
+
+  // ---- teardown: on abort, give in-flight copies and MMAs time to land first, then the pair leaves
+  // together (no copy or remote arrival may target a CTA that has left).
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 20000000ull) {
+    }
+  }
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(P_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int MODE>
+cudaError_t launch_tcp_mode(const CUtensorMap& mx, const CUtensorMap& mw, const GemmArgs& a, int grid, size_t smem,
+                            cudaStream_t stream) {
+  auto k = tcp_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k<<<grid, P_THREADS, smem, stream>>>(mx, mw, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tcp_gemm(const GemmArgs& a, const void* a_f16, int num_sms, cudaStream_t stream) {
+  if (a.R == 0) return cudaSuccess;
+  // fp16 token rows [R, K] in boxes of 96 rows x 64 K, and the int8 weight payload [E*N, K] in boxes of
+  // 128 rows x 128 K; rows past the ends read as zero
+  CUtensorMap mx, mw;
+  const uint8_t* w_i8 = static_cast<const uint8_t*>(a.packed) + pack_layout(a.E, a.N, a.K, 0).i8_offset;
+  if (!encode_map_2d(&mx, a_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.R, a.K, 64, P_NHALF,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_2d(&mw, w_i8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.E * a.N, a.K, P_BK, P_WHALF,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const int64_t wb = (a.N + P_WROWS - 1) / P_WROWS;
+  const int64_t units = ((a.R + P_NT - 1) / P_NT + (a.group_list != nullptr ? a.E : 0)) * wb;
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / P_CLUSTER));
+  const int grid = static_cast<int>(clusters * P_CLUSTER);
+  const size_t smem_sw = static_cast<size_t>(p_stages(EPI_SWIGLU)) * P_STAGE_BYTES + P_XCH_BYTES + 1024;
+  const size_t smem = static_cast<size_t>(p_stages(EPI_BF16)) * P_STAGE_BYTES + 1024;
+  switch (a.mode) {
+    case EPI_ACC: return launch_tcp_mode<EPI_ACC>(mx, mw, a, grid, smem, stream);
+    case EPI_SWIGLU: return launch_tcp_mode<EPI_SWIGLU>(mx, mw, a, grid, smem_sw, stream);
+    default: return launch_tcp_mode<EPI_BF16>(mx, mw, a, grid, smem, stream);
+  }
+}
+
+}  // namespace w8a8

@@ -109,14 +109,21 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f
 // tcgen05 engine for grouped contractions: int8 weights (the packed payload) widened in TMEM as the A
 // operand, a_f16: [R,K] activations as fp16 (B operand).
 cudaError_t launch_tcw_gemm(const GemmArgs& a, const void* a_f16, int num_sms, cudaStream_t stream);
+// tcgen05 engine on CTA pairs for large M, dense or grouped: int8 weights (the packed payload) widened in
+// TMEM as the M = 256 side, a_f16: [R,K] activations as fp16 (the N side, up to 192 tokens per tile).
+cudaError_t launch_tcp_gemm(const GemmArgs& a, const void* a_f16, int num_sms, cudaStream_t stream);
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
 // tcgen05 decode engine (dense, M <= 64): int8 weights widened into TMEM, K
 // split over clusters of CTAs whose partials meet in distributed shared memory
 // and, across clusters, in workspace slots.
-// dec_plan_ksplit returns 0 when the shape does not suit it.
+// dec_plan returns ksplit 0 when the shape does not suit it.
+struct DecPlan {
+  int ksplit = 0;   // K splits per 128-row weight block
+  int cluster = 0;  // CTAs per cluster (consecutive K splits)
+};
 size_t dec_ws_bytes(int64_t N);
-int dec_plan_ksplit(int64_t M, int64_t N, int64_t K, int num_sms);
-cudaError_t launch_dec_gemm(const GemmArgs& a, int ksplit, void* dec_ws, cudaStream_t stream);
+DecPlan dec_plan(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_dec_gemm(const GemmArgs& a, const DecPlan& plan, void* dec_ws, cudaStream_t stream);
 
 }  // namespace w8a8
