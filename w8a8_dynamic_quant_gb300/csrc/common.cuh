@@ -85,14 +85,15 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t v, uint32_t& lo, uint32_t
 //   ln2_hi = ln 2 cut to 15 significant bits (n*ln2_hi exact),
 //   ln2_lo = fl(ln 2 - ln2_hi); c_k = fl(1/k!);
 //   e^x = (p * 2^(n/2)) * 2^(n - n/2) with n/2 truncated toward zero.
-// x > 89 -> +inf, x < -104 -> 0.  Each step is a correctly rounded binary32
-// operation, so the result is fully determined by these steps.
+// x > 89 -> +inf, x < -104 -> 0, NaN -> NaN.  Each step is a correctly
+// rounded binary32 operation, so the result is fully determined by these steps.
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
 
-__device__ __forceinline__ float exp_cw(float x) {
-  if (x != x) return x;
-  if (x > 89.0f) return __int_as_float(0x7f800000);
-  if (x < -104.0f) return 0.0f;
+// Branch-free: the steps run on x clamped to [-104, 89] (unchanged inside that range, so every result there
+// is the same), and the out-of-range and NaN results are selected at the end; without branches the
+// compiler can interleave the steps of neighbouring elements.
+__device__ __forceinline__ float exp_cw(float x_in) {
+  const float x = fminf(fmaxf(x_in, -104.0f), 89.0f);
   const float log2e = __int_as_float(0x3fb8aa3b);
   const float ln2_hi = __int_as_float(0x3f317200);
   const float ln2_lo = __int_as_float(0x35bfbe8e);
@@ -115,7 +116,10 @@ __device__ __forceinline__ float exp_cw(float x) {
   const int ni = static_cast<int>(n);
   const int n1 = ni / 2;
   const int n2 = ni - n1;
-  return __fmul_rn(__fmul_rn(p, pow2i(n1)), pow2i(n2));
+  const float y = __fmul_rn(__fmul_rn(p, pow2i(n1)), pow2i(n2));
+  const float hi = x_in > 89.0f ? __int_as_float(0x7f800000) : y;
+  const float lo = x_in < -104.0f ? 0.0f : hi;
+  return x_in != x_in ? x_in : lo;
 }
 
 // h = bf16((g * sigmoid(g)) * u), sigmoid(g) = 1 / (1 + exp(-g)).

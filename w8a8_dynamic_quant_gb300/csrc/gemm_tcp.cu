@@ -21,8 +21,11 @@
 // rounded up to 16, so an expert's ragged last block costs at most 15 rows of
 // work.  Per CTA and 128 of K a stage holds the 128 x 128-byte INT8 weight
 // tile and the two 64-K FP16 sub-tiles of its token rows (128-byte swizzle),
-// 40 KB, brought by TMA into a ring of five stages (four for W13 + SwiGLU,
-// whose epilogue needs 24 KB of shared memory to exchange values).  Four converter warps widen
+// 40 KB, brought by TMA into a ring of four stages (five for the INT32
+// output, whose epilogue needs no shared memory).  The BF16 epilogues stage
+// each warp's results in shared memory as [token][32 channels] and write them
+// as 16-byte pieces of output rows: one thread per channel storing 2 bytes
+// per token row cost about 80 cycles a store.  Four converter warps widen
 // the weight tile -- lane r takes row r -- to integer-valued FP16 and store it
 // into tensor memory, where the MMA reads its A operand, so the large operand
 // is never written back to shared memory.  Per SM and 128 of K this moves
@@ -56,7 +59,8 @@
 // its up warp meet through shared memory: the gate warp passes its BF16 gate
 // values of the second 48 tokens of its half, the up warp its BF16 up values
 // of the first 48, and each computes SwiGLU for 48 tokens (the SwiGLU math is
-// spread over all four SM sub-partitions).
+// spread over all four SM sub-partitions) in a compact loop over values kept
+// in shared memory.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA sets
 // W8A8_ERR_DEVICE_TIMEOUT, lets in-flight copies land, frees TMEM and returns.
 #include "kernels.cuh"
@@ -74,7 +78,7 @@ constexpr int P_NT = 192;     // most tokens per tile (MMA N)
 constexpr int P_NHALF = 96;   // token rows per CTA
 constexpr int P_BK = 128;     // K per shared-memory stage
 constexpr int P_MAX_STAGES = 5;
-constexpr int p_stages(int mode) { return mode == EPI_SWIGLU ? 4 : 5; }
+constexpr int p_stages(int mode) { return mode == EPI_ACC ? 5 : 4; }
 constexpr int P_KB_PER_CHUNK = kChunkK / P_BK;  // 8
 constexpr uint32_t P_X_SUB = P_NHALF * 64 * 2;  // 64-K fp16 token sub-tile (12 KB)
 constexpr uint32_t P_X_BYTES = 2 * P_X_SUB;     // 24 KB
@@ -94,8 +98,13 @@ static_assert(p_abuf_col(1) + 64u <= 512u && p_acc_col(1) + 192u <= p_abuf_col(1
               "tensor memory budget");
 constexpr int kMaxE = 1024;
 constexpr int P_XCH = P_NHALF / 2;  // SwiGLU tokens each warp of a gate/up pair hands to the other
-// SwiGLU exchange: [gate warp pair][token half][direction gate->up, up->gate][48 tokens][32 lanes] bf16
-constexpr uint32_t P_XCH_BYTES = 2 * 2 * 2 * P_XCH * 32 * 2;
+// SwiGLU buffers: [gate warp pair][token half][gate give, gate keep, up give, up keep][48 tokens][32 lanes] bf16
+constexpr uint32_t P_XCH_BYTES = 4 * 4 * P_XCH * 32 * 2;
+// BF16 output staging: per epilogue warp [96 tokens][32 channels] bf16
+constexpr uint32_t P_OUT_BYTES = P_EPI_WARPS * P_NHALF * 32 * 2;
+__host__ __device__ constexpr uint32_t p_epi_bytes(int mode) {
+  return mode == EPI_SWIGLU ? P_XCH_BYTES : mode == EPI_BF16 ? P_OUT_BYTES : 0u;
+}
 static_assert(P_STAGE_BYTES % 1024 == 0 && P_W_BYTES % 1024 == 0 && P_X_SUB % 1024 == 0, "1024-byte tiles");
 static_assert(P_NHALF % 8 == 0, "whole 8-row swizzle atoms per CTA");
 
@@ -115,14 +124,30 @@ __device__ __forceinline__ void tc_mma_pair_tmem_a(uint32_t d_tmem, uint32_t a_t
       : "memory");
 }
 
-__device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
-
 // 16 int8 (one 16-byte chunk) -> 8 words of fp16 pairs.
 __device__ __forceinline__ void widen16(const uint4& x, uint32_t* h) {
   s8x4_to_f16x4(x.x, h[0], h[1]);
   s8x4_to_f16x4(x.y, h[2], h[3]);
   s8x4_to_f16x4(x.z, h[4], h[5]);
   s8x4_to_f16x4(x.w, h[6], h[7]);
+}
+
+// Rows [0, rows) of a warp's staging buffer [rows][32] bf16 (shared memory) to out[(row0 + r) * ld + c0 + c],
+// c < min(32, ld - c0): 16-byte stores of whole 64-byte row pieces when they fit (8 rows a warp instruction),
+// else one 2-byte store a lane and row.
+__device__ __forceinline__ void store_rows(const uint16_t* stg, uint16_t* out, int64_t row0, int64_t ld, int64_t c0,
+                                           int rows, int lane) {
+  const int64_t ncols = ld - c0 < 32 ? ld - c0 : 32;
+  if (ncols <= 0 || rows <= 0) return;
+  if (ncols == 32 && (ld & 7) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0u) {
+    const int c = (lane & 3) * 8;
+#pragma unroll 4
+    for (int r = lane >> 2; r < rows; r += 8)
+      *reinterpret_cast<uint4*>(out + (row0 + r) * ld + c0 + c) = *reinterpret_cast<const uint4*>(stg + r * 32 + c);
+  } else {
+    for (int r = 0; r < rows; ++r)
+      if (lane < ncols) out[(row0 + r) * ld + c0 + lane] = stg[r * 32 + lane];
+  }
 }
 
 struct PTile {
@@ -185,9 +210,11 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   const int nkb = static_cast<int>((K + P_BK - 1) / P_BK);
   const int nchunk = (nkb + P_KB_PER_CHUNK - 1) / P_KB_PER_CHUNK;
 
-  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // (pointer arithmetic on the shared array keeps the shared address space known to the compiler)
+  uint8_t* stages = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // after the ring: the SwiGLU exchange buffers, or the BF16 output staging
+  uint16_t* xch = reinterpret_cast<uint16_t*>(stages + STAGES * P_STAGE_BYTES);
   const uint32_t stage_base = smem_u32(stages);
-  uint16_t* xchbuf = reinterpret_cast<uint16_t*>(stages + STAGES * P_STAGE_BYTES);
   uint32_t rank, cluster_id, nclusters;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
   asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cluster_id));
@@ -373,6 +400,46 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     const uint32_t acce_even = smem_cluster_addr(smem_u32(&bar_acce[0]), 0);
     float* sxw = s_sx[ew];
     uint32_t acc_count = 0, ntile = 0;
+    // W13 + SwiGLU: the SwiGLU of a tile's tokens runs in slices before each chunk wait of the next tile
+    // (and what is left after its last chunk), so it overlaps that tile's MMAs instead of holding up the
+    // accumulator hand-over.  The tile whose SwiGLU is outstanding:
+    struct PendingSwiglu {
+      bool on = false;
+      int i = 0, nown = 0;       // next token of the 48, tokens with rows
+      uint32_t par = 0;          // the tile's exchange phase
+      int64_t row = 0, j = 0;    // first output row, this lane's channel
+      uint16_t* keep = nullptr;  // my kept values (h replaces them in place)
+      const uint16_t* other = nullptr;
+    } pd;
+    const bool sw_up = (q >= 2);
+    const int sw_pi = (q & 1) * 2 + h;
+    const int sw_slice = (P_XCH + nchunk - 1) / nchunk;
+    // SwiGLU of up to `budget` outstanding tokens; false when the CTA aborts.
+    auto swiglu_work = [&](int budget) -> bool {
+      if (!pd.on) return true;
+      if (pd.i == 0) {  // the partner's hand-over of that tile
+        int got = 0;
+        const uint32_t o_full = smem_u32(sw_up ? &bar_gfull[sw_pi] : &bar_ufull[sw_pi]);
+        if (lane == 0) got = mbar_wait(o_full, pd.par, &s_abort, a.status, 10u) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, got, 0)) return false;
+      }
+      const int end = min(P_XCH, pd.i + budget);
+#pragma unroll 4
+      for (int i = pd.i; i < end; ++i) {
+        const float mine = bf16_bits_to_f32(pd.keep[i * 32]);
+        const float theirs = bf16_bits_to_f32(pd.other[i * 32]);
+        pd.keep[i * 32] = sw_up ? swiglu_bf16(theirs, mine) : swiglu_bf16(mine, theirs);  // h, in place
+      }
+      pd.i = end;
+      if (pd.i == P_XCH) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sw_up ? &bar_gfree[sw_pi] : &bar_ufree[sw_pi]));
+        // h of my 48 tokens, [token][32 channels j], to 16-byte stores of 64-byte row pieces
+        store_rows(pd.keep - lane, static_cast<uint16_t*>(a.out), pd.row, N / 2, pd.j - lane, pd.nown, lane);
+        pd.on = false;
+      }
+      return true;
+    };
     for (int t = c0; t < units && !s_abort; t += cstep) {
       const PTile ti = p_decode(t, E, WB, s_unit_prefix, s_row_off);
       const int64_t rowh = ti.row0 + P_NHALF * h;                    // routed row of column 96h
@@ -387,6 +454,10 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
       for (int i = 0; i < P_NHALF; ++i) sums[i] = 0;
       bool ok = true;
       for (int c = 0; c < nchunk; ++c) {
+        if (MODE == EPI_SWIGLU && !swiglu_work(sw_slice)) {
+          ok = false;
+          break;
+        }
         const uint32_t b = acc_count & 1u;
         const uint32_t use = acc_count >> 1;
         int got = 0;
@@ -412,7 +483,10 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         ++acc_count;
       }
       if (!ok) break;
+      if (MODE == EPI_SWIGLU && !swiglu_work(P_XCH)) break;  // the previous tile's SwiGLU, all of what is left
 
+      // Results are computed first (register and shared-memory reads only) and stored afterwards, so the
+      // reads and the arithmetic of different tokens overlap instead of queueing behind each global store.
       const int64_t n = static_cast<int64_t>(ti.wb) * P_WROWS + static_cast<int64_t>(rank) * P_WHALF + n_loc;
       if constexpr (MODE == EPI_ACC) {
         if (n < N) {
@@ -422,86 +496,69 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             if (i < tv) dst[i * N] = sums[i];
         }
       } else if constexpr (MODE == EPI_BF16) {
-        if (n < N) {
-          const float sw = a.w_scale[static_cast<int64_t>(ti.e) * N + n];
-          const float bias = a.bias ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
-          const int32_t qb = a.qbias ? a.qbias[n] : 0;
-          uint16_t* dst = static_cast<uint16_t*>(a.out) + rowh * N + n;
+        const bool nin = n < N;
+        const float sw = nin ? a.w_scale[static_cast<int64_t>(ti.e) * N + n] : 0.0f;
+        const float bias = (nin && a.bias != nullptr) ? bf16_bits_to_f32(a.bias[n]) : 0.0f;
+        const int32_t qb = (nin && a.qbias != nullptr) ? a.qbias[n] : 0;
+        // through shared memory, [token][this warp's 32 channels], to 16-byte stores of 64-byte row pieces
+        uint16_t* stg = xch + ew * P_NHALF * 32;
 #pragma unroll
-          for (int i = 0; i < P_NHALF; ++i) {
-            if (i < tv) {
-              float f = a.qbias != nullptr ? dequant_q(sums[i], qb, sxw[i], sw) : dequant(sums[i], sxw[i], sw);
-              if (a.bias) f = __fadd_rn(f, bias);
-              dst[i * N] = f32_to_bf16_bits(f);
-            }
-          }
+        for (int i = 0; i < P_NHALF; ++i) {
+          float f = a.qbias != nullptr ? dequant_q(sums[i], qb, sxw[i], sw) : dequant(sums[i], sxw[i], sw);
+          if (a.bias) f = __fadd_rn(f, bias);
+          stg[i * 32 + lane] = f32_to_bf16_bits(f);
         }
+        __syncwarp();
+        store_rows(xch + ew * P_NHALF * 32, static_cast<uint16_t*>(a.out), rowh, N, n - lane, tv, lane);
+        __syncwarp();  // the staging buffer is read before the next tile writes it
       } else {  // EPI_SWIGLU: rows [0,64) of this CTA's half are gate channels, [64,128) the matching up channels
-        const int p = q & 1;
-        const bool up = q >= 2;
         const int64_t I = N / 2;
-        const int64_t j = (static_cast<int64_t>(ti.wb) * 2 + rank) * kGateUpBlock + 32 * p + lane;
-        const float swv = j < I ? a.w_scale[static_cast<int64_t>(ti.e) * N + (up ? I : 0) + j] : 0.0f;
-        const int pi = p * 2 + h;
-        uint16_t* gbuf = xchbuf + (pi * 2 + 0) * P_XCH * 32 + lane;  // gate -> up: gate of tokens [48, 96)
-        uint16_t* ubuf = xchbuf + (pi * 2 + 1) * P_XCH * 32 + lane;  // up -> gate: up of tokens [0, 48)
+        const int64_t j = (static_cast<int64_t>(ti.wb) * 2 + rank) * kGateUpBlock + 32 * (q & 1) + lane;
+        const float swv = j < I ? a.w_scale[static_cast<int64_t>(ti.e) * N + (sw_up ? I : 0) + j] : 0.0f;
+        // buffers of this pair: gate warp's hand-over (gate of tokens [48, 96)) and keep (gate of [0, 48)),
+        // up warp's hand-over (up of [0, 48)) and keep (up of [48, 96))
+        uint16_t* pair_buf = xch + sw_pi * 4 * P_XCH * 32 + lane;
+        uint16_t* give = pair_buf + (sw_up ? 2 : 0) * P_XCH * 32;
+        uint16_t* keep = pair_buf + (sw_up ? 3 : 1) * P_XCH * 32;
         const uint32_t par = ntile & 1u;
-        // my BF16 values of the tokens the other warp computes
-        const uint32_t b_free = smem_u32(up ? &bar_ufree[pi] : &bar_gfree[pi]);
-        const uint32_t b_full = smem_u32(up ? &bar_ufull[pi] : &bar_gfull[pi]);
+        // my BF16 values into the hand-over and keep buffers, once the partner has read the previous
+        // tile's hand-over (this warp's own SwiGLU of that tile is complete: it ran above)
         int got = 0;
+        const uint32_t b_free = smem_u32(sw_up ? &bar_ufree[sw_pi] : &bar_gfree[sw_pi]);
         if (lane == 0) got = mbar_wait(b_free, par ^ 1u, &s_abort, a.status, 9u) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, got, 0)) break;
-        // (the token offsets are compile-time constants in each branch, so sums[] stays in registers)
-        if (up) {
+        // gate warp: hands over tokens [48, 96), keeps [0, 48); up warp the other way round (compile-time
+        // offsets in each branch keep sums[] in registers)
+        if (sw_up) {
 #pragma unroll
           for (int i = 0; i < P_XCH; ++i) {
-            float v = 0.0f;
-            if (i < tv && j < I) v = dequant(sums[i], sxw[i], swv);
-            ubuf[i * 32] = f32_to_bf16_bits(v);
+            give[i * 32] = f32_to_bf16_bits(dequant(sums[i], sxw[i], swv));
+            keep[i * 32] = f32_to_bf16_bits(dequant(sums[P_XCH + i], sxw[P_XCH + i], swv));
           }
         } else {
 #pragma unroll
           for (int i = 0; i < P_XCH; ++i) {
-            float v = 0.0f;
-            if (P_XCH + i < tv && j < I) v = dequant(sums[P_XCH + i], sxw[P_XCH + i], swv);
-            gbuf[i * 32] = f32_to_bf16_bits(v);
+            give[i * 32] = f32_to_bf16_bits(dequant(sums[P_XCH + i], sxw[P_XCH + i], swv));
+            keep[i * 32] = f32_to_bf16_bits(dequant(sums[i], sxw[i], swv));
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_full);
-        // the other warp's values of my tokens, then SwiGLU and the store
-        const uint32_t o_full = smem_u32(up ? &bar_gfull[pi] : &bar_ufull[pi]);
-        const uint32_t o_free = smem_u32(up ? &bar_gfree[pi] : &bar_ufree[pi]);
-        if (lane == 0) got = mbar_wait(o_full, par, &s_abort, a.status, 10u) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, got, 0)) break;
-        if (j < I) {
-          if (up) {  // tokens [48, 96): gate from the gate warp, my up
-            uint16_t* dst = static_cast<uint16_t*>(a.out) + (rowh + P_XCH) * I + j;
-#pragma unroll
-            for (int i = 0; i < P_XCH; ++i) {
-              if (P_XCH + i < tv) {
-                const float u = bf16_round(dequant(sums[P_XCH + i], sxw[P_XCH + i], swv));
-                dst[static_cast<int64_t>(i) * I] = swiglu_bf16(bf16_bits_to_f32(gbuf[i * 32]), u);
-              }
-            }
-          } else {  // tokens [0, 48): my gate, up from the up warp
-            uint16_t* dst = static_cast<uint16_t*>(a.out) + rowh * I + j;
-#pragma unroll
-            for (int i = 0; i < P_XCH; ++i) {
-              if (i < tv) {
-                const float gt = bf16_round(dequant(sums[i], sxw[i], swv));
-                dst[static_cast<int64_t>(i) * I] = swiglu_bf16(gt, bf16_bits_to_f32(ubuf[i * 32]));
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
+        if (lane == 0) mbar_arrive(smem_u32(sw_up ? &bar_ufull[sw_pi] : &bar_gfull[sw_pi]));
+        // this tile's SwiGLU becomes the outstanding work of the next tile's chunks
+        const int own0 = sw_up ? P_XCH : 0;
+        pd.on = true;
+        pd.i = 0;
+        pd.nown = min(P_XCH, tv - own0);
+        pd.par = par;
+        pd.row = rowh + own0;
+        pd.j = j;
+        pd.keep = keep;
+        pd.other = pair_buf + (sw_up ? 0 : 2) * P_XCH * 32;
         ++ntile;
       }
       __syncwarp();  // the scales of this tile are read before the next tile overwrites them
     }
+    if (MODE == EPI_SWIGLU && !s_abort) swiglu_work(P_XCH);  // the last tile's SwiGLU
   }
 
   // ---- teardown: on abort, give in-flight copies and MMAs time to land first, then the pair leaves
@@ -550,12 +607,11 @@ cudaError_t launch_tcp_gemm(const GemmArgs& a, const void* a_f16, int num_sms, c
   const int64_t units = ((a.R + P_NT - 1) / P_NT + (a.group_list != nullptr ? a.E : 0)) * wb;
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / P_CLUSTER));
   const int grid = static_cast<int>(clusters * P_CLUSTER);
-  const size_t smem_sw = static_cast<size_t>(p_stages(EPI_SWIGLU)) * P_STAGE_BYTES + P_XCH_BYTES + 1024;
-  const size_t smem = static_cast<size_t>(p_stages(EPI_BF16)) * P_STAGE_BYTES + 1024;
+  auto smem = [](int mode) { return static_cast<size_t>(p_stages(mode)) * P_STAGE_BYTES + p_epi_bytes(mode) + 1024; };
   switch (a.mode) {
-    case EPI_ACC: return launch_tcp_mode<EPI_ACC>(mx, mw, a, grid, smem, stream);
-    case EPI_SWIGLU: return launch_tcp_mode<EPI_SWIGLU>(mx, mw, a, grid, smem_sw, stream);
-    default: return launch_tcp_mode<EPI_BF16>(mx, mw, a, grid, smem, stream);
+    case EPI_ACC: return launch_tcp_mode<EPI_ACC>(mx, mw, a, grid, smem(EPI_ACC), stream);
+    case EPI_SWIGLU: return launch_tcp_mode<EPI_SWIGLU>(mx, mw, a, grid, smem(EPI_SWIGLU), stream);
+    default: return launch_tcp_mode<EPI_BF16>(mx, mw, a, grid, smem(EPI_BF16), stream);
   }
 }
 
