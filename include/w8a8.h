@@ -243,7 +243,12 @@ W8A8_API w8a8_status w8a8_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint
  * activations), qw [N,K] E4M3 + sw [N,K/32] (of the weights) ->
  * y[m,n] = bf16( sum_g 2^(sa[m,g]-127) 2^(sw[n,g]-127) sum_{k in g} qa[m,k] qw[n,k] ),
  * accumulated in binary32 (so within a bound of the exact sum, not bit-exact).
- * K % 128 == 0; all pointers 16-byte aligned. */
+ * K % 128 == 0; all pointers 16-byte aligned.  With K % 512 == 0 and N % 8 == 0
+ * it runs on the block-scaled tensor cores (tcgen05 kind::mxf8f6f4, both
+ * scales applied inside the MMA; w8a8_last_engine() reports W8A8_ENGINE_TC),
+ * otherwise on the warp-level FP8 instruction (W8A8_ENGINE_WARP).  The call
+ * has no workspace, so an exhausted bounded wait on the tensor-core path
+ * (which only a stalled GPU produces) leaves y incomplete without a status. */
 W8A8_API w8a8_status w8a8_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
                                     const uint8_t* sw, int64_t N, uint16_t* y, w8a8_stream_t stream);
 

@@ -1,6 +1,8 @@
-"""GPU parity of the MXFP8 quantiser (through the C ABI): E4M3 codes and E8M0
-scales bit-exact against the oracle, over wide dynamic ranges, zero groups,
-BF16 subnormals, saturating groups and every finite BF16 value."""
+"""GPU parity of the MXFP8 path (through the C ABI): the quantiser's E4M3 codes
+and E8M0 scales bit-exact against the oracle, over wide dynamic ranges, zero
+groups, BF16 subnormals, saturating groups and every finite BF16 value; the
+contraction, on the block-scaled tensor cores and on the warp-level FP8
+instruction, within the binary32 accumulation bound of the exact result."""
 import numpy as np
 import pytest
 import torch
@@ -63,8 +65,10 @@ def mx_bound(qa, sa, qw, sw, y_ref):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (37, 200, 512), (128, 256, 1024), (300, 130, 384),
-                                   (64, 2048, 7168)])
+                                   (64, 2048, 7168), (300, 520, 1024), (193, 264, 2048), (16, 8, 512)])
 def test_mx_matmul_within_bound(M, N, K):
+    """Both engines: the block-scaled tensor cores for K % 512 == 0 and N % 8 == 0, else the warp-level
+    FP8 instruction."""
     rng = np.random.default_rng(M + N + K)
     xa = S.to_bf16_bits((rng.standard_normal((M, K)) * 2.0 ** rng.integers(-6, 6, (M, 1))).astype(np.float32))
     xw = S.to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
@@ -72,6 +76,7 @@ def test_mx_matmul_within_bound(M, N, K):
     qw, sw = oracle.mx_quant(xw)
     from gpu_helpers import dev
     y = W.w8a8_mx_matmul(dev(qa), dev(sa), dev(qw), dev(sw))
+    assert W.last_engine() == (W.ENGINE_TC if K % 512 == 0 and N % 8 == 0 else W.ENGINE_WARP)
     torch.cuda.synchronize()
     got = S.bf16_bits_to_f32(y.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
     y_ref = oracle.mx_matmul(qa, sa, qw, sw)

@@ -472,6 +472,11 @@ w8a8_status w8a8_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int6
   if (!aligned16(qa) || !aligned16(qw) || !aligned16(sa) || !aligned16(sw)) return W8A8_ERR_ALIGN;
   int sms = 0;
   if (w8a8_status s = device_info(sms)) return s;
+  if (mx_tc_supported(M, N, K)) {  // block-scaled tensor cores
+    t_last_engine = W8A8_ENGINE_TC;
+    return cuda_status(launch_mx_tc(qa, sa, M, K, qw, sw, N, y, nullptr, sms, reinterpret_cast<cudaStream_t>(stream)));
+  }
+  t_last_engine = W8A8_ENGINE_WARP;
   return cuda_status(launch_mx_matmul(qa, sa, M, K, qw, sw, N, y, reinterpret_cast<cudaStream_t>(stream)));
 }
 

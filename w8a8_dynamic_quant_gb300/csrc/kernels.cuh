@@ -58,9 +58,16 @@ cudaError_t launch_static_prepare(const int8_t* w, int64_t N, int64_t K, const f
 cudaError_t launch_mx_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint8_t* scale, cudaStream_t stream,
                             int num_sms);
 
-// MXFP8 contraction (mx.cu): E4M3 a [M,K] + E8M0 [M,K/32], E4M3 w [N,K] + E8M0 [N,K/32] -> bf16 y [M,N].
+// MXFP8 contraction (mx.cu): E4M3 a [M,K] + E8M0 [M,K/32], E4M3 w [N,K] + E8M0 [N,K/32] -> bf16 y [M,N],
+// on the warp-level FP8 instruction.
 cudaError_t launch_mx_matmul(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
                              const uint8_t* sw, int64_t N, uint16_t* y, cudaStream_t stream);
+// The same on the block-scaled tensor cores (mx_tc.cu, CTA pairs, tcgen05 kind::mxf8f6f4) for the shapes
+// mx_tc_supported() accepts (K % 512 == 0, N % 8 == 0).  status may be nullptr.
+bool mx_tc_supported(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_mx_tc(const uint8_t* qa, const uint8_t* sa, int64_t M, int64_t K, const uint8_t* qw,
+                         const uint8_t* sw, int64_t N, uint16_t* y, DeviceStatus* status, int num_sms,
+                         cudaStream_t stream);
 
 // Epilogue of the contraction.
 enum EpiMode : int {
