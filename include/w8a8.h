@@ -279,9 +279,11 @@ W8A8_API w8a8_status moe_w13_swiglu_requant_w2(const void* x, const float* x_sca
 
 /* Offsets (bytes from ws) of the MoE intermediates kept in the workspace after
  * a call: 0 xq int8 [R,H], 1 xs fp32 [R], 2 h bf16 [R,I], 3 hq int8 [R,I],
- * 4 hs fp32 [R], and on shapes the tensor-core engine takes 5 xq as fp16
- * [R,H] and 6 hq as fp16 [R,I].  Returns -1 for an unknown index or a copy the
- * shape does not keep.  (Validation aid.) */
+ * 4 hs fp32 [R], 5 xq as fp16 [R,H], 6 hq as fp16 [R,I].  The codes are kept
+ * in the form the contraction reads: int8 (0, 3) on shapes the warp engine
+ * takes, integer-valued fp16 (5, 6) on shapes a tensor-core engine takes
+ * (R >= 64 * E).  Returns -1 for an unknown index or a copy the shape does not
+ * keep.  (Validation aid.) */
 W8A8_API int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int which);
 
 /* ------------------------------------------------------------------------ */

@@ -319,7 +319,11 @@ def test_moe_configs_sampled_rows(cfg, n_rows):
     rows = sample_rows(m.R, n_rows, seed=cfg)
     y_ref, it = moe_subset_oracle(m, rows)
     assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I))[rows], it["h"])
-    assert np.array_equal(ws_slice(ws, m, 3, np.int8, (m.R, m.I))[rows], it["hq"])
+    if W.moe_workspace_offset(m.R, m.H, m.I, m.E, 3) >= 0:
+        hq = ws_slice(ws, m, 3, np.int8, (m.R, m.I))
+    else:  # tensor-core shapes keep the codes as integer-valued fp16 only
+        hq = ws_slice(ws, m, 6, np.float16, (m.R, m.I)).astype(np.int8)
+    assert np.array_equal(hq[rows], it["hq"])
     assert np.array_equal(y[rows], y_ref)
     # every routed row was written (no row left at the workspace's initial state)
     assert int(np.count_nonzero(np.all(y == 0, axis=1))) == 0

@@ -139,8 +139,15 @@ def tc_moe(m, f16_copy=True):
 
 def ws_slice(ws, m, which, dtype, shape):
     off = W.moe_workspace_offset(m.R, m.H, m.I, m.E, which)
+    assert off >= 0, f"workspace item {which} is not kept for this shape"
     n = int(np.prod(shape)) * np.dtype(dtype).itemsize
     return ws[off:off + n].cpu().numpy().view(dtype).reshape(shape)
+
+
+def hq_codes(ws, m):
+    """The requantised h: on tensor-core shapes the workspace keeps only its integer-valued fp16 copy."""
+    assert W.moe_workspace_offset(m.R, m.H, m.I, m.E, 3) == -1
+    return ws_slice(ws, m, 6, np.float16, (m.R, m.I)).astype(np.int8)
 
 
 @pytest.mark.parametrize("prequant", [False, True])
@@ -152,8 +159,11 @@ def test_tc_moe_small_full(prequant, f16_copy):
     y_ref, it = oracle.moe_w13_swiglu_requant_w2(m.x, m.x_scale, m.group_list, m.w13.numpy(), m.s13,
                                                  m.w2.numpy(), m.s2, intermediates=True)
     assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I)), it["h"])
-    assert np.array_equal(ws_slice(ws, m, 3, np.int8, (m.R, m.I)), it["hq"])
+    assert np.array_equal(hq_codes(ws, m), it["hq"])
     assert np.array_equal(f32_bits(ws_slice(ws, m, 4, np.float32, (m.R,))), f32_bits(it["hs"]))
+    if m.x_scale is None:  # the routed rows' codes, quantised once
+        assert W.moe_workspace_offset(m.R, m.H, m.I, m.E, 0) == -1
+        assert np.array_equal(ws_slice(ws, m, 5, np.float16, (m.R, m.H)).astype(np.int8), it["xq"])
     assert np.array_equal(y, y_ref)
 
 
@@ -164,4 +174,5 @@ def test_tc_moe_prefill_config_sampled_rows(f16_copy):
     rows = sample_rows(m.R, 24, seed=9)
     y_ref, it = moe_subset_oracle(m, rows)
     assert np.array_equal(ws_slice(ws, m, 2, np.uint16, (m.R, m.I))[rows], it["h"])
+    assert np.array_equal(hq_codes(ws, m)[rows], it["hq"])
     assert np.array_equal(y[rows], y_ref)

@@ -149,16 +149,19 @@ struct MoeWs {
   size_t xq, xs, h, hq, hs, xq16, hq16, gemm, total;
   GemmWs g;
 };
+// The codes of the routed rows and of h: int8 for the warp engine, or on shapes the tensor-core engines
+// take only as the integer-valued fp16 they read (xq16, hq16; xq and hq are then 0: not kept).
 MoeWs moe_layout(int64_t R, int64_t H, int64_t I, int64_t E) {
   MoeWs L;
+  const bool tc = tc_shape(E, R);
   size_t off = kStatusBytes;
-  L.xq = off; off = align_up(off + static_cast<uint64_t>(R) * H, 256);
+  L.xq = L.hq = L.xq16 = L.hq16 = 0;
+  if (!tc) { L.xq = off; off = align_up(off + static_cast<uint64_t>(R) * H, 256); }
   L.xs = off; off = align_up(off + static_cast<uint64_t>(R) * 4, 256);
   L.h = off;  off = align_up(off + static_cast<uint64_t>(R) * I * 2, 256);
-  L.hq = off; off = align_up(off + static_cast<uint64_t>(R) * I, 256);
+  if (!tc) { L.hq = off; off = align_up(off + static_cast<uint64_t>(R) * I, 256); }
   L.hs = off; off = align_up(off + static_cast<uint64_t>(R) * 4, 256);
-  L.xq16 = L.hq16 = 0;
-  if (tc_shape(E, R)) {  // fp16 copies of the int8 codes for the tcgen05 engine
+  if (tc) {
     L.xq16 = off; off = align_up(off + static_cast<uint64_t>(R) * H * 2, 256);
     L.hq16 = off; off = align_up(off + static_cast<uint64_t>(R) * I * 2, 256);
   }
@@ -250,7 +253,7 @@ w8a8_status moe_chain(const void* x, const float* x_scale, bool x16_ready, const
   const int8_t* xq = static_cast<const int8_t*>(x);
   const float* xs = x_scale;
   uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
-  int8_t* hq = reinterpret_cast<int8_t*>(b + L.hq);
+  int8_t* hq = L.hq ? reinterpret_cast<int8_t*>(b + L.hq) : nullptr;  // warp engine only
   float* hs = reinterpret_cast<float*>(b + L.hs);
   // tensor-core engines for shapes that take them: the packed fp16 weight copies when both packs carry
   // them, else the int8 weights widened in tensor memory
@@ -262,10 +265,10 @@ w8a8_status moe_chain(const void* x, const float* x_scale, bool x16_ready, const
   uint16_t* hq16 = tc ? reinterpret_cast<uint16_t*>(b + L.hq16) : nullptr;
 
   if (x_scale == nullptr) {  // BF16 input: quantise once; an INT8 input with its scale is used as is
-    int8_t* q = reinterpret_cast<int8_t*>(b + L.xq);
     float* s = reinterpret_cast<float*>(b + L.xs);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    const cudaError_t e = tc ? launch_dynamic_quant_dual(xb, R, H, q, xq16, s, st, sms)
+    int8_t* q = tc ? nullptr : reinterpret_cast<int8_t*>(b + L.xq);
+    const cudaError_t e = tc ? launch_dynamic_quant_f16(xb, R, H, xq16, s, st, sms)
                              : launch_dynamic_quant(xb, R, H, q, s, st, sms);
     if (e != cudaSuccess) return W8A8_ERR_CUDA;
     xq = q;
@@ -294,7 +297,7 @@ w8a8_status moe_chain(const void* x, const float* x_scale, bool x16_ready, const
                              : launch_reg_gemm(a13, plan_reg_gemm(a13, sms), st);
   if (e13 != cudaSuccess) return W8A8_ERR_CUDA;
 
-  const cudaError_t eq = tc ? launch_dynamic_quant_dual(h, R, I, hq, hq16, hs, st, sms)
+  const cudaError_t eq = tc ? launch_dynamic_quant_f16(h, R, I, hq16, hs, st, sms)
                             : launch_dynamic_quant(h, R, I, hq, hs, st, sms);
   if (eq != cudaSuccess) return W8A8_ERR_CUDA;
 
@@ -572,10 +575,10 @@ int64_t moe_workspace_offset(int64_t R, int64_t H, int64_t I, int64_t E, int whi
   if (R < 0 || H <= 0 || I <= 0 || E <= 0) return -1;
   const MoeWs L = moe_layout(R, H, I, E);
   switch (which) {
-    case 0: return static_cast<int64_t>(L.xq);
+    case 0: return L.xq ? static_cast<int64_t>(L.xq) : -1;
     case 1: return static_cast<int64_t>(L.xs);
     case 2: return static_cast<int64_t>(L.h);
-    case 3: return static_cast<int64_t>(L.hq);
+    case 3: return L.hq ? static_cast<int64_t>(L.hq) : -1;
     case 4: return static_cast<int64_t>(L.hs);
     case 5: return L.xq16 ? static_cast<int64_t>(L.xq16) : -1;
     case 6: return L.hq16 ? static_cast<int64_t>(L.hq16) : -1;
@@ -697,7 +700,7 @@ w8a8_status moe_layer(const void* x, const float* x_scale, const int64_t* topk_i
   const int kk = static_cast<int>(k);
   int64_t* gl = reinterpret_cast<int64_t*>(b + L.group_list);
   int32_t* pos = reinterpret_cast<int32_t*>(b + L.pos);
-  int8_t* xq = reinterpret_cast<int8_t*>(b + L.m.xq);
+  int8_t* xq = L.m.xq ? reinterpret_cast<int8_t*>(b + L.m.xq) : nullptr;  // warp engine only
   float* xs = reinterpret_cast<float*>(b + L.m.xs);
   uint16_t* xq16 = L.m.xq16 ? reinterpret_cast<uint16_t*>(b + L.m.xq16) : nullptr;
   uint16_t* yr = reinterpret_cast<uint16_t*>(b + L.y_routed);

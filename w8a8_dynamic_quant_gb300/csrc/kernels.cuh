@@ -25,9 +25,9 @@ cudaError_t launch_quant_pack(const uint16_t* w, int64_t E, int64_t N, int64_t K
 
 cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* scale,
                                  cudaStream_t stream, int num_sms);
-// int8 codes and the same codes as integer-valued fp16 (operand of the tcgen05 engine)
-cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
-                                      float* scale, cudaStream_t stream, int num_sms);
+// the codes as integer-valued fp16 only (the operand the tcgen05 engines read)
+cudaError_t launch_dynamic_quant_f16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q_f16, float* scale,
+                                     cudaStream_t stream, int num_sms);
 
 // MoE routing permute: token row m of x [T,H] quantised once, its codes and scale written to the
 // routed rows dst[m*k + j] (j < k; an index < 0 is skipped).  out: 0 int8 into q, 1 fp16 into q_f16,

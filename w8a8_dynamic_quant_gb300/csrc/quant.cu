@@ -343,9 +343,9 @@ cudaError_t launch_dynamic_quant(const uint16_t* x, int64_t M, int64_t K, int8_t
   return launch_quant_t<0>(x, M, K, q, nullptr, scale, RowId{}, stream, num_sms);
 }
 
-cudaError_t launch_dynamic_quant_dual(const uint16_t* x, int64_t M, int64_t K, int8_t* q, uint16_t* q_f16,
-                                      float* scale, cudaStream_t stream, int num_sms) {
-  return launch_quant_t<2>(x, M, K, q, q_f16, scale, RowId{}, stream, num_sms);
+cudaError_t launch_dynamic_quant_f16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q_f16, float* scale,
+                                     cudaStream_t stream, int num_sms) {
+  return launch_quant_t<1>(x, M, K, nullptr, q_f16, scale, RowId{}, stream, num_sms);
 }
 
 cudaError_t launch_quant_scatter(const uint16_t* x, int64_t T, int64_t H, const int32_t* dst, int k, int8_t* q,
