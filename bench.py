@@ -71,10 +71,11 @@ def weight_read_bound_ms(active_params: float, bytes_per_param: float, n_gpus: i
 # only while these files are unchanged)
 KERNEL_SOURCES = {
     "dynamic_quant": ["quant.cu", "common.cuh", "kernels.cuh"],
-    "quant_matmul": ["gemm_reg.cu", "gemm_dec.cu", "gemm_tc.cu", "tc_common.cuh", "capi.cu", "common.cuh",
-                     "kernels.cuh"],
-    "moe_layer": ["gemm_reg.cu", "gemm_tc.cu", "gemm_tcw.cu", "tc_common.cuh", "quant.cu", "route.cu", "capi.cu",
+    "quant_matmul": ["gemm_reg.cu", "gemm_dec.cu", "gemm_tc.cu", "gemm_tcp.cu", "tc_common.cuh", "capi.cu",
+                     "common.cuh", "kernels.cuh"],
+    "moe_layer": ["gemm_reg.cu", "gemm_tc.cu", "gemm_tcp.cu", "tc_common.cuh", "quant.cu", "route.cu", "capi.cu",
                   "common.cuh", "kernels.cuh"],
+    "mx_matmul": ["mx.cu", "mx_tc.cu", "tc_common.cuh", "capi.cu", "common.cuh", "kernels.cuh"],
 }
 
 
@@ -827,6 +828,31 @@ class _HostMoETokens(MoETokens):
         self.step_rows = 1  # tokens (each with topk routed rows)
 
 
+def int8_tensor_reference(torch, device, n: int = 8192, reps: int = 5):
+    """Throughput of the INT8 tensor-core path the libraries expose (torch._int_mm: cuBLASLt INT8 x INT8 ->
+    INT32) on an n^3 GEMM, best of `reps`, in TOPS.  The library's exact engines feed integer-valued FP16 to
+    the FP16 tensor instruction instead (sm_103a has no integer tcgen05 kind), so this is the INT8 rate the
+    metric's "% INT8 peak" refers to, not the roof of those engines."""
+    try:
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device).t()
+        torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._int_mm(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return {"tops": 2.0 * n ** 3 / (best / 1e3) / 1e12, "how": f"torch._int_mm int8 {n}^3, best of {reps}"}
+    except Exception as e:  # an INT8 library path the installed torch lacks
+        return {"tops": None, "how": f"unavailable: {type(e).__name__}"}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -955,6 +981,12 @@ def run_gpu(args):
                 "alg_bytes_per_launch": wl.alg_bytes[dom],
                 "per_kernel_us": {k: v * 1e3 for k, v in per_kernel_ms.items()},
                 "sum_of_kernels_us": sum(per_kernel_ms[k] for k in step_kernels) * 1e3}
+    if wl.bound == "tensor" and not args.quick:
+        # the metric's "% INT8 peak": the INT8 tensor-core path of the libraries on this GPU, measured here
+        int8 = int8_tensor_reference(torch, device)
+        roofline["int8_reference"] = int8
+        if int8.get("tops"):
+            roofline["frac_of_int8_reference"] = achieved / int8["tops"]
     if "dynamic_quant" in per_kernel_ms:
         roofline["quant_gbs"] = wl.alg_bytes["dynamic_quant"] / (per_kernel_ms["dynamic_quant"] / 1e3) / 1e9
     if dom in wl.alg_flops:

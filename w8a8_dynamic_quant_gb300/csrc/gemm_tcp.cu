@@ -157,20 +157,27 @@ struct PTile {
   int64_t row0;  // first routed row of the block
 };
 
-// Work unit t -> (expert, 256-row weight block, token block); the token block varies fastest, so the pairs
-// in flight share a weight block and the expert's token rows stay in L2 while the weight blocks sweep past.
+// Work unit t -> (expert, 256-row weight block, token block), rasterised in groups of up to P_GROUP_W weight
+// blocks: inside a group the weight block varies fastest, then the token block.  The pairs in flight then
+// work on a few token blocks against the group's weight blocks, which stay in L2 while the expert's token
+// blocks sweep past them, and each token block is fetched from HBM about once per group.  (With the token
+// block fastest over a whole expert, the dense prefill shape read its 126 MB of operands 7 times from DRAM:
+// the output writes pushed the activations out of L2 between weight blocks.)
+constexpr int P_GROUP_W = 16;
 __device__ __forceinline__ PTile p_decode(int t, int E, int WB, const int* s_unit_prefix, const int* s_row_off) {
   PTile ti;
   ti.e = expert_of(t, E, s_unit_prefix);
   const int local = t - s_unit_prefix[ti.e];
   ti.cnt = s_row_off[ti.e + 1] - s_row_off[ti.e];
   const int TB = (ti.cnt + P_NT - 1) / P_NT;
-  ti.wb = local / TB;
-  ti.tb = local - ti.wb * TB;
+  const int g = local / (TB * P_GROUP_W);
+  const int rem = local - g * TB * P_GROUP_W;
+  const int gw = min(P_GROUP_W, WB - g * P_GROUP_W);
+  ti.tb = rem / gw;
+  ti.wb = g * P_GROUP_W + rem % gw;
   ti.tvalid = min(P_NT, ti.cnt - ti.tb * P_NT);
   ti.n_eff = (ti.tvalid + 15) & ~15;
   ti.row0 = static_cast<int64_t>(s_row_off[ti.e]) + static_cast<int64_t>(ti.tb) * P_NT;
-  (void)WB;
   return ti;
 }
 

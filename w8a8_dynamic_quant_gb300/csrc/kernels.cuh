@@ -113,9 +113,6 @@ cudaError_t launch_reg_gemm(const GemmArgs& a, const GemmPlan& p, cudaStream_t s
 // tcgen05 engine (large M): both operands as integer-valued fp16, K-major.
 // a_f16: [R,K] activations; b_f16: [E*N,K] packed weights (fp16 copy).
 cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream);
-// tcgen05 engine for grouped contractions: int8 weights (the packed payload) widened in TMEM as the A
-// operand, a_f16: [R,K] activations as fp16 (B operand).
-cudaError_t launch_tcw_gemm(const GemmArgs& a, const void* a_f16, int num_sms, cudaStream_t stream);
 // tcgen05 engine on CTA pairs for large M, dense or grouped: int8 weights (the packed payload) widened in
 // TMEM as the M = 256 side, a_f16: [R,K] activations as fp16 (the N side, up to 192 tokens per tile).
 cudaError_t launch_tcp_gemm(const GemmArgs& a, const void* a_f16, int num_sms, cudaStream_t stream);
