@@ -119,12 +119,11 @@ cudaError_t launch_tcp_gemm(const GemmArgs& a, const void* a_f16, int num_sms, c
 cudaError_t launch_s8_to_f16(const int8_t* src, uint16_t* dst, int64_t n, cudaStream_t stream, int num_sms);
 
 // tcgen05 decode engine (dense, M <= 64): int8 weights widened into TMEM, K
-// split over clusters of CTAs whose partials meet in distributed shared memory
-// and, across clusters, in workspace slots.
-// dec_plan returns ksplit 0 when the shape does not suit it.
+// split over CTAs whose exact int32 partials are added into a per-row-block
+// sum tile in the workspace (bulk reduce-add); the last CTA to arrive applies
+// the epilogue.  dec_plan returns ksplit 0 when the shape does not suit it.
 struct DecPlan {
-  int ksplit = 0;   // K splits per 128-row weight block
-  int cluster = 0;  // CTAs per cluster (consecutive K splits)
+  int ksplit = 0;  // K splits per 128-row weight block
 };
 size_t dec_ws_bytes(int64_t N);
 DecPlan dec_plan(int64_t M, int64_t N, int64_t K, int num_sms);
