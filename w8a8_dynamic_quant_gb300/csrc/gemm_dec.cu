@@ -114,23 +114,6 @@ __device__ __forceinline__ void issue_activations(const CUtensorMap* xmap, uint6
 // pdl_wait, and every global write of this kernel follows that wait (through
 // the activation tiles the whole computation waits for).
 
-// One MMA of the stage loop, issued by one elected lane of the (converged) MMA warp.
-__device__ __forceinline__ void mma_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(kIdescDec), "r"(accumulate)
-      : "memory");
-}
-// Completion of the MMAs issued so far by the elected lane, signalled on an mbarrier (the same election
-// as in mma_elect: the full warp elects the same lane).
-__device__ __forceinline__ void commit_elect(uint32_t mbar) {
-  asm volatile(
-      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(mbar)
-      : "memory");
-}
-
 // The partial tile (shared memory) added into the row block's sum tile (global) by the bulk copy engine.
 __device__ __forceinline__ void bulk_reduce_add_s32(int32_t* dst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.s32 [%0], [%1], %2;"
@@ -231,17 +214,16 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
     __syncwarp();
     // ------------------------------------------------------------- MMA issuer (whole warp)
     for (int i = 0; i < my; ++i) {
-      const int got = mbar_wait(smem_u32(&bar_ready[i]), 0u, &s_abort, a.status, 12u) ? 1 : 0;
-      if (!__all_sync(0xffffffffu, got)) break;
+      if (!warp_wait(smem_u32(&bar_ready[i]), 0u, &s_abort, a.status, 12u)) break;
       tc_fence_after();
       const uint64_t bdesc0 = smem_desc_sw128(btiles_base + i * DC_B_BYTES);
 #pragma unroll
       for (int kk = 0; kk < DC_BK / 16; ++kk)
-        mma_elect(tmem_base + DC_D_COL, tmem_base + i * DC_A_COLS + 8u * kk,
-                  bdesc0 + static_cast<uint64_t>((kk >> 2) * (DC_B_SUB >> 4) + 2 * (kk & 3)),
-                  (i > 0 || kk > 0) ? 1u : 0u);
+        tc_mma_tmem_a(tmem_base + DC_D_COL, tmem_base + i * DC_A_COLS + 8u * kk,
+                      bdesc0 + static_cast<uint64_t>((kk >> 2) * (DC_B_SUB >> 4) + 2 * (kk & 3)), kIdescDec,
+                      (i > 0 || kk > 0) ? 1u : 0u);
     }
-    commit_elect(smem_u32(&bar_accf));
+    tc_commit(smem_u32(&bar_accf));
   } else if (run) {
     // ------------------------------------------------ converters, then the partial tile
     const int q = warp & 3;            // TMEM lane quadrant

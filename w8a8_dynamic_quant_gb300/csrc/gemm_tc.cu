@@ -19,7 +19,7 @@
 // Data movement.  Both operands are K-major FP16 tiles brought in by TMA
 // (cp.async.bulk.tensor, 128-byte swizzle) into a 4-stage ring: A = 128
 // activation rows x 64 K, B = 256 weight rows x 64 K (48 KB per stage).  One
-// elected thread issues tcgen05.mma M=128 N=256 K=16 four times per stage.
+// elected lane of the MMA warp issues tcgen05.mma M=128 N=256 K=16 four times per stage.
 //
 // Clusters of two CTAs.  The CTAs of a cluster are scheduled together and
 // work on neighbouring tiles that share one operand: for m-blocks 2p and
@@ -358,8 +358,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------- MMA issuer (whole warp, elected lane)
+    {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_count = 0;
@@ -367,13 +367,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int c = 0; c < nchunk && !s_abort; ++c) {
           const uint32_t b = acc_count & 1u;
           const uint32_t use = acc_count >> 1;
-          if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+          if (!warp_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * TC_BN;
           const int kb_end = min(nkb, (c + 1) * TC_KB_PER_CHUNK);
           bool ok = true;
           for (int kb = c * TC_KB_PER_CHUNK; kb < kb_end; ++kb) {
-            if (!mbar_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
+            if (!warp_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
               ok = false;
               break;
             }
@@ -609,8 +609,8 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer (even CTA)
-    if (lane == 0 && rank == 0) {
+    // ------------------------------------------------------------- MMA issuer (even CTA, whole warp)
+    if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_count = 0;
@@ -618,13 +618,13 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int c = 0; c < nchunk && !s_abort; ++c) {
           const uint32_t b = acc_count & 1u;
           const uint32_t use = acc_count >> 1;
-          if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+          if (!warp_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * TC_BN;
           const int kb_end = min(nkb, (c + 1) * TC_KB_PER_CHUNK);
           bool ok = true;
           for (int kb = c * TC_KB_PER_CHUNK; kb < kb_end; ++kb) {
-            if (!mbar_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
+            if (!warp_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
               ok = false;
               break;
             }

@@ -43,7 +43,7 @@
 // Synchronisation.  TMA: each CTA's weight tile completes on its own barrier
 // (its converters wait for it); both CTAs' token tiles complete on the even
 // CTA's barrier.  Converters of both CTAs arrive on the even CTA's A-buffer
-// barrier once per stage; the even CTA's MMA thread issues tcgen05.mma.cta_group::2
+// barrier once per stage; the even CTA's MMA warp (one elected lane) issues tcgen05.mma.cta_group::2
 // M = 256 N = 16..192 K = 16 and frees shared-memory stages (with their A
 // slots) and accumulators in both CTAs by multicast commits.  Both CTAs'
 // epilogue warps release an accumulator on the even CTA's barrier.
@@ -115,15 +115,16 @@ __device__ __forceinline__ uint32_t idesc_pair(int n) {
 
 // D(tmem, both CTAs) (+)= A(tmem, both CTAs) * B(smem desc, both CTAs), kind::f16 on a CTA pair: each CTA's
 // tensor memory holds its 128 rows of A (K packed two fp16 per column) and of D; B rows [0,N/2) in the even
-// CTA, [N/2,N) in the odd one.  Issued by one thread of the even CTA.
+// CTA, [N/2,N) in the odd one.
+// Issued by the elected lane of the (converged) MMA warp, as the issue helpers of tc_common.cuh.
 __device__ __forceinline__ void tc_mma_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                    uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
 // 16 int8 (one 16-byte chunk) -> 8 words of fp16 pairs.
 __device__ __forceinline__ void widen16(const uint4& x, uint32_t* h) {
   s8x4_to_f16x4(x.x, h[0], h[1]);
@@ -314,8 +315,8 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer (even CTA)
-    if (lane == 0 && rank == 0) {
+    // ------------------------------------------------------------- MMA issuer (even CTA, whole warp)
+    if (rank == 0) {
       uint32_t g = 0;  // stages consumed so far: ring index g % STAGES, A buffer g % 2
       uint32_t acc_count = 0;
       for (int t = c0; t < units && !s_abort; t += cstep) {
@@ -325,14 +326,14 @@ tcp_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         for (int c = 0; c < nchunk && ok; ++c) {
           const uint32_t b = acc_count & 1u;
           const uint32_t use = acc_count >> 1;
-          if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+          if (!warp_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + p_acc_col(b);
           const int kb_end = min(nkb, (c + 1) * P_KB_PER_CHUNK);
           for (int kb = c * P_KB_PER_CHUNK; kb < kb_end && ok; ++kb, ++g) {
             const int stage = static_cast<int>(g % STAGES);
-            if (!mbar_wait(smem_u32(&bar_xfull[stage]), (g / STAGES) & 1u, &s_abort, a.status, 3u) ||
-                !mbar_wait(smem_u32(&bar_aready[g & 1u]), (g >> 1) & 1u, &s_abort, a.status, 6u)) {
+            if (!warp_wait(smem_u32(&bar_xfull[stage]), (g / STAGES) & 1u, &s_abort, a.status, 3u) ||
+                !warp_wait(smem_u32(&bar_aready[g & 1u]), (g >> 1) & 1u, &s_abort, a.status, 6u)) {
               ok = false;
               break;
             }

@@ -95,11 +95,12 @@ __device__ __forceinline__ uint32_t idesc_mx(int n, uint32_t kb) {
          (static_cast<uint32_t>(X_WROWS >> 4) << 24) | (kb << 29);
 }
 
+// Issued by the elected lane of the (converged) MMA warp, as the issue helpers of tc_common.cuh.
 __device__ __forceinline__ void tc_mma_pair_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %6, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
@@ -252,22 +253,22 @@ mx_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer (even CTA)
-    if (lane == 0 && rank == 0) {
+    // ------------------------------------------------------------- MMA issuer (even CTA, whole warp)
+    if (rank == 0) {
       uint32_t g = 0, acc_count = 0;
       bool ok = true;
       for (int t = c0; t < units && ok && !s_abort; t += cstep) {
         const XTile ti = x_decode(t, TB, M);
         const uint32_t b = acc_count & 1u;
         const uint32_t use = acc_count >> 1;
-        if (!mbar_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
+        if (!warp_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + x_acc_col(b);
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int stage = static_cast<int>(g % X_STAGES);
           const int slot = static_cast<int>(g % X_SF_SLOTS);
-          if (!mbar_wait(smem_u32(&bar_full[stage]), (g / X_STAGES) & 1u, &s_abort, a.status, 3u) ||
-              !mbar_wait(smem_u32(&bar_sfready[slot]), (g / X_SF_SLOTS) & 1u, &s_abort, a.status, 6u)) {
+          if (!warp_wait(smem_u32(&bar_full[stage]), (g / X_STAGES) & 1u, &s_abort, a.status, 3u) ||
+              !warp_wait(smem_u32(&bar_sfready[slot]), (g / X_SF_SLOTS) & 1u, &s_abort, a.status, 6u)) {
             ok = false;
             break;
           }
