@@ -17,6 +17,8 @@
 // Each row is read once with 16-byte vector loads and held in registers
 // between the absmax pass and the quantise pass; absmax is reduced with warp
 // shuffles (and shared memory across the warps of a CTA).
+#include <type_traits>
+
 #include "kernels.cuh"
 
 namespace w8a8 {
@@ -44,23 +46,43 @@ constexpr float kRoundMagic = 12582912.0f;
 // half-integer both lie strictly inside the same rounding interval and round to the same integer, with
 // |code| <= 127 (|y| <= 127 * (1 + 2^-22)); otherwise (rare), and for non-finite y, the whole chunk
 // takes the quotient itself and the clamp.
+// Two binary32 values in one 64-bit register, for the paired instructions below (each lane of
+// mul/add/fma.rn.f32x2 is the correctly rounded binary32 operation of its own operands).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 __device__ __forceinline__ void codes8(const uint4& v, float s, float rs, float (&m)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float x[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+  const uint64_t rs2 = pk2(rs, rs), mg2 = pk2(kRoundMagic, kRoundMagic), nmg2 = pk2(-kRoundMagic, -kRoundMagic),
+                 neg1 = pk2(-1.0f, -1.0f);
   float dmax = 0.0f;  // max |y - rint(y)| over the chunk; NaN if any y is not finite
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float y = __fmul_rn(x[e], rs);
-    m[e] = __fadd_rn(y, kRoundMagic);
-    const float t = __fsub_rn(y, __fsub_rn(m[e], kRoundMagic));  // y - rint(y), exact
-    asm("max.NaN.f32 %0, %0, %1;" : "+f"(dmax) : "f"(fabsf(t)));
+  for (int i = 0; i < 4; ++i) {  // elements 2i, 2i+1 side by side
+    const uint64_t x2 = pk2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    uint64_t y2, m2, r2, t2;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y2) : "l"(x2), "l"(rs2));         // y = x * rs
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(m2) : "l"(y2), "l"(mg2));         // m = y + magic
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r2) : "l"(m2), "l"(nmg2));        // rint(y), exact
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t2) : "l"(r2), "l"(neg1), "l"(y2));  // y - rint(y), exact
+    float t0, t1;
+    upk2(t2, t0, t1);
+    upk2(m2, m[2 * i], m[2 * i + 1]);
+    asm("max.NaN.f32 %0, %0, %1;" : "+f"(dmax) : "f"(fabsf(t0)));
+    asm("max.NaN.f32 %0, %0, %1;" : "+f"(dmax) : "f"(fabsf(t1)));
   }
   if (__builtin_expect(!(dmax < 0.5f - 0x1p-14f), 0)) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int r = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], s))));
@@ -147,6 +169,15 @@ __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_
     if (OUT != 0) reinterpret_cast<uint4*>(q16 + r * K)[idx] = f;
   }
 }
+// The same for a plain row (one destination, row m of the output) whose output rows were located once:
+// q8 / q16r point at chunk 0 of the row.
+template <int OUT>
+__device__ __forceinline__ void store8_row(const uint4& v, float s, float rs, int64_t idx, uint2* q8, uint4* q16r) {
+  float m[8];
+  codes8(v, s, rs, m);
+  if constexpr (OUT != 1) q8[idx] = pack_i8(m);
+  if constexpr (OUT != 0) q16r[idx] = pack_f16(m);
+}
 
 template <class D>
 __device__ __forceinline__ void store_scale(float s, int64_t row, float* scale, const D& d) {
@@ -173,82 +204,69 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// One row per warp; CH 16-byte chunks per lane (K <= 256 * CH).  At least four CTAs (32 warps, 32 rows of
-// loads in flight) per SM.
-template <int CH, int OUT, class D>
-__global__ void __launch_bounds__(256, 4) quant_warp_rows(const uint16_t* __restrict__ x, int64_t M,
-                                                       int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                       float* __restrict__ scale, D d) {
+// Rows in groups of G warps (32 G threads per row), CH 16-byte chunks of 8 bf16 per thread (K <= 256 G CH).
+// A CTA of 256 threads holds 8 / G groups; group g of CTA b takes rows b (8/G) + g, then every
+// gridDim.x (8/G) rows.  The loads of a group's next row are issued before its current row is reduced
+// and quantised, so an SM keeps reading while it computes.  absmax: warp shuffles, then (G > 1) the
+// group's warps meet in shared memory behind a named barrier of the group alone.  G is chosen so that
+// each thread holds about 64 elements of its row: the per-row work (the reduction, the binary32 divide
+// and reciprocal) is then a small part of the per-element work.
+template <int CH, int G, int OUT, class D>
+__global__ void __launch_bounds__(256, (CH <= 2 ? 4 : 2)) quant_rows(const uint16_t* __restrict__ x, int64_t M,
+                                                                   int64_t K, void* __restrict__ q,
+                                                                   uint16_t* __restrict__ q16,
+                                                                   float* __restrict__ scale, D d) {
   pdl_enter();
+  constexpr int NG = 8 / G;
+  __shared__ float red[NG][2][G];
   const int lane = threadIdx.x & 31;
+  const int grp = static_cast<int>(threadIdx.x) / (32 * G);
+  const int gl = static_cast<int>(threadIdx.x) % (32 * G);  // thread of the group
   const int64_t nchunk = K / 8;
-  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; row < M;
-       row += warps_total) {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
-    uint4 v[CH];
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * NG;
+  uint4 v[CH], vn[CH];
+  auto load_row = [&](int64_t r, uint4 (&dst)[CH]) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + r * K);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {  // every load of the row in flight before any is used
-      const int64_t idx = lane + 32 * c;
-      v[c] = idx < nchunk ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
-    amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
-    const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (lane == 0) store_scale(s, row, scale, d);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int64_t idx = lane + 32 * c;
-      if (idx < nchunk) {
-        store8<OUT>(v[c], s, rs, row, K, idx, q, q16, d);
-      }
-    }
-  }
-}
-
-// One row per CTA of 256 threads; CH 16-byte chunks per thread (K <= 2048 * CH).  A CTA takes rows
-// blockIdx.x, + gridDim.x, ...; the loads of its next row are issued before the current one is reduced
-// and quantised, so an SM keeps reading while it computes.
-template <int CH, int OUT, class D>
-__global__ void __launch_bounds__(256) quant_cta_rows(const uint16_t* __restrict__ x, int64_t M,
-                                                      int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
-                                                      float* __restrict__ scale, D d) {
-  pdl_enter();
-  __shared__ float red[2][8];
-  const int64_t nchunk = K / 8;
-  uint4 v[CH];
-  auto load_row = [&](int64_t row, uint4 (&dst)[CH]) {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {  // every load of the row in flight before any is used
-      const int64_t idx = threadIdx.x + 256 * c;
-      dst[c] = (row < M && idx < nchunk) ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
+      const int64_t idx = gl + 32 * G * c;
+      dst[c] = (r < M && idx < nchunk) ? ldg_stream(xr + idx) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  load_row(blockIdx.x, v);
+  int64_t row = static_cast<int64_t>(blockIdx.x) * NG + grp;
+  load_row(row, v);
   int buf = 0;
-  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-    uint4 vn[CH];
-    load_row(row + gridDim.x, vn);
+  for (; row < M; row += stride) {
+    load_row(row + stride, vn);
     float amax = 0.0f;
 #pragma unroll
     for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
     amax = warp_max(amax);
-    if ((threadIdx.x & 31) == 0) red[buf][threadIdx.x >> 5] = amax;
-    __syncthreads();  // (red[buf] was last read two rows ago, before the previous barrier)
-    amax = red[buf][0];
+    if constexpr (G > 1) {
+      // (red[grp][buf] was last read two rows ago, before the group's previous barrier)
+      if (lane == 0) red[grp][buf][gl >> 5] = amax;
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(32 * G) : "memory");
+      amax = red[grp][buf][0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[buf][w]);
+      for (int w = 1; w < G; ++w) amax = fmaxf(amax, red[grp][buf][w]);
+    }
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (threadIdx.x == 0) store_scale(s, row, scale, d);
+    if (gl == 0) store_scale(s, row, scale, d);
+    if constexpr (std::is_same<D, RowId>::value) {  // one destination: its row located once
+      uint2* q8 = OUT != 1 ? reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K) : nullptr;
+      uint4* qh = OUT != 0 ? reinterpret_cast<uint4*>(q16 + row * K) : nullptr;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int64_t idx = threadIdx.x + 256 * c;
-      if (idx < nchunk) store8<OUT>(v[c], s, rs, row, K, idx, q, q16, d);
+      for (int c = 0; c < CH; ++c) {
+        const int64_t idx = gl + 32 * G * c;
+        if (idx < nchunk) store8_row<OUT>(v[c], s, rs, idx, q8, qh);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int64_t idx = gl + 32 * G * c;
+        if (idx < nchunk) store8<OUT>(v[c], s, rs, row, K, idx, q, q16, d);
+      }
     }
 #pragma unroll
     for (int c = 0; c < CH; ++c) v[c] = vn[c];
@@ -284,14 +302,13 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
   }
 }
 
-// CTAs of quant_cta_rows<CH, OUT, D> resident per SM (queried once).
-template <int CH, int OUT, class D>
-int cta_rows_per_sm() {
+// CTAs of quant_rows<CH, G, OUT, D> resident per SM (queried once per instantiation).
+template <int CH, int G, int OUT, class D>
+int rows_ctas_per_sm() {
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_cta_rows<CH, OUT, D>, 256, 0) != cudaSuccess ||
-        n < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_rows<CH, G, OUT, D>, 256, 0) != cudaSuccess || n < 1) {
       cudaGetLastError();
       n = 1;
     }
@@ -300,40 +317,44 @@ int cta_rows_per_sm() {
   return per_sm;
 }
 
+template <int CH, int G, int OUT, class D>
+cudaError_t launch_rows(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale, D d,
+                        cudaStream_t stream, int num_sms) {
+  constexpr int NG = 8 / G;
+  const int64_t ctas = (M + NG - 1) / NG;  // as many as rows need, at most as many as are resident at once
+  const int64_t grid = std::min<int64_t>(ctas, static_cast<int64_t>(num_sms) * rows_ctas_per_sm<CH, G, OUT, D>());
+  return launch_pdl(quant_rows<CH, G, OUT, D>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream, x, M, K, q,
+                    q16, scale, d);
+}
+
 template <int OUT, class D>
 cudaError_t launch_quant_t(const uint16_t* x, int64_t M, int64_t K, void* q, uint16_t* q16, float* scale,
                            D d, cudaStream_t stream, int num_sms) {
   if (M == 0) return cudaSuccess;
   const int64_t nchunk = K / 8;
-  const int64_t max_grid = static_cast<int64_t>(num_sms) * 64;
-  if (nchunk <= 32 * 8) {
-    // warp per row, 8 rows per CTA
-    const int64_t blocks = std::min<int64_t>((M + 7) / 8, max_grid);
-    const int ch = static_cast<int>((nchunk + 31) / 32);
-    dim3 g(static_cast<unsigned>(blocks)), b(256);
-    if (ch <= 1) return launch_pdl(quant_warp_rows<1, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-    else if (ch <= 2) return launch_pdl(quant_warp_rows<2, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-    else if (ch <= 4) return launch_pdl(quant_warp_rows<4, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-    else return launch_pdl(quant_warp_rows<8, OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
-  } else {
-    // as many CTAs as are resident at once; each then works through its rows
-    const int ch = static_cast<int>((nchunk + 255) / 256);
-    dim3 b(256);
-    auto grid = [&](int per_sm) {
-      return dim3(static_cast<unsigned>(std::min<int64_t>(M, static_cast<int64_t>(num_sms) * per_sm)));
-    };
-    if (ch <= 2)
-      return launch_pdl(quant_cta_rows<2, OUT, D>, grid(cta_rows_per_sm<2, OUT, D>()), b, 0, stream, x, M, K, q,
-                        q16, scale, d);
-    if (ch <= 4)
-      return launch_pdl(quant_cta_rows<4, OUT, D>, grid(cta_rows_per_sm<4, OUT, D>()), b, 0, stream, x, M, K, q,
-                        q16, scale, d);
-    if (ch <= 8)
-      return launch_pdl(quant_cta_rows<8, OUT, D>, grid(cta_rows_per_sm<8, OUT, D>()), b, 0, stream, x, M, K, q,
-                        q16, scale, d);
-    const dim3 g(static_cast<unsigned>(std::min<int64_t>(M, max_grid)));
-    return launch_pdl(quant_cta_rows_any<OUT, D>, g, b, 0, stream, x, M, K, q, q16, scale, d);
+  if (nchunk > 256 * 8) {  // K > 16384: more than 8 chunks per thread even for a whole CTA per row
+    const dim3 g(static_cast<unsigned>(std::min<int64_t>(M, static_cast<int64_t>(num_sms) * 64)));
+    return launch_pdl(quant_cta_rows_any<OUT, D>, g, dim3(256), 0, stream, x, M, K, q, q16, scale, d);
   }
+  // the narrowest group holding the row in at most 8 chunks per thread ...
+  int G = 1;
+  while (G < 8 && nchunk > 32 * G * 8) G *= 2;
+  // ... widened while the rows alone would occupy fewer CTAs than there are SMs (few rows: latency-bound)
+  while (G < 8 && (M + 8 / G - 1) / (8 / G) < num_sms) G *= 2;
+  if (G == 1) {
+    const int64_t ch = (nchunk + 31) / 32;
+    if (ch <= 1) return launch_rows<1, 1, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+    if (ch <= 2) return launch_rows<2, 1, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+    if (ch <= 4) return launch_rows<4, 1, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+    return launch_rows<8, 1, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+  }
+  if (G == 2) return launch_rows<8, 2, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+  if (G == 4) return launch_rows<8, 4, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+  const int64_t ch = (nchunk + 255) / 256;
+  if (ch <= 1) return launch_rows<1, 8, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+  if (ch <= 2) return launch_rows<2, 8, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+  if (ch <= 4) return launch_rows<4, 8, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
+  return launch_rows<8, 8, OUT>(x, M, K, q, q16, scale, d, stream, num_sms);
 }
 
 }  // namespace
