@@ -88,6 +88,13 @@ def source_digest(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(wl) -> str:
+    """The workload a recorded DRAM figure belongs to: its name and, where the workload has one, the packed
+    weight layout (the contractions read different bytes with and without the fp16 weight copy)."""
+    pack = getattr(wl, "pack", None)
+    return f"{wl.name} [{pack}]" if pack else wl.name
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture (profiles/ncu_traffic.md), if the
     kernel sources are unchanged since; else None."""
@@ -972,7 +979,7 @@ def run_gpu(args):
     else:
         achieved = wl.alg_flops[dom] / dur_s / 1e12
         peak, unit = peaks["bf16_tflops"] * getattr(wl, "tensor_peak_ratio", 1.0), "TFLOP/s"
-    traffic = recorded_traffic(dom, wl.name)
+    traffic = recorded_traffic(dom, traffic_key(wl))
     roofline = {"bound": wl.bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": traffic, "kernel": dom, "peak_source": (f"{peaks['source']} (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback") +
