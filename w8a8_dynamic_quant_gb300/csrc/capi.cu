@@ -216,7 +216,7 @@ w8a8_status run_gemm(GemmArgs a, void* ws, const GemmWs& L, cudaStream_t stream,
   const bool tc_rows = L.dec > L.a16;
   uint16_t* a16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.a16);
   const void* b16 = tc_rows ? pack_f16(a.packed, a.E, a.N, a.K, a.pack_flags) : nullptr;
-  if (b16 != nullptr) {  // the packed fp16 weight copy (dense: CTA pairs; grouped: clusters of two)
+  if (b16 != nullptr) {  // the packed fp16 weight copy (CTA pairs, dense or grouped)
     if (w8a8_status e = cuda_status(launch_s8_to_f16(a.q, a16, a.R * a.K, stream, sms))) return e;
     t_last_engine = W8A8_ENGINE_TC;
     return cuda_status(launch_tc_gemm(a, a16, b16, sms, stream));

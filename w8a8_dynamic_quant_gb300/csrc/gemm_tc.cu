@@ -17,23 +17,22 @@
 // int32 registers while the MMA fills the other one.
 //
 // Data movement.  Both operands are K-major FP16 tiles brought in by TMA
-// (cp.async.bulk.tensor, 128-byte swizzle) into a 4-stage ring: A = 128
-// activation rows x 64 K, B = 256 weight rows x 64 K (48 KB per stage).  One
-// elected lane of the MMA warp issues tcgen05.mma M=128 N=256 K=16 four times per stage.
-//
-// Clusters of two CTAs.  The CTAs of a cluster are scheduled together and
-// work on neighbouring tiles that share one operand: for m-blocks 2p and
-// 2p+1 of an expert at one n-block the shared operand is the 256-row weight
-// block; an expert with an odd number of m-blocks leaves its last m-block,
-// and for it the pair takes n-blocks 2j and 2j+1 and shares the 128-row
-// activation block.  Each CTA loads its whole stage itself with plain tensor
-// copies; the copy of the shared operand that lands second is served from L2,
-// because both CTAs request it at about the same time.  The CTAs exchange
-// nothing: each stage is freed by its own CTA's MMA commit.
+// (cp.async.bulk.tensor, 128-byte swizzle).  A tile is 256 rows of one expert
+// x 256 weight rows (dense: one expert of R rows), computed on a CTA pair
+// (tcgen05 cta_group::2): the even CTA holds activation rows [0,128) and
+// weight rows [0,128) of every 64-deep stage, the odd CTA rows [128,256) and
+// weight rows [128,256), 32 KB per CTA and stage, six stages.  One elected
+// lane of the even CTA's MMA warp issues tcgen05.mma M=256 N=256 K=16 over
+// both CTAs' shared memory four times per stage; each CTA's tensor memory
+// receives its 128 rows of the accumulator.  Both CTAs' copies complete on
+// the even CTA's full barrier; the MMA commit frees the stage in both CTAs;
+// both CTAs' epilogues release an accumulator on the even CTA's barrier.  The
+// second 128 rows of an expert's last tile may lie past its rows: computed,
+// not stored.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over output tiles):
 //   warp 0     TMA producer
-//   warp 1     TMEM owner and MMA issuer
+//   warp 1     TMEM owner and (even CTA) MMA issuer
 //   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4).. and one half
 //              (128 columns) of the tile; each thread owns one output row.
 // Every mbarrier wait is bounded (%globaltimer, 2 s): on expiry the CTA sets
@@ -46,15 +45,10 @@ namespace w8a8 {
 
 namespace {
 
-constexpr int TC_BM = 128;
 constexpr int TC_BN = 256;
 constexpr int TC_BK = 64;  // fp16 elements = 128 bytes = one swizzle row
-constexpr int TC_STAGES = 4;
 constexpr int TC_GROUP_N = 16;  // n-blocks per rasterisation group
 constexpr int TC_KB_PER_CHUNK = kChunkK / TC_BK;  // 16
-constexpr uint32_t TC_A_BYTES = TC_BM * TC_BK * 2;
-constexpr uint32_t TC_B_BYTES = TC_BN * TC_BK * 2;
-constexpr uint32_t TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
 constexpr int TC_THREADS = 320;
 constexpr int TC_EPI_WARPS = 8;
 constexpr uint32_t TC_TMEM_COLS = 512;  // two 256-column fp32 accumulators
@@ -62,53 +56,9 @@ constexpr int TC_CLUSTER = 2;
 constexpr uint16_t TC_PAIR_MASK = 0x3;
 constexpr int kMaxE = 1024;
 
-// kind::f16 instruction descriptor: D = F32, A = B = F16, both K-major, N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(TC_BN >> 3) << 17) | (uint32_t(TC_BM >> 4) << 24);
-
 using namespace tc;
 
 __device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
-
-struct TileInfo {
-  int e, mb, nb, cnt;
-  int64_t row0;  // first global row of the tile (into the [R,K] activation matrix)
-};
-
-// Work units (tile pairs) of an expert with `cnt` rows: pairs of m-blocks at
-// every n-block, then pairs of n-blocks for a leftover odd m-block.
-__host__ __device__ __forceinline__ int pair_units(int cnt, int NB) {
-  const int mblocks = (cnt + TC_BM - 1) / TC_BM;
-  return (mblocks >> 1) * NB + (mblocks & 1) * ((NB + 1) >> 1);
-}
-
-// Tile of CTA `rank` (0 or 1) of the cluster for work unit t.  The second tile
-// of a unit may lie past the expert's n-blocks: it is computed and not stored.
-__device__ __forceinline__ TileInfo decode_tile(int t, int E, int NB, const int* tile_prefix, const int* row_off,
-                                                int rank) {
-  const int lo = expert_of(t, E, tile_prefix);
-  TileInfo ti;
-  ti.e = lo;
-  const int local = t - tile_prefix[lo];
-  ti.cnt = row_off[lo + 1] - row_off[lo];
-  const int mblocks = (ti.cnt + TC_BM - 1) / TC_BM;
-  const int mpairs = mblocks >> 1;
-  if (local < mpairs * NB) {
-    // Rasterise in groups of up to TC_GROUP_N n-blocks: inside a group the
-    // n-block varies fastest, then the m-block pair, so the clusters in
-    // flight share activation blocks and the group's weight blocks stay
-    // resident in L2 while all m-blocks sweep past them.
-    const int g = local / (mpairs * TC_GROUP_N);
-    const int rem = local - g * mpairs * TC_GROUP_N;
-    const int gn = min(TC_GROUP_N, NB - g * TC_GROUP_N);
-    ti.mb = 2 * (rem / gn) + rank;
-    ti.nb = g * TC_GROUP_N + rem % gn;
-  } else {
-    ti.mb = mblocks - 1;
-    ti.nb = 2 * (local - mpairs * NB) + rank;
-  }
-  ti.row0 = static_cast<int64_t>(row_off[lo]) + static_cast<int64_t>(ti.mb) * TC_BM;
-  return ti;
-}
 
 // Per-channel factors of a 128-column output segment, staged in shared memory by each epilogue warp for
 // the BF16 epilogue: weight scale, integer bias (static W8A8) and float bias (0 where absent).
@@ -253,233 +203,8 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, int e, int64_t gr, 
   }
 }
 
-template <int MODE>
-__global__ void __cluster_dims__(TC_CLUSTER, 1, 1) __launch_bounds__(TC_THREADS, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[TC_STAGES];
-  __shared__ __align__(8) uint64_t bar_empty[TC_STAGES];
-  __shared__ __align__(8) uint64_t bar_accf[2];
-  __shared__ __align__(8) uint64_t bar_acce[2];
-  __shared__ uint32_t s_tmem_base;
-  __shared__ volatile int s_abort;
-  __shared__ int s_bad;
-  __shared__ int s_tile_prefix[kMaxE + 1];
-  __shared__ int s_row_off[kMaxE + 1];
-  __shared__ int s_warp[TC_THREADS / 32];
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int E = static_cast<int>(a.E);
-  const int64_t N = a.N;
-  const int64_t K = a.K;
-  const int NB = static_cast<int>((N + TC_BN - 1) / TC_BN);
-  const int nkb = static_cast<int>((K + TC_BK - 1) / TC_BK);
-  const int nchunk = (nkb + TC_KB_PER_CHUNK - 1) / TC_KB_PER_CHUNK;
-
-  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t stage_base = smem_u32(stages);
-  uint32_t rank, cluster_id, nclusters;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cluster_id));
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(nclusters));
-
-  if (tid == 0) {
-    s_abort = 0;
-    s_bad = 0;
-    const PackedHeader* h = static_cast<const PackedHeader*>(a.packed);
-    if (h->magic != kPackMagic || h->version != kPackVersion || h->E != a.E || h->N != a.N || h->K != a.K ||
-        ((h->flags ^ a.pack_flags) & W8A8_PACK_GATE_UP) != 0u || (h->flags & W8A8_PACK_F16) == 0u)
-      s_bad = W8A8_ERR_PACKED;
-    for (int s = 0; s < TC_STAGES; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);  // this CTA's MMA commit
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bar_accf[b]), 1);
-      mbar_init(smem_u32(&bar_acce[b]), TC_EPI_WARPS);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
-                 "r"(TC_TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-
-  // ---- per-expert rows and work units (tile pairs)
-  int tiles_total;
-  const int rows_total = scan_groups<TC_THREADS, kMaxE>(
-      a, E, [NB](int c) { return pair_units(c, NB); }, s_row_off, s_tile_prefix, s_warp, &s_bad, &tiles_total);
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem_base = s_tmem_base;
-  int bad = s_bad;
-  if (rows_total != a.R) bad |= W8A8_ERR_GROUP_LIST << 8;
-  if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, (bad & 0xff) ? (bad & 0xff) : (bad >> 8), 0u);
-  const int my_tiles = bad ? 0 : tiles_total;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int t = static_cast<int>(cluster_id); t < my_tiles && !s_abort; t += static_cast<int>(nclusters)) {
-        const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off, static_cast<int>(rank));
-        const int ya = static_cast<int>(ti.row0);
-        const int yb = static_cast<int>(static_cast<int64_t>(ti.e) * N + static_cast<int64_t>(ti.nb) * TC_BN);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 1u)) break;
-          const uint32_t full = smem_u32(&bar_full[stage]);
-          mbar_expect_tx(full, TC_STAGE_BYTES);
-          const uint32_t sa = stage_base + stage * TC_STAGE_BYTES;
-          const int x = kb * TC_BK;
-          tma_load_2d(sa, &tmA, x, ya, full);
-          tma_load_2d(sa + TC_A_BYTES, &tmB, x, yb, full);
-          if (++stage == TC_STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // Drain: every stage's last fill has been consumed, so no copy into this CTA is still in flight
-      // when it leaves.
-      for (int i = 0; i < TC_STAGES && !s_abort; ++i) {
-        if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, a.status, 5u)) break;
-        if (++stage == TC_STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer (whole warp, elected lane)
-    {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_count = 0;
-      for (int t = static_cast<int>(cluster_id); t < my_tiles && !s_abort; t += static_cast<int>(nclusters)) {
-        for (int c = 0; c < nchunk && !s_abort; ++c) {
-          const uint32_t b = acc_count & 1u;
-          const uint32_t use = acc_count >> 1;
-          if (!warp_wait(smem_u32(&bar_acce[b]), (use & 1u) ^ 1u, &s_abort, a.status, 2u)) break;
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + b * TC_BN;
-          const int kb_end = min(nkb, (c + 1) * TC_KB_PER_CHUNK);
-          bool ok = true;
-          for (int kb = c * TC_KB_PER_CHUNK; kb < kb_end; ++kb) {
-            if (!warp_wait(smem_u32(&bar_full[stage]), phase, &s_abort, a.status, 3u)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sa = stage_base + stage * TC_STAGE_BYTES;
-            const uint64_t adesc = smem_desc_sw128(sa);
-            const uint64_t bdesc = smem_desc_sw128(sa + TC_A_BYTES);
-#pragma unroll
-            for (int k = 0; k < TC_BK / 16; ++k) {
-              // +32 bytes per 16-element step along K inside the swizzled row
-              tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc,
-                     (kb > c * TC_KB_PER_CHUNK || k > 0) ? 1u : 0u);
-            }
-            tc_commit(smem_u32(&bar_empty[stage]));  // frees the stage
-            if (++stage == TC_STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          tc_commit(smem_u32(&bar_accf[b]));
-          ++acc_count;
-          if (!ok) break;
-        }
-      }
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;         // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;  // which 128-column half of the tile
-    const int r_loc = 32 * q + lane;
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-    uint32_t acc_count = 0;
-    for (int t = static_cast<int>(cluster_id); t < my_tiles && !s_abort; t += static_cast<int>(nclusters)) {
-      const TileInfo ti = decode_tile(t, E, NB, s_tile_prefix, s_row_off, static_cast<int>(rank));
-      int sums[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) sums[i] = 0;
-      bool ok = true;
-      for (int c = 0; c < nchunk; ++c) {
-        const uint32_t b = acc_count & 1u;
-        const uint32_t use = acc_count >> 1;
-        int got = 0;
-        if (lane == 0) got = mbar_wait(smem_u32(&bar_accf[b]), use & 1u, &s_abort, a.status, 4u) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t col0 = b * TC_BN + half * 128;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + col0 + 32 * j, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sums[32 * j + i] += __float2int_rn(__uint_as_float(v[i]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_acce[b]));
-        ++acc_count;
-      }
-      if (!ok) break;
-
-      const int rows_valid = min(TC_BM, ti.cnt - ti.mb * TC_BM);
-      const int64_t n_base = static_cast<int64_t>(ti.nb) * TC_BN + half * 128;
-      if (r_loc < rows_valid && n_base < N) {
-        store_row<MODE>(a, ti.e, ti.row0 + r_loc, n_base, sums);
-      }
-    }
-  }
-
-  // ---- teardown: on abort, give in-flight copies and MMAs time to land first.
-  // Lanes 1-31 of warps 0 and 1 skipped the single-lane role loops; reconverge
-  // every warp before the block-wide (aligned) barrier, so TMEM is not freed
-  // while epilogue warps still read it.
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (s_abort) {
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 20000000ull) {
-    }
-  }
-  cluster_sync_all();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TC_TMEM_COLS)
-                 : "memory");
-  }
-}
-
 // ---------------------------------------------------------------------------
-// Contraction on CTA pairs (tcgen05 cta_group::2), dense or grouped.  One tile
-// is 256 rows of one expert x 256 columns (the second 128 rows may lie past
-// the expert's rows: computed, not stored); the even CTA of the cluster holds rows [0,128) of A and
-// weight rows [0,128) of B, the odd CTA rows [128,256) and weight rows
-// [128,256), so a stage is 32 KB per CTA and six stages fit (more copies in
-// flight than the four 48 KB stages of the single-CTA tile).  One thread of
-// the even CTA issues tcgen05.mma M=256 N=256 K=16 over both CTAs' shared
-// memory; each CTA's tensor memory receives its 128 rows of the accumulator.
-// Both CTAs' copies complete on the even CTA's full barrier; the MMA commit
-// frees the stage in both CTAs; both CTAs' epilogues release an accumulator
-// on the even CTA's barrier.
+// The contraction on CTA pairs (layout in the file comment).
 constexpr int P_BM = 256;       // rows per pair tile
 constexpr int P_HALF = 128;     // rows of A and of B held by each CTA
 constexpr int P_STAGES = 6;
@@ -560,8 +285,9 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   if (bad && tid == 0 && blockIdx.x == 0) set_status(a.status, (bad & 0xff) ? (bad & 0xff) : (bad >> 8), 0u);
   const int units = bad ? 0 : units_total;
 
-  // Unit t -> expert e, 256-row block mb of the expert, n-block nb; rasterised like the single-CTA
-  // kernel: groups of TC_GROUP_N n-blocks, m-block slower.
+  // Unit t -> expert e, 256-row block mb of the expert, n-block nb; rasterised in groups of TC_GROUP_N
+  // n-blocks (n-block fastest, then the m-block), so the pairs in flight share activation blocks and the
+  // group's weight blocks stay resident in L2 while the expert's m-blocks sweep past them.
   auto tile_of = [&](int t, int& e, int& mb, int& nb) {
     e = expert_of(t, E, s_unit_prefix);
     const int local = t - s_unit_prefix[e];
@@ -701,7 +427,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
   }
 
-  // ---- teardown (as in the single-CTA kernel), then the pair leaves together.
+  // ---- teardown, then the pair leaves together.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -740,12 +466,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MODE, bool PAIR>
+template <int MODE>
 cudaError_t launch_tc_mode(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int grid, size_t smem,
                            cudaStream_t stream) {
-  void (*k)(CUtensorMap, CUtensorMap, GemmArgs);
-  if constexpr (PAIR) k = tc_pair_gemm_kernel<MODE>;
-  else k = tc_gemm_kernel<MODE>;
+  void (*k)(CUtensorMap, CUtensorMap, GemmArgs) = tc_pair_gemm_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   k<<<grid, TC_THREADS, smem, stream>>>(ma, mb, a);
@@ -754,40 +478,21 @@ cudaError_t launch_tc_mode(const CUtensorMap& ma, const CUtensorMap& mb, const G
 
 }  // namespace
 
-// Upper bound on the kernel's work units (tile pairs): every unit holds at
-// least one tile with rows, except the second n-block of a pair past an odd NB.
-static int64_t tc_upper_units(int64_t E, int64_t R, int64_t N, bool grouped) {
-  const int64_t nb = (N + TC_BN - 1) / TC_BN;
-  return ((R + TC_BM - 1) / TC_BM + (grouped ? E : 0)) * ((nb + 1) / 2 + 1);
-}
-
 cudaError_t launch_tc_gemm(const GemmArgs& a, const void* a_f16, const void* b_f16, int num_sms, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (a.group_list == nullptr && a.E == 1 && a.mode != EPI_SWIGLU) {
-    // Dense: 256-row tiles on CTA pairs.  (Grouped contractions stay on the single-CTA tiles: an expert
-    // with an odd number of 128-row blocks would leave half a pair tile idle, about 9 % more work on the
-    // MoE prefill layer, which costs more than the deeper pipeline gains.)
-    if (!make_map(&ma, a_f16, a.R, a.K, P_HALF)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, b_f16, a.E * a.N, a.K, P_HALF)) return cudaErrorInvalidValue;
-    const int64_t units =
-        ((a.R + P_BM - 1) / P_BM + (a.group_list != nullptr ? a.E : 0)) * ((a.N + TC_BN - 1) / TC_BN);
-    const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / TC_CLUSTER));
-    const int grid = static_cast<int>(clusters * TC_CLUSTER);
-    const size_t smem = static_cast<size_t>(P_STAGES) * P_STAGE_BYTES + 1024;
-    if (a.mode == EPI_ACC) return launch_tc_mode<EPI_ACC, true>(ma, mb, a, grid, smem, stream);
-    return launch_tc_mode<EPI_BF16, true>(ma, mb, a, grid, smem, stream);
-  }
-  if (!make_map(&ma, a_f16, a.R, a.K, TC_BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, b_f16, a.E * a.N, a.K, TC_BN)) return cudaErrorInvalidValue;
-  const int64_t units = tc_upper_units(a.E, a.R, a.N, a.group_list != nullptr);
+  if (!make_map(&ma, a_f16, a.R, a.K, P_HALF)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, b_f16, a.E * a.N, a.K, P_HALF)) return cudaErrorInvalidValue;
+  // work units: 256-row blocks of every expert (at most one partial block per expert) x n-blocks
+  const int64_t units =
+      ((a.R + P_BM - 1) / P_BM + (a.group_list != nullptr ? a.E : 0)) * ((a.N + TC_BN - 1) / TC_BN);
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, num_sms / TC_CLUSTER));
   const int grid = static_cast<int>(clusters * TC_CLUSTER);
-  const size_t smem = static_cast<size_t>(TC_STAGES) * TC_STAGE_BYTES + 1024;
+  const size_t smem = static_cast<size_t>(P_STAGES) * P_STAGE_BYTES + 1024;
   switch (a.mode) {
-    case EPI_ACC: return launch_tc_mode<EPI_ACC, false>(ma, mb, a, grid, smem, stream);
-    case EPI_SWIGLU: return launch_tc_mode<EPI_SWIGLU, false>(ma, mb, a, grid, smem, stream);
-    default: return launch_tc_mode<EPI_BF16, false>(ma, mb, a, grid, smem, stream);
+    case EPI_ACC: return launch_tc_mode<EPI_ACC>(ma, mb, a, grid, smem, stream);
+    case EPI_SWIGLU: return launch_tc_mode<EPI_SWIGLU>(ma, mb, a, grid, smem, stream);
+    default: return launch_tc_mode<EPI_BF16>(ma, mb, a, grid, smem, stream);
   }
 }
 
