@@ -64,6 +64,13 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
+// Two values rounded to bf16 (round to nearest even, as f32_to_bf16_bits) in one instruction: lo in bits
+// 0-15, hi in bits 16-31.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 // Four signed bytes -> two f16x2 words holding the same integers exactly.
 // Each byte b is biased to u = b + 128 (xor 0x80), placed as the low mantissa

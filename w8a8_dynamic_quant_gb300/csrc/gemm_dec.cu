@@ -390,19 +390,21 @@ dec_gemm_kernel(const GemmArgs a, const DecWs ws, const __grid_constant__ CUtens
             }
           } else {
             const float sx = s_sx[t];
-            uint32_t h[4];
+            float fv[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-              float fv = has_qb ? dequant_q(sum[r], qb4[r], sx, sw4[r]) : dequant(sum[r], sx, sw4[r]);
-              fv = has_bias ? __fadd_rn(fv, bias4[r]) : fv;
-              h[r] = f32_to_bf16_bits(fv);
+              fv[r] = has_qb ? dequant_q(sum[r], qb4[r], sx, sw4[r]) : dequant(sum[r], sx, sw4[r]);
+              fv[r] = has_bias ? __fadd_rn(fv[r], bias4[r]) : fv[r];
             }
+            const uint2 h = make_uint2(f32x2_to_bf16x2_bits(fv[0], fv[1]), f32x2_to_bf16x2_bits(fv[2], fv[3]));
             uint16_t* dst = static_cast<uint16_t*>(a.out) + t * N + n0;
             if (vec) {
-              __stcg(reinterpret_cast<uint2*>(dst), make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16)));
+              __stcg(reinterpret_cast<uint2*>(dst), h);
             } else {
+              const uint16_t hs[4] = {static_cast<uint16_t>(h.x), static_cast<uint16_t>(h.x >> 16),
+                                      static_cast<uint16_t>(h.y), static_cast<uint16_t>(h.y >> 16)};
               for (int r = 0; r < 4; ++r)
-                if (n0 + r < N) dst[r] = static_cast<uint16_t>(h[r]);
+                if (n0 + r < N) dst[r] = hs[r];
             }
           }
         }
