@@ -294,28 +294,35 @@ mx_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     const uint32_t sfready_even0 = smem_cluster_addr(smem_u32(&bar_sfready[0]), 0);
     uint32_t g = 0;
     bool ok = true;
+    // The group's 16 scale bytes of this lane's rows (weights: rows lane + 32c, c < 4; tokens: c < 6), read
+    // from shared memory once per group as whole 16-byte rows (a warp reads 512 contiguous bytes: no bank
+    // conflict) and kept in registers for the group's four stages.
+    uint4 wv[4], xv[6];
     for (int t = c0; t < units && ok; t += cstep) {
       for (int kb = 0; kb < nkb && ok; ++kb, ++g) {
         const uint32_t grp = g / X_SF_GROUP;
         const uint32_t sl = grp & 1u;
         const int w4 = static_cast<int>(g % X_SF_GROUP);  // which 32-bit word of the group's 16 bytes a row
-        const int got = mbar_wait(smem_u32(&bar_sffull[sl]), (grp >> 1) & 1u, &s_abort, a.status, 12u) ? 1 : 0;
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
+        if (w4 == 0) {  // groups start at kb % 4 == 0 of every tile (nkb % 4 == 0)
+          const int got = mbar_wait(smem_u32(&bar_sffull[sl]), (grp >> 1) & 1u, &s_abort, a.status, 12u) ? 1 : 0;
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          const uint4* sw128 = reinterpret_cast<const uint4*>(sfbuf + sl * X_SF_BYTES);
+          const uint4* sx128 = reinterpret_cast<const uint4*>(sfbuf + sl * X_SF_BYTES + X_SFW_BYTES);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) wv[c] = sw128[32 * c + lane];
+#pragma unroll
+          for (int c = 0; c < 6; ++c) xv[c] = sx128[32 * c + lane];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_sfempty[sl]));  // this warp is done with the group's bytes
         }
-        const uint32_t* sw32 = reinterpret_cast<const uint32_t*>(sfbuf + sl * X_SF_BYTES);
-        const uint32_t* sx32 = reinterpret_cast<const uint32_t*>(sfbuf + sl * X_SF_BYTES + X_SFW_BYTES);
+        auto word = [w4](const uint4& v) { return w4 == 0 ? v.x : w4 == 1 ? v.y : w4 == 2 ? v.z : v.w; };
         // lane i of every quadrant holds, in column c, the scales of row 32c + i (weights: 4 columns, tokens: 6)
-        const uint32_t w0 = sw32[(lane) * 4 + w4], w1 = sw32[(32 + lane) * 4 + w4];
-        const uint32_t w2 = sw32[(64 + lane) * 4 + w4], w3 = sw32[(96 + lane) * 4 + w4];
-        const uint32_t x0 = sx32[(lane) * 4 + w4], x1 = sx32[(32 + lane) * 4 + w4];
-        const uint32_t x2 = sx32[(64 + lane) * 4 + w4], x3 = sx32[(96 + lane) * 4 + w4];
-        const uint32_t x4 = sx32[(128 + lane) * 4 + w4], x5 = sx32[(160 + lane) * 4 + w4];
-        __syncwarp();
-        if (w4 == X_SF_GROUP - 1 || kb == nkb - 1) {  // this warp is done with the group
-          if (lane == 0) mbar_arrive(smem_u32(&bar_sfempty[sl]));
-        }
+        const uint32_t w0 = word(wv[0]), w1 = word(wv[1]), w2 = word(wv[2]), w3 = word(wv[3]);
+        const uint32_t x0 = word(xv[0]), x1 = word(xv[1]), x2 = word(xv[2]), x3 = word(xv[3]);
+        const uint32_t x4 = word(xv[4]), x5 = word(xv[5]);
         const int slot = static_cast<int>(g % X_SF_SLOTS);
         if (g >= X_SF_SLOTS) {  // the slot was last read by the MMAs of stage g - 4
           const uint32_t gp = g - X_SF_SLOTS;
