@@ -21,7 +21,9 @@ quantisation still runs).  Each kernel type is
 also captured on its own over the same sets for the per-kernel breakdown and
 the roofline of the dominant kernel.  The
 `e2e` leg runs the same step through the public Python API with the inputs
-copied from pinned host memory and the result copied back every step.
+copied from pinned host memory and the result copied back every step, the
+copies of one step overlapping the compute of its neighbours (two buffer
+slots, three streams).
 `cpu_baseline` times the CPU oracle on the host cores on a bounded sample.
 `--impl reference` runs that oracle as the reference arm.
 """
@@ -184,6 +186,42 @@ def aggregate(units: float, seconds: float, group=None):
     return float(u.item()), float(s.item())
 
 
+E2E_SLOTS = 2
+E2E_PIPELINE = (f"{E2E_SLOTS} buffer slots; host->device copies, the API calls and the device->host read "
+                "on three streams, so that step i's copies overlap the compute of its neighbours")
+
+
+def run_e2e(torch, wl, steps: int):
+    """`steps` end-to-end steps of a workload through its public API calls, pipelined over E2E_SLOTS
+    device input/output slots: the copy-in of step i waits until step i - E2E_SLOTS has computed (its
+    slot's inputs are free), the compute waits for its inputs and for the read-back of the slot's
+    previous output, the read-back waits for the compute.  Returns after a device synchronize."""
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(E2E_SLOTS)]
+    ev_comp = [torch.cuda.Event() for _ in range(E2E_SLOTS)]
+    ev_out = [torch.cuda.Event() for _ in range(E2E_SLOTS)]
+    s_in.wait_stream(s_comp)
+    s_out.wait_stream(s_comp)
+    for i in range(steps):
+        slot = i % E2E_SLOTS
+        if i >= E2E_SLOTS:
+            s_in.wait_event(ev_comp[slot])
+        with torch.cuda.stream(s_in):
+            wl.e2e_in(slot)
+        ev_in[slot].record(s_in)
+        s_comp.wait_event(ev_in[slot])
+        if i >= E2E_SLOTS:
+            s_comp.wait_event(ev_out[slot])
+        wl.e2e_compute(slot)
+        ev_comp[slot].record(s_comp)
+        s_out.wait_event(ev_comp[slot])
+        with torch.cuda.stream(s_out):
+            wl.e2e_out(slot)
+        ev_out[slot].record(s_out)
+    torch.cuda.synchronize()
+
+
 # --------------------------------------------------------------- workloads --
 
 class Dense:
@@ -248,21 +286,29 @@ class Dense:
     def value(self, units, seconds):
         return units / seconds / 1e12
 
-    # end to end through the public API, host buffers
+    # end to end through the public API, host buffers: per pipeline slot a device input and output and a
+    # pinned host output (the step's compute buffers are shared: the steps compute one after the other)
     def e2e_setup(self, device):
         torch = self.torch
         self.hx = torch.from_numpy(self.d.x.view("int16")).view(torch.bfloat16).pin_memory()
-        self.hy = torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory()
+        self.e2e_slots = [dict(x=torch.empty((self.M, self.K), dtype=torch.bfloat16, device=device),
+                               y=torch.empty((self.M, self.N), dtype=torch.bfloat16, device=device),
+                               hy=torch.empty((self.M, self.N), dtype=torch.bfloat16).pin_memory())
+                          for _ in range(E2E_SLOTS)]
         self.h2d = self.hx.numel() * 2
-        self.d2h = self.hy.numel() * 2
+        self.d2h = self.M * self.N * 2
 
-    def e2e_step(self):
-        st = self.sets[0]
-        st["x"].copy_(self.hx, non_blocking=True)
-        q, s = self.W.w8a8_dynamic_quant(st["x"], st["q"], st["s"])
-        y = self.W.w8a8_quant_matmul(q, s, st["wp"], st["sw"], self.N, st["bias"], st["ws"], st["y"])
-        self.hy.copy_(y, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
+    def e2e_in(self, slot):
+        self.e2e_slots[slot]["x"].copy_(self.hx, non_blocking=True)
+
+    def e2e_compute(self, slot):
+        st, sl = self.sets[0], self.e2e_slots[slot]
+        q, s = self.W.w8a8_dynamic_quant(sl["x"], st["q"], st["s"])
+        self.W.w8a8_quant_matmul(q, s, st["wp"], st["sw"], self.N, st["bias"], st["ws"], sl["y"])
+
+    def e2e_out(self, slot):
+        sl = self.e2e_slots[slot]
+        sl["hy"].copy_(sl["y"], non_blocking=True)
 
     # CPU oracle on `rows` rows of the same workload
     def oracle_units(self, rows):
@@ -310,13 +356,10 @@ class DenseStatic(Dense):
         c.update(workload=self.name, input_scale=self.s_in, input_offset=self.o_in)
         return c
 
-    def e2e_step(self):
-        st = self.sets[0]
-        st["x"].copy_(self.hx, non_blocking=True)
-        q = self.W.w8a8_static_quant(st["x"], self.s_in, self.o_in, st["q"])
-        y = self.W.w8a8_static_quant_matmul(q, st["wp"], st["deq"], st["qb"], st["ws"], st["y"])
-        self.hy.copy_(y, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
+    def e2e_compute(self, slot):
+        st, sl = self.sets[0], self.e2e_slots[slot]
+        q = self.W.w8a8_static_quant(sl["x"], self.s_in, self.o_in, st["q"])
+        self.W.w8a8_static_quant_matmul(q, st["wp"], st["deq"], st["qb"], st["ws"], sl["y"])
 
     def oracle_step(self, rows):
         import oracle
@@ -356,13 +399,10 @@ class DenseMX(Dense):
         else:
             self.W.w8a8_mx_matmul(st["mq"], st["ms"], st["wq"], st["wsc"], st["y"])
 
-    def e2e_step(self):
-        st = self.sets[0]
-        st["x"].copy_(self.hx, non_blocking=True)
-        q, s = self.W.w8a8_mx_quant(st["x"], st["mq"], st["ms"])
-        y = self.W.w8a8_mx_matmul(q, s, st["wq"], st["wsc"], st["y"])
-        self.hy.copy_(y, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
+    def e2e_compute(self, slot):
+        st, sl = self.sets[0], self.e2e_slots[slot]
+        q, s = self.W.w8a8_mx_quant(sl["x"], st["mq"], st["ms"])
+        self.W.w8a8_mx_matmul(q, s, st["wq"], st["wsc"], sl["y"])
 
     def oracle_step(self, rows):
         import oracle
@@ -445,20 +485,29 @@ class MoE:
             self.hx = torch.from_numpy(m.x).pin_memory()
             self.hxs = torch.from_numpy(m.x_scale).pin_memory()
         self.hgl = torch.from_numpy(m.group_list).pin_memory()
-        self.hy = torch.empty((m.R, m.H), dtype=torch.bfloat16).pin_memory()
+        self.e2e_slots = [dict(x=torch.empty_like(self.x), xs=None if self.xs is None else torch.empty_like(self.xs),
+                               gl=torch.empty_like(self.gl), y=torch.empty_like(self.y),
+                               hy=torch.empty((m.R, m.H), dtype=torch.bfloat16).pin_memory())
+                          for _ in range(E2E_SLOTS)]
         self.h2d = self.hx.numel() * self.hx.element_size() + (0 if self.hxs is None else self.hxs.numel() * 4) + \
             self.hgl.numel() * 8
-        self.d2h = self.hy.numel() * 2
+        self.d2h = m.R * m.H * 2
 
-    def e2e_step(self):
-        self.x.copy_(self.hx, non_blocking=True)
+    def e2e_in(self, slot):
+        sl = self.e2e_slots[slot]
+        sl["x"].copy_(self.hx, non_blocking=True)
         if self.hxs is not None:
-            self.xs.copy_(self.hxs, non_blocking=True)
-        self.gl.copy_(self.hgl, non_blocking=True)
-        y = self.W.moe_w13_swiglu_requant_w2(self.x, self.xs, self.gl, self.w13p, self.s13, self.w2p, self.s2,
-                                             self.ws, self.y)
-        self.hy.copy_(y, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
+            sl["xs"].copy_(self.hxs, non_blocking=True)
+        sl["gl"].copy_(self.hgl, non_blocking=True)
+
+    def e2e_compute(self, slot):
+        sl = self.e2e_slots[slot]
+        self.W.moe_w13_swiglu_requant_w2(sl["x"], sl["xs"], sl["gl"], self.w13p, self.s13, self.w2p, self.s2,
+                                         self.ws, sl["y"])
+
+    def e2e_out(self, slot):
+        sl = self.e2e_slots[slot]
+        sl["hy"].copy_(sl["y"], non_blocking=True)
 
     # CPU oracle on a subset of routed rows (tokens = rows / topk)
     def oracle_units(self, rows):
@@ -546,15 +595,17 @@ class MoETokens(MoE):
         if "moe_layer" not in self.step_kernels:
             self.bound = "hbm"
 
-    def launch(self, kernel: str, i: int):
+    def _call(self, kernel, xt, xts, ids, tw, y):
         W = self.W
         if kernel == "moe_layer":
-            W.moe_layer(self.xt, self.xts, self.ids, self.tw, self.w13p, self.s13, self.w2p, self.s2, self.lws,
-                        self.yt)
+            W.moe_layer(xt, xts, ids, tw, self.w13p, self.s13, self.w2p, self.s2, self.lws, y)
         elif kernel == "moe_permute_quant":
-            W.moe_permute_quant(self.xt, self.xts, self.ids, self.m.E, self.rws, out=self.pq_out)
+            W.moe_permute_quant(xt, xts, ids, self.m.E, self.rws, out=self.pq_out)
         else:
-            W.moe_unpermute_combine(self.yr, self.pq_out[3], self.tw, self.cws, self.yc)
+            W.moe_unpermute_combine(self.yr, self.pq_out[3], tw, self.cws, y)
+
+    def launch(self, kernel: str, i: int):
+        self._call(kernel, self.xt, self.xts, self.ids, self.tw, self.yt if kernel == "moe_layer" else self.yc)
 
     def config(self):
         c = super().config()
@@ -572,26 +623,31 @@ class MoETokens(MoE):
             self.hxs = torch.from_numpy(m.x_tok_scale).pin_memory()
         self.hids = torch.from_numpy(m.topk_ids).pin_memory()
         self.htw = torch.from_numpy(m.topk_weights).pin_memory()
-        self.hy = torch.empty((m.T, m.H), dtype=torch.bfloat16).pin_memory()
+        self.e2e_slots = [dict(xt=torch.empty_like(self.xt), xts=None if self.xts is None else torch.empty_like(self.xts),
+                               ids=torch.empty_like(self.ids), tw=torch.empty_like(self.tw),
+                               y=torch.empty_like(self.yt),
+                               hy=torch.empty((m.T, m.H), dtype=torch.bfloat16).pin_memory())
+                          for _ in range(E2E_SLOTS)]
         self.h2d = self.hx.numel() * self.hx.element_size() + (0 if self.hxs is None else self.hxs.numel() * 4) + \
             self.hids.numel() * 8 + self.htw.numel() * 4
-        self.d2h = self.hy.numel() * 2
+        self.d2h = m.T * m.H * 2
 
-    def e2e_step(self):
-        self.xt.copy_(self.hx, non_blocking=True)
+    def e2e_in(self, slot):
+        sl = self.e2e_slots[slot]
+        sl["xt"].copy_(self.hx, non_blocking=True)
         if self.hxs is not None:
-            self.xts.copy_(self.hxs, non_blocking=True)
-        self.ids.copy_(self.hids, non_blocking=True)
-        self.tw.copy_(self.htw, non_blocking=True)
-        if "moe_layer" in self.step_kernels:
-            y = self.W.moe_layer(self.xt, self.xts, self.ids, self.tw, self.w13p, self.s13, self.w2p, self.s2,
-                                 self.lws, self.yt)
-        else:  # profiling runs of the routing calls alone
-            for k in self.step_kernels:
-                self.launch(k, 0)
-            y = self.yc
-        self.hy.copy_(y, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
+            sl["xts"].copy_(self.hxs, non_blocking=True)
+        sl["ids"].copy_(self.hids, non_blocking=True)
+        sl["tw"].copy_(self.htw, non_blocking=True)
+
+    def e2e_compute(self, slot):
+        sl = self.e2e_slots[slot]
+        for k in self.step_kernels:  # the layer, or the routing calls alone in profiling runs
+            self._call(k, sl["xt"], sl["xts"], sl["ids"], sl["tw"], sl["y"])
+
+    def e2e_out(self, slot):
+        sl = self.e2e_slots[slot]
+        sl["hy"].copy_(sl["y"], non_blocking=True)
 
     # CPU oracle on a subset of tokens (units = tokens)
     def oracle_units(self, rows):
@@ -671,19 +727,29 @@ class WeightPrep:
     def value(self, units, seconds):
         return units / seconds / 1e9
 
+    # the packed weights stay on the device (where the contractions read them); the scales come back
     def e2e_setup(self, device):
+        torch = self.torch
         self.hw = [w.cpu().pin_memory() for w in self.w]
-        self.hs = [torch_s.cpu().pin_memory() for torch_s in self.scales]
+        self.e2e_slots = [dict(w=[torch.empty_like(w) for w in self.w], sc=[torch.empty_like(x) for x in self.scales],
+                               hs=[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in self.scales])
+                          for _ in range(E2E_SLOTS)]
         self.h2d = sum(w.numel() * 2 for w in self.hw)
-        self.d2h = sum(x.numel() * 4 for x in self.hs)
+        self.d2h = sum(x.numel() * 4 for x in self.scales)
 
-    def e2e_step(self):
-        for w, hw in zip(self.w, self.hw):
+    def e2e_in(self, slot):
+        for w, hw in zip(self.e2e_slots[slot]["w"], self.hw):
             w.copy_(hw, non_blocking=True)
-        self.launch("quantize_prepack_weight", 0)
-        for sc, hs in zip(self.scales, self.hs):
+
+    def e2e_compute(self, slot):
+        sl = self.e2e_slots[slot]
+        for w, (_, _, _, f), p, sc in zip(sl["w"], self.shapes, self.packed, sl["sc"]):
+            self.W.w8a8_quantize_prepack_weight(w, f, p, sc)
+
+    def e2e_out(self, slot):
+        sl = self.e2e_slots[slot]
+        for sc, hs in zip(sl["sc"], sl["hs"]):
             hs.copy_(sc, non_blocking=True)
-        self.torch.cuda.current_stream().synchronize()
 
     # CPU oracle on `rows` output channels of the first weight (units: algorithmic bytes of those channels)
     def oracle_units(self, rows):
@@ -961,12 +1027,10 @@ def run_gpu(args):
 
     # e2e through the public API with host buffers
     wl.e2e_setup(device)
-    for _ in range(3):
-        wl.e2e_step()
+    run_e2e(torch, wl, 3)
     e2e_steps = 3 if args.quick else max(3, min(args.steps, 200))
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        wl.e2e_step()
+    run_e2e(torch, wl, e2e_steps)
     e2e_s = time.perf_counter() - t0
     e_units, e_seconds = aggregate(wl.units_per_step * e2e_steps, e2e_s)
 
@@ -1011,7 +1075,7 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "int8", "data": "synthetic", "config": wl.config(),
             "roofline": roofline, "clocks": clocks, "gpu_launches": steps * wl.launches_per_step,
             "e2e": {"value": wl.value(e_units, e_seconds), "unit": wl.unit, "h2d_bytes_per_step": wl.h2d,
-                    "d2h_bytes_per_step": wl.d2h},
+                    "d2h_bytes_per_step": wl.d2h, "steps": e2e_steps, "pipeline": E2E_PIPELINE},
             "wall_s_timed_region": t_wall}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(wl, args.cpu_budget)

@@ -50,7 +50,7 @@
 //
 // Warp roles (448 threads, one CTA per SM, persistent over tiles):
 //   warp 0       TMA producer
-//   warp 1       TMEM owner; the even CTA's lane 0 issues the MMAs
+//   warp 1       TMEM owner; one elected lane of the even CTA's warp issues the MMAs
 //   warps 2-5    converters: lane r of warp w widens weight row 32*(w%4)+r
 //   warps 6-13   epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows)
 //                and one half (96 tokens) of the accumulator's columns

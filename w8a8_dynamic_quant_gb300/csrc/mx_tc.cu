@@ -38,7 +38,7 @@
 //
 // Warp roles (448 threads, one CTA per SM, persistent over tiles):
 //   warp 0       TMA producer (operand tiles, scale groups)
-//   warp 1       TMEM owner; the even CTA's lane 0 issues the MMAs
+//   warp 1       TMEM owner; one elected lane of the even CTA's warp issues the MMAs
 //   warps 2-5    scale warps
 //   warps 6-13   epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows)
 //                and one half (96 tokens) of the columns, rounds to BF16 and
