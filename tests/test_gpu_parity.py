@@ -100,6 +100,46 @@ def test_quant_quotients_at_and_near_half_integers():
     assert np.count_nonzero(np.abs(quot - np.rint(quot)) == 0.5) > 500
 
 
+@pytest.mark.parametrize("M,K", [(2437, 16), (4096, 256), (2500, 2064), (3001, 4096), (2433, 8192),
+                                 (2440, 8208)])
+def test_quant_many_rows(M, K):
+    """Row sets that fill every SM several times over, rows of 32 B to 16 KB, row counts that leave the
+    last CTAs with one row fewer; the rows mix random values, exact ties, zeros and extremes."""
+    rng = np.random.default_rng(M + K)
+    x = rng.standard_normal((M, K)).astype(np.float32) * np.float32(3)
+    ks = np.arange(-127, 127, dtype=np.float32)
+    for i in range(0, M, 7):  # every 7th row: quotients exactly on half-integers (s = 2^e)
+        base = np.float32(2.0 ** int(rng.integers(-20, 20)))
+        x[i] = np.resize((ks + np.float32(0.5)) * base, K)
+        x[i, int(rng.integers(0, K))] = np.float32(127) * base
+    x[3] = 0.0
+    x[5] *= np.float32(1e-38)
+    x[M - 1] *= np.float32(1e36)
+    assert_quant_equal(S.to_bf16_bits(x))
+
+
+def test_quant_every_scale_near_half_integers():
+    """One row for every positive finite bf16 absmax (32639 rows, so every scale s = amax / 127 the
+    quantiser can meet): the row holds its absmax and, for each half-integer h = k + 0.5 (k = 0 .. 126),
+    the four bf16 values bracketing h * s, with alternating signs.  These are the quotients where a
+    reciprocal product can round to the wrong side; the codes must still be those of the binary32
+    quotient, for the tiny scales (exact path) as for the rest."""
+    amax_bits = np.arange(1, 0x7F80, dtype=np.uint32)  # 0x0001 .. 0x7F7F
+    amax = (amax_bits << 16).view(np.float32)
+    s = (amax / np.float32(127)).astype(np.float32)
+    h = np.arange(127, dtype=np.float64) + 0.5
+    t = h[None, :] * s[:, None].astype(np.float64)  # exact in binary64
+    lo = (t.astype(np.float32).view(np.uint32) >> 16).astype(np.int64)  # bf16 at or below h * s
+    cand = np.stack([lo - 1, lo, lo + 1, lo + 2], axis=2).reshape(len(amax_bits), -1)
+    cand = np.clip(cand, 0, amax_bits[:, None].astype(np.int64))  # |x| <= amax
+    sign = np.where((np.arange(cand.shape[1]) // 4) % 2 == 1, 0x8000, 0)[None, :]
+    K = 512
+    x = np.zeros((len(amax_bits), K), dtype=np.uint16)
+    x[:, 0] = amax_bits
+    x[:, 1:1 + cand.shape[1]] = (cand | sign).astype(np.uint16)
+    assert_quant_equal(x)
+
+
 def test_quant_empty_is_noop():
     x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     q, s = W.w8a8_dynamic_quant(x)

@@ -25,27 +25,55 @@ namespace w8a8 {
 
 namespace {
 
-// max |x| over 8 bf16 (two per 32-bit word): sign bits cleared, then packed bf16 maxima; the larger
-// half of the result, widened to binary32 (exact).
-__device__ __forceinline__ float absmax8(const uint4& v) {
-  uint32_t m01, m23, m;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(m01) : "r"(v.x & 0x7fff7fffu), "r"(v.y & 0x7fff7fffu));
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(m23) : "r"(v.z & 0x7fff7fffu), "r"(v.w & 0x7fff7fffu));
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
-  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+// Running max |x| over bf16 values, two lanes packed in a 32-bit word: max.xorsign.abs compares the
+// operands' magnitudes and returns the larger one (its sign the XOR of the two signs, so that only the
+// magnitude of the result means anything).  KeepNaN: a NaN operand makes the lane NaN (the pass that
+// finds rows holding a NaN); else it is passed over, as max passes it over (the absmax of such a row).
+template <bool KeepNaN>
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t m;
+  if constexpr (KeepNaN) asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+  else asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+  return m;
+}
+// acc folded with the 8 bf16 of a chunk.
+template <bool KeepNaN>
+__device__ __forceinline__ uint32_t absmax8_acc(const uint4& v, uint32_t acc) {
+  return absmax_bf16x2<KeepNaN>(
+      absmax_bf16x2<KeepNaN>(absmax_bf16x2<KeepNaN>(v.x, v.y), absmax_bf16x2<KeepNaN>(v.z, v.w)), acc);
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+// The larger magnitude of the two lanes, widened to binary32 (exact); NaN if a lane is NaN.
+__device__ __forceinline__ float absmax_of(uint32_t acc) {
+  return fmax_nan(__uint_as_float((acc << 16) & 0x7fff0000u), __uint_as_float(acc & 0x7fff0000u));
 }
 
 // y + 1.5 * 2^23 rounds y (|y| < 2^22) to an integer, ties to even, held in the low mantissa bits: the
 // sum's low byte is the two's-complement int8 code and (sum - 1.5 * 2^23) the code as a float.
 constexpr float kRoundMagic = 12582912.0f;
 
-// The 8 codes of a chunk of 8 bf16 (x[e] = element e), as sums m[e] = code + kRoundMagic.
-// rint(x / s) with the quotient rounded to binary32 first (round half to even), clamped to +-127;
-// s > 0 and rs = the binary32 reciprocal of s, or s = rs = 0 (an all-zero row: every code 0).  y = x * rs is within |x / s| * 2^-23 + 2^-18 <= 2^-15 of
-// the correctly rounded quotient (|x / s| <= 128), so when y is more than 2^-14 from the nearest
-// half-integer both lie strictly inside the same rounding interval and round to the same integer, with
-// |code| <= 127 (|y| <= 127 * (1 + 2^-22)); otherwise (rare), and for non-finite y, the whole chunk
-// takes the quotient itself and the clamp.
+// The 8 codes of a chunk of 8 bf16 (x[e] = element e), as sums m[e] = code + kRoundMagic: rint(x / s)
+// with the quotient rounded to binary32 first (round half to even), clamped to +-127.  s = RN(amax / 127)
+// of the row, rs = RN(1 / s) (0 when s = 0).
+//
+// Fast path, for rows without a NaN whose s is 0 or in [2^-120, FLT_MAX]: the quotient by one
+// correction of the reciprocal product (Markstein's step): y0 = RN(x * rs), r = x - y0 * s (exact, one
+// fma), y = RN(y0 + r * rs).  Over the whole domain the kernel meets -- every positive finite bf16 amax
+// whose s lies in that range and every bf16 x with |x| <= amax, 532 million pairs, negative x by symmetry
+// -- y equals RN(x / s) wherever it decides the code: rint(y) = rint(RN(x / s)) for all of them, checked
+// exhaustively on the GPU against the correctly rounded divide (y0 alone misses 5,959, all at quotients
+// within a few ulps of a half-integer).  |x / s| <= 127 (1 + 2^-23), so no code passes 127 and no clamp
+// is needed.  s = 0 means every x is +-0: y = 0.
+//
+// Other rows (rare): a row holding a NaN (its absmax passes NaNs over) takes the fast path but sends
+// each chunk holding a NaN down the exact path: the binary32 quotient itself, rint, clamp, a NaN quotient
+// giving code 0; a row holding an infinity has s = inf, where every quotient is 0 or NaN: all codes 0;
+// a row with 0 < s < 2^-120 takes the exact path throughout.
+//
 // Two binary32 values in one 64-bit register, for the paired instructions below (each lane of
 // mul/add/fma.rn.f32x2 is the correctly rounded binary32 operation of its own operands).
 __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
@@ -57,37 +85,61 @@ __device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 
-__device__ __forceinline__ void codes8(const uint4& v, float s, float rs, float (&m)[8]) {
+__device__ __forceinline__ void codes8_fast(const uint4& v, float s, float rs, float (&m)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  const uint64_t rs2 = pk2(rs, rs), mg2 = pk2(kRoundMagic, kRoundMagic), nmg2 = pk2(-kRoundMagic, -kRoundMagic),
-                 neg1 = pk2(-1.0f, -1.0f);
-  float dmax = 0.0f;  // max |y - rint(y)| over the chunk; NaN if any y is not finite
+  const uint64_t rs2 = pk2(rs, rs), ns2 = pk2(-s, -s), mg2 = pk2(kRoundMagic, kRoundMagic);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {  // elements 2i, 2i+1 side by side
     const uint64_t x2 = pk2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-    uint64_t y2, m2, r2, t2;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y2) : "l"(x2), "l"(rs2));         // y = x * rs
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(m2) : "l"(y2), "l"(mg2));         // m = y + magic
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r2) : "l"(m2), "l"(nmg2));        // rint(y), exact
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t2) : "l"(r2), "l"(neg1), "l"(y2));  // y - rint(y), exact
-    float t0, t1;
-    upk2(t2, t0, t1);
+    uint64_t y0, r2, y2, m2;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y0) : "l"(x2), "l"(rs2));               // y0 = x * rs
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r2) : "l"(y0), "l"(ns2), "l"(x2));  // r = x - y0 * s, exact
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y2) : "l"(r2), "l"(rs2), "l"(y0));  // y = y0 + r * rs
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(m2) : "l"(y2), "l"(mg2));               // m = rint(y) + magic
     upk2(m2, m[2 * i], m[2 * i + 1]);
-    asm("max.NaN.f32 %0, %0, %1;" : "+f"(dmax) : "f"(fabsf(t0)));
-    asm("max.NaN.f32 %0, %0, %1;" : "+f"(dmax) : "f"(fabsf(t1)));
   }
-  if (__builtin_expect(!(dmax < 0.5f - 0x1p-14f), 0)) {
-    float x[8];
+}
+__device__ __forceinline__ void codes8_exact(const uint4& v, float s, float (&m)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+  for (int e = 0; e < 8; ++e) {
+    const float x = __uint_as_float(e & 1 ? w[e >> 1] & 0xffff0000u : w[e >> 1] << 16);
+    const int r = max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+    m[e] = __fadd_rn(static_cast<float>(r), kRoundMagic);
+  }
+}
+enum RowMode : int { kRowFast = 0, kRowFastNaN = 1, kRowZero = 2, kRowExact = 3 };
+// The mode of a row (see above); nan_row: the row holds a NaN.
+__device__ __forceinline__ int row_mode(float s, bool nan_row) {
+  constexpr float kMaxFinite = 3.4028234663852886e38f;
+  if (s == 0.0f || (s >= 0x1p-120f && s <= kMaxFinite)) return nan_row ? kRowFastNaN : kRowFast;
+  return s > kMaxFinite ? kRowZero : kRowExact;
+}
+struct Codes8 {
+  float m[8];
+};
+__device__ __forceinline__ Codes8 codes8_rare(const uint4& v, float s, float rs, int mode) {
+  Codes8 c;
+  if (mode == kRowFastNaN) {
+    codes8_fast(v, s, rs, c.m);
+    const float a = absmax_of(absmax8_acc<true>(v, 0u));
+    if (a != a) codes8_exact(v, s, c.m);
+  } else if (mode == kRowZero) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int r = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], s))));
-      m[e] = __fadd_rn(static_cast<float>(r), kRoundMagic);
-    }
+    for (int e = 0; e < 8; ++e) c.m[e] = kRoundMagic;
+  } else {
+    codes8_exact(v, s, c.m);
+  }
+  return c;
+}
+// Callers branch on the mode once per row, so that the common rows' chunk loop sees the constant kRowFast.
+__device__ __forceinline__ void codes8(const uint4& v, float s, float rs, int mode, float (&m)[8]) {
+  if (mode == kRowFast) {
+    codes8_fast(v, s, rs, m);
+  } else {
+    const Codes8 c = codes8_rare(v, s, rs, mode);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m[e] = c.m[e];
   }
 }
 
@@ -102,12 +154,16 @@ __device__ __forceinline__ uint2 pack_i8(const float (&m)[8]) {
 
 // the codes as integer-valued fp16 (exact) packed in a uint4.
 __device__ __forceinline__ uint4 pack_f16(const float (&m)[8]) {
+  const uint64_t nmg2 = pk2(-kRoundMagic, -kRoundMagic);
   uint32_t h[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;"
-        : "=r"(h[i])
-        : "f"(__fsub_rn(m[2 * i + 1], kRoundMagic)), "f"(__fsub_rn(m[2 * i], kRoundMagic)));
+  for (int i = 0; i < 4; ++i) {
+    uint64_t c2;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(pk2(m[2 * i], m[2 * i + 1])), "l"(nmg2));  // the codes, exact
+    float lo, hi;
+    upk2(c2, lo, hi);
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[i]) : "f"(hi), "f"(lo));
+  }
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
@@ -154,10 +210,10 @@ struct RowPack {
 // OUT: 0 = int8 codes into q; 1 = the same codes as fp16 into q16; 2 = both (each code computed once).
 // s = rs = 0 (an all-zero row) gives zero codes.
 template <int OUT, class D>
-__device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_t row, int64_t K, int64_t idx,
-                                       void* q, uint16_t* q16, const D& d) {
+__device__ __forceinline__ void store8(const uint4& v, float s, float rs, int mode, int64_t row, int64_t K,
+                                       int64_t idx, void* q, uint16_t* q16, const D& d) {
   float m[8];
-  codes8(v, s, rs, m);
+  codes8(v, s, rs, mode, m);
   uint2 c = make_uint2(0u, 0u);
   uint4 f = make_uint4(0u, 0u, 0u, 0u);
   if constexpr (OUT != 1) c = pack_i8(m);
@@ -172,9 +228,10 @@ __device__ __forceinline__ void store8(const uint4& v, float s, float rs, int64_
 // The same for a plain row (one destination, row m of the output) whose output rows were located once:
 // q8 / q16r point at chunk 0 of the row.
 template <int OUT>
-__device__ __forceinline__ void store8_row(const uint4& v, float s, float rs, int64_t idx, uint2* q8, uint4* q16r) {
+__device__ __forceinline__ void store8_row(const uint4& v, float s, float rs, int mode, int64_t idx, uint2* q8,
+                                           uint4* q16r) {
   float m[8];
-  codes8(v, s, rs, m);
+  codes8(v, s, rs, mode, m);
   if constexpr (OUT != 1) q8[idx] = pack_i8(m);
   if constexpr (OUT != 0) q16r[idx] = pack_f16(m);
 }
@@ -215,6 +272,12 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+// The same with NaN propagated.
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
 
 // Rows in groups of G warps (32 G threads per row), CH 16-byte chunks of 8 bf16 per thread (K <= 256 G CH).
 // A CTA of 256 threads holds 8 / G groups; group g of CTA b takes rows b (8/G) + g, then every
@@ -233,6 +296,7 @@ __global__ void __launch_bounds__(256, 4) quant_rows(const uint16_t* __restrict_
   constexpr bool kPrefetch = CH <= 4;
   constexpr int NG = 8 / G;
   __shared__ float red[NG][2][G];
+  __shared__ float red_nan[NG][G];  // second exchange, rows holding a NaN only
   const int lane = threadIdx.x & 31;
   const int grp = static_cast<int>(threadIdx.x) / (32 * G);
   const int gl = static_cast<int>(threadIdx.x) % (32 * G);  // thread of the group
@@ -253,34 +317,66 @@ __global__ void __launch_bounds__(256, 4) quant_rows(const uint16_t* __restrict_
   for (; row < M; row += stride) {
     if constexpr (kPrefetch) load_row(row + stride, vn);
     else load_row(row, v);
-    float amax = 0.0f;
+    uint32_t am2 = 0u;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) amax = fmaxf(amax, absmax8(v[c]));
-    amax = warp_max(amax);
+    for (int c = 0; c < CH; ++c) am2 = absmax8_acc<true>(v[c], am2);
+    float amax = warp_max_nan(absmax_of(am2));  // NaN if the row holds one
     if constexpr (G > 1) {
       // (red[grp][buf] was last read two rows ago, before the group's previous barrier)
       if (lane == 0) red[grp][buf][gl >> 5] = amax;
       group_sync<G>(grp);
       amax = red[grp][buf][0];
 #pragma unroll
-      for (int w = 1; w < G; ++w) amax = fmaxf(amax, red[grp][buf][w]);
+      for (int w = 1; w < G; ++w) amax = fmax_nan(amax, red[grp][buf][w]);
+    }
+    const bool nan_row = amax != amax;
+    if (nan_row) {  // rare: the absmax over the row's other values (the group's threads all come here)
+      am2 = 0u;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) am2 = absmax8_acc<false>(v[c], am2);
+      amax = warp_max(absmax_of(am2));
+      if constexpr (G > 1) {
+        // (red_nan[grp] was last read before the barrier of this row's first exchange)
+        if (lane == 0) red_nan[grp][gl >> 5] = amax;
+        group_sync<G>(grp);
+        amax = red_nan[grp][0];
+#pragma unroll
+        for (int w = 1; w < G; ++w) amax = fmaxf(amax, red_nan[grp][w]);
+      }
     }
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
+    const int mode = row_mode(s, nan_row);
     if (gl == 0) store_scale(s, row, scale, d);
     if constexpr (std::is_same<D, RowId>::value) {  // one destination: its row located once
       uint2* q8 = OUT != 1 ? reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + row * K) : nullptr;
       uint4* qh = OUT != 0 ? reinterpret_cast<uint4*>(q16 + row * K) : nullptr;
+      if (mode == kRowFast) {
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int64_t idx = gl + 32 * G * c;
-        if (idx < nchunk) store8_row<OUT>(v[c], s, rs, idx, q8, qh);
+        for (int c = 0; c < CH; ++c) {
+          const int64_t idx = gl + 32 * G * c;
+          if (idx < nchunk) store8_row<OUT>(v[c], s, rs, kRowFast, idx, q8, qh);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int64_t idx = gl + 32 * G * c;
+          if (idx < nchunk) store8_row<OUT>(v[c], s, rs, mode, idx, q8, qh);
+        }
       }
     } else {
+      if (mode == kRowFast) {
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int64_t idx = gl + 32 * G * c;
-        if (idx < nchunk) store8<OUT>(v[c], s, rs, row, K, idx, q, q16, d);
+        for (int c = 0; c < CH; ++c) {
+          const int64_t idx = gl + 32 * G * c;
+          if (idx < nchunk) store8<OUT>(v[c], s, rs, kRowFast, row, K, idx, q, q16, d);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int64_t idx = gl + 32 * G * c;
+          if (idx < nchunk) store8<OUT>(v[c], s, rs, mode, row, K, idx, q, q16, d);
+        }
       }
     }
     if constexpr (kPrefetch) {
@@ -297,23 +393,35 @@ __global__ void __launch_bounds__(256) quant_cta_rows_any(const uint16_t* __rest
                                                           int64_t K, void* __restrict__ q, uint16_t* __restrict__ q16,
                                                           float* __restrict__ scale, D d) {
   pdl_enter();
-  __shared__ float red[8];
+  __shared__ float red[2][8];
   const int64_t nchunk = K / 8;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
-    float amax = 0.0f;
-    for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) amax = fmaxf(amax, absmax8(xr[idx]));
-    amax = warp_max(amax);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    uint32_t am2 = 0u;
+    for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) am2 = absmax8_acc<true>(xr[idx], am2);
+    float amax = warp_max_nan(absmax_of(am2));
+    if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = amax;
     __syncthreads();
-    amax = red[0];
+    amax = red[0][0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    for (int w = 1; w < 8; ++w) amax = fmax_nan(amax, red[0][w]);
+    const bool nan_row = amax != amax;
+    if (nan_row) {  // rare: the absmax over the row's other values, from a third read of the row
+      am2 = 0u;
+      for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) am2 = absmax8_acc<false>(xr[idx], am2);
+      amax = warp_max(absmax_of(am2));
+      if ((threadIdx.x & 31) == 0) red[1][threadIdx.x >> 5] = amax;
+      __syncthreads();
+      amax = red[1][0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[1][w]);
+    }
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
+    const int mode = row_mode(s, nan_row);
     if (threadIdx.x == 0) store_scale(s, row, scale, d);
     for (int64_t idx = threadIdx.x; idx < nchunk; idx += 256) {
-      store8<OUT>(xr[idx], s, rs, row, K, idx, q, q16, d);
+      store8<OUT>(xr[idx], s, rs, mode, row, K, idx, q, q16, d);
     }
     __syncthreads();
   }
