@@ -109,7 +109,11 @@ __device__ __forceinline__ float exp_cw(float x_in) {
   const float c5 = __int_as_float(0x3c088889);  // 1/120
   const float c4 = __int_as_float(0x3d2aaaab);  // 1/24
   const float c3 = __int_as_float(0x3e2aaaab);  // 1/6
-  const float n = rintf(__fmul_rn(x, log2e));
+  // n = rint(x * log2e) by the magic-number add (|x * log2e| < 2^22: the sum's low mantissa bits hold n,
+  // rounded half to even as rint rounds), which also gives n as an integer without a conversion
+  const float nm = __fadd_rn(__fmul_rn(x, log2e), 12582912.0f);
+  const float n = __fsub_rn(nm, 12582912.0f);
+  const int ni = __float_as_int(nm) - 0x4b400000;
   float r = __fmaf_rn(-n, ln2_hi, x);
   r = __fmaf_rn(-n, ln2_lo, r);
   float p = c7;
@@ -120,7 +124,6 @@ __device__ __forceinline__ float exp_cw(float x_in) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  const int ni = static_cast<int>(n);
   const int n1 = ni / 2;
   const int n2 = ni - n1;
   const float y = __fmul_rn(__fmul_rn(p, pow2i(n1)), pow2i(n2));
@@ -129,12 +132,14 @@ __device__ __forceinline__ float exp_cw(float x_in) {
   return x_in != x_in ? x_in : lo;
 }
 
-// h = bf16((g * sigmoid(g)) * u), sigmoid(g) = 1 / (1 + exp(-g)).
-__device__ __forceinline__ uint16_t swiglu_bf16(float g, float u) {
+// h = bf16((g * sigmoid(g)) * u), sigmoid(g) = 1 / (1 + exp(-g)) (the correctly rounded reciprocal, the
+// same value as the correctly rounded quotient 1 / (1 + e)); swiglu_f32 stops before the bf16 rounding.
+__device__ __forceinline__ float swiglu_f32(float g, float u) {
   const float e = exp_cw(-g);
-  const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
-  return f32_to_bf16_bits(__fmul_rn(__fmul_rn(g, sig), u));
+  const float sig = __frcp_rn(__fadd_rn(1.0f, e));
+  return __fmul_rn(__fmul_rn(g, sig), u);
 }
+__device__ __forceinline__ uint16_t swiglu_bf16(float g, float u) { return f32_to_bf16_bits(swiglu_f32(g, u)); }
 
 // Dequant epilogue of one element: bf16(((float)acc * sx) * sw (+ bias)).
 __device__ __forceinline__ float dequant(int32_t acc, float sx, float sw) {

@@ -58,8 +58,6 @@ constexpr int kMaxE = 1024;
 
 using namespace tc;
 
-__device__ __forceinline__ float bf16_round(float v) { return bf16_bits_to_f32(f32_to_bf16_bits(v)); }
-
 // Per-channel factors of a 128-column output segment, staged in shared memory by each epilogue warp for
 // the BF16 epilogue: weight scale, integer bias (static W8A8) and float bias (0 where absent).
 struct __align__(16) SegFactors {
@@ -91,6 +89,21 @@ __device__ __forceinline__ void stage_factors(const GemmArgs& a, int e, int64_t 
     for (int i = 0; i < 4; ++i) ok = ok && (f.qb[lane + 32 * i] <= room && -static_cast<int64_t>(f.qb[lane + 32 * i]) <= room);
     const bool all = __all_sync(0xffffffffu, ok);
     if (lane == 0) f.narrow = all ? 1 : 0;
+  }
+}
+
+// The same for the SwiGLU epilogue: columns [n_base, n_base + 128) of W13 hold gate channels j0 + [0,64)
+// and up channels j0 + [0,64), j0 = (n_base / 128) * 64; f.w[c] takes the gate scale of channel j0 + c
+// (c < 64) or the up scale of channel j0 + c - 64, in the original channel order of w_scale.
+__device__ __forceinline__ void stage_factors_swiglu(const GemmArgs& a, int e, int64_t n_base, int lane,
+                                                     SegFactors& f) {
+  const int64_t N = a.N, I = N / 2;
+  const int64_t j0 = (n_base / 128) * kGateUpBlock;
+  const float* sw = a.w_scale + static_cast<int64_t>(e) * N;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;
+    f.w[c] = c < kGateUpBlock ? sw[j0 + c] : sw[I + j0 + c - kGateUpBlock];
   }
 }
 
@@ -174,30 +187,38 @@ __device__ __forceinline__ void store_row(const GemmArgs& a, int e, int64_t gr, 
           if (n_base + 8 * c8 + k < N) dst[8 * c8 + k] = v[k];
       }
     }
-  } else {  // EPI_SWIGLU: columns [0,64) gate j, [64,128) up j, j = n_base/2 + [0,64)
+  } else {  // EPI_SWIGLU: columns [0,64) gate j, [64,128) up j, j = j0 + [0,64); factors staged in fac
     const float sx = a.x_scale[gr];
     const int64_t I = N / 2;
-    const float* sw = a.w_scale + static_cast<int64_t>(e) * N;
     const int64_t j0 = (n_base / 128) * kGateUpBlock;
     uint16_t* dst = static_cast<uint16_t*>(a.out) + gr * I + j0;
     const bool vec = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0u) && ((I & 7) == 0);
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8) {
-      uint16_t v[8];
+      const float4 g0 = reinterpret_cast<const float4*>(fac->w)[2 * c8];
+      const float4 g1 = reinterpret_cast<const float4*>(fac->w)[2 * c8 + 1];
+      const float4 u0 = reinterpret_cast<const float4*>(fac->w + kGateUpBlock)[2 * c8];
+      const float4 u1 = reinterpret_cast<const float4*>(fac->w + kGateUpBlock)[2 * c8 + 1];
+      const float wg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float wu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      uint32_t h[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 8; k += 2) {
         const int jj = 8 * c8 + k;
-        const float gte = bf16_round(dequant(sums[jj], sx, sw[j0 + jj]));
-        const float up = bf16_round(dequant(sums[kGateUpBlock + jj], sx, sw[I + j0 + jj]));
-        v[k] = swiglu_bf16(gte, up);
+        // gate and up of two channels rounded to bf16 (two per instruction), then h in binary32, rounded
+        // to bf16 two at a time
+        const uint32_t gb = f32x2_to_bf16x2_bits(dequant(sums[jj], sx, wg[k]), dequant(sums[jj + 1], sx, wg[k + 1]));
+        const uint32_t ub = f32x2_to_bf16x2_bits(dequant(sums[kGateUpBlock + jj], sx, wu[k]),
+                                                 dequant(sums[kGateUpBlock + jj + 1], sx, wu[k + 1]));
+        const float ha = swiglu_f32(__uint_as_float(gb << 16), __uint_as_float(ub << 16));
+        const float hb = swiglu_f32(__uint_as_float(gb & 0xffff0000u), __uint_as_float(ub & 0xffff0000u));
+        h[k / 2] = f32x2_to_bf16x2_bits(ha, hb);
       }
       if (vec) {
-        reinterpret_cast<uint4*>(dst)[c8] =
-            make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
-                       v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
+        reinterpret_cast<uint4*>(dst)[c8] = make_uint4(h[0], h[1], h[2], h[3]);
       } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) dst[8 * c8 + k] = v[k];
+        for (int k = 0; k < 8; ++k) dst[8 * c8 + k] = static_cast<uint16_t>(h[k / 2] >> (16 * (k & 1)));
       }
     }
   }
@@ -385,9 +406,13 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int e, mb, nb;
       tile_of(t, e, mb, nb);
       SegFactors& fac = s_fac[warp - 2];
+      __syncwarp();  // every lane is done with the previous tile's factors
       if constexpr (MODE == EPI_BF16) {
         // the segment's factors, loaded while the tile's MMAs run (read by this warp only)
         stage_factors(a, e, static_cast<int64_t>(nb) * TC_BN + half * 128, lane, fac);
+        __syncwarp();
+      } else if constexpr (MODE == EPI_SWIGLU) {
+        stage_factors_swiglu(a, e, static_cast<int64_t>(nb) * TC_BN + half * 128, lane, fac);
         __syncwarp();
       }
       int sums[128];
