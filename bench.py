@@ -417,13 +417,20 @@ class DenseMX(Dense):
 class MoE:
     """MoE expert FFN: (quant) -> W13 grouped GEMM + SwiGLU -> requant -> W2 grouped GEMM."""
 
-    def __init__(self, cfg_id: int, device, pack_weights: bool = True, pack: str = "auto"):
+    def __init__(self, cfg_id: int, device, pack_weights: bool = True, pack: str = "auto", scale: int = 1):
         import numpy as np
         import torch
         import w8a8_dynamic_quant_gb300 as W
         from w8a8_dynamic_quant_gb300 import synthetic as S
         self.W, self.torch, self.np = W, torch, np
-        m = S.moe_config(cfg_id, device=str(device))
+        if scale == 1:
+            m = S.moe_config(cfg_id, device=str(device))
+        else:  # a small case of the same layer: T and E divided by `scale` (profiler captures)
+            c = S.CONFIGS[cfg_id]
+            T, E = c["T"] // scale, c["E"] // scale
+            m = S.make_moe(T, c["H"], c["I"], E, c["topk"], c["routing"], c.get("zipf_s", 1.1),
+                           c.get("n_dead", 0) // scale, c["prequant"], 0, str(device),
+                           name=f"{c['name']}_reduced_T{T}_E{E}")
         self.m = m
         self.name = m.name
         self.n_sets = 1
@@ -545,9 +552,10 @@ class MoETokens(MoE):
     top-k weighted combine (one moe_layer call).  The permute and the combine are also timed alone,
     through their own calls, for their HBM rooflines."""
 
-    def __init__(self, cfg_id: int, device, kernels=None, pack: str = "auto"):
+    def __init__(self, cfg_id: int, device, kernels=None, pack: str = "auto", scale: int = 1):
         # the routing kernels alone (profiling) need no packed weights
-        super().__init__(cfg_id, device, pack_weights=kernels is None or "moe_layer" in kernels, pack=pack)
+        super().__init__(cfg_id, device, pack_weights=kernels is None or "moe_layer" in kernels, pack=pack,
+                         scale=scale)
         W, torch, m = self.W, self.torch, self.m
         T, k, H, I, E, R = m.T, m.topk, m.H, m.I, m.E, m.R
         self.name = m.name + "_from_tokens"
@@ -773,7 +781,7 @@ class WeightPrep:
 
 
 def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False, static=False, mx=False,
-                  pack="auto"):
+                  pack="auto", moe_scale=1):
     from w8a8_dynamic_quant_gb300 import synthetic as S
     if prepare:
         return WeightPrep(cfg_id, device)
@@ -781,7 +789,8 @@ def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False
         return DenseMX(cfg_id, device)
     if S.CONFIGS[cfg_id]["kind"] == "dense":
         return DenseStatic(cfg_id, device) if static else Dense(cfg_id, device, pack)
-    return MoETokens(cfg_id, device, kernels, pack) if from_tokens else MoE(cfg_id, device, pack=pack)
+    return (MoETokens(cfg_id, device, kernels, pack, moe_scale) if from_tokens
+            else MoE(cfg_id, device, pack=pack, scale=moe_scale))
 
 
 # -------------------------------------------------------------- the arms --
@@ -940,7 +949,7 @@ def run_gpu(args):
     peaks = load_peaks()
     kernels = args.kernels.split(",") if args.kernels else None
     wl = make_workload(args.workload, device, args.from_tokens, kernels, args.prepare, args.static, args.mx,
-                       args.pack)
+                       args.pack, args.moe_scale)
     step_kernels = getattr(wl, "step_kernels", wl.kernels)
     stream = torch.cuda.current_stream(device)
 
@@ -1116,6 +1125,9 @@ def main(argv=None):
                          "moe_unpermute_combine), for profiler captures")
     ap.add_argument("--quick", action="store_true",
                     help="short run for profiler captures: no clock-sampling hold, 3 e2e steps")
+    ap.add_argument("--moe-scale", type=int, default=1,
+                    help="MoE workloads: T and E divided by this, a small case of the same kernels for "
+                         "profiler captures that collect many metrics (not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
