@@ -355,8 +355,10 @@ W8A8_API int64_t moe_layer_workspace_offset(int64_t T, int64_t k, int64_t H, int
 
 /* Same arguments and result as w8a8_quant_matmul, minus the workspace.  The
  * scratch lives in a fixed 8 MiB device array inside the library (held by every
- * GPU that loads it until exit); problems that need more (roughly M*N > 2M)
- * return W8A8_ERR_WORKSPACE before any launch.  The first call on a device
+ * GPU that loads it until exit): problems whose split-K partial sums do not fit
+ * (roughly M*N > 2M) run without splitting K, and a problem whose per-tile
+ * counters alone do not fit (M*N beyond about 2^31) returns W8A8_ERR_WORKSPACE
+ * before any launch.  The first call on a device
  * looks up the array's address, clears its status word, and should come
  * before any stream capture.  All calls share the array: calls that overlap
  * on the GPU race.  Errors found on the device go to the array's status

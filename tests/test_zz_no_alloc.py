@@ -6,8 +6,9 @@ check, through the C ABI, that two calls in a row give the oracle's output
 bit for bit and the same output as the workspace entry point
 w8a8_quant_matmul, that a device-side error (a packed weight whose header
 does not match the call) reaches the caller through
-w8a8_quant_matmul_noalloc_status, and that a problem too large for the array
-is refused before launch.  Collected last on purpose."""
+w8a8_quant_matmul_noalloc_status, that a problem whose partial sums do not fit
+the array runs without splitting K, and that one whose counters do not fit is
+refused before launch.  Collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -74,9 +75,24 @@ def test_noalloc_reports_a_mismatched_pack_through_its_status_call():
     assert np.array_equal(host_bits(y2), oracle.quant_matmul(q, xs, d.w, d.w_scale, d.bias))
 
 
-def test_noalloc_refuses_problems_larger_than_its_scratch():
+def test_noalloc_runs_problems_whose_partial_sums_do_not_fit():
+    """4096 x 4096 outputs: their int32 partial sums (64 MiB) do not fit the built-in array, so the call
+    runs without splitting K and must still give the oracle's output bit for bit."""
+    lib = _capi.lib()
+    d = S.make_dense(4096, 64, 4096, n_outlier=2, outlier_mult=10.0, bias=True, seed=11)
+    q, xs = oracle.dynamic_quant(d.x)
+    qd, xsd, swd = dev(q), dev(xs), dev(d.w_scale)
+    wp = W.w8a8_prepack_weight(dev(d.w))
+    y = torch.empty((d.M, d.N), dtype=torch.bfloat16, device="cuda")
+    assert _call(lib, qd, xsd, d.M, d.K, wp, swd, d.N, dev_bf16(d.bias), y) == 0
+    assert lib.w8a8_quant_matmul_noalloc_status(torch.cuda.current_stream().cuda_stream) == 0
+    assert np.array_equal(host_bits(y), oracle.quant_matmul(q, xs, d.w, d.w_scale, d.bias))
+
+
+def test_noalloc_refuses_problems_whose_counters_do_not_fit():
     lib = _capi.lib()
     fake = ctypes.c_void_p(256)
-    # 4096 x 4096 int32 partial sums need 64 MiB: more than the built-in array
-    rc = lib.w8a8_quant_matmul_noalloc(fake, fake, 4096, 64, fake, fake, 4096, None, fake, None)
+    # 65536 x 65536 outputs need 4 Mi arrival counters (16 MiB): more than the built-in array; refused
+    # before anything is read or launched
+    rc = lib.w8a8_quant_matmul_noalloc(fake, fake, 65536, 64, fake, fake, 65536, None, fake, None)
     assert rc == _capi.W8A8_ERR_WORKSPACE

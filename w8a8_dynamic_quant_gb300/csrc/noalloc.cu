@@ -12,9 +12,11 @@
 // library keeps until the process exits.
 //
 // Rules of use:
-//   - the array holds kNoAllocScratchBytes; problems whose scratch would not
-//     fit (roughly M * N > 2 million) are rejected with W8A8_ERR_WORKSPACE
-//     before anything is launched;
+//   - the array holds kNoAllocScratchBytes: the status word, the arrival
+//     counters and, when they fit (roughly M * N <= 2 million), the split-K
+//     partial sums; larger problems run without splitting K, and only a
+//     problem whose counters alone would not fit (M * N beyond about 2^31)
+//     is rejected with W8A8_ERR_WORKSPACE before anything is launched;
 //   - the first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current and clears the status
 //     word; make that first call before any stream capture;
@@ -73,13 +75,13 @@ extern "C" W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const
   if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(w_packed) & 255u))
     return W8A8_ERR_ALIGN;
 
-  // scratch layout: status word, partial sums [M,N] int32, one counter per output tile
-  const size_t acc_off = kStatusBytes;
-  const size_t acc_bytes = align_up(static_cast<uint64_t>(M) * N * 4, 256);
-  const size_t count_off = acc_off + acc_bytes;
+  // scratch layout: status word, one counter per output tile, partial sums [M,N] int32 (split-K) when they
+  // fit; without room for them K is not split
+  const size_t count_off = kStatusBytes;
   const int64_t count_len = ((M + 7) / 8) * ((N + 127) / 128);
-  const size_t total = count_off + align_up(static_cast<uint64_t>(count_len) * 4, 256);
-  if (total > kNoAllocScratchBytes) return W8A8_ERR_WORKSPACE;
+  const size_t acc_off = count_off + align_up(static_cast<uint64_t>(count_len) * 4, 256);
+  if (acc_off > kNoAllocScratchBytes) return W8A8_ERR_WORKSPACE;
+  const bool split_room = acc_off + align_up(static_cast<uint64_t>(M) * N * 4, 256) <= kNoAllocScratchBytes;
 
   int dev = 0, major = 0, minor = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -112,7 +114,7 @@ extern "C" W8A8_API w8a8_status w8a8_quant_matmul_noalloc(const int8_t* q, const
   a.out = y;
   a.mode = EPI_BF16;
   a.status = reinterpret_cast<DeviceStatus*>(b);
-  a.ws_acc = reinterpret_cast<int32_t*>(b + acc_off);
+  a.ws_acc = split_room ? reinterpret_cast<int32_t*>(b + acc_off) : nullptr;  // nullptr: the plan keeps K whole
   a.ws_count = reinterpret_cast<uint32_t*>(b + count_off);
   a.ws_count_len = count_len;
   const GemmPlan p = plan_reg_gemm(a, sms);
