@@ -795,6 +795,26 @@ def make_workload(cfg_id, device, from_tokens=False, kernels=None, prepare=False
 
 # -------------------------------------------------------------- the arms --
 
+def cpu_model() -> str:
+    """The host CPU's model as the kernel reports it (x86: "model name"; Arm: implementer and part)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for ln in info.splitlines():
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    arm_parts = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd0c": "Neoverse N1", "0xd49": "Neoverse N2"}
+    part = fields.get("CPU part", "")
+    if part:
+        return f"{arm_parts.get(part, 'Arm')} (implementer {fields.get('CPU implementer', '?')}, part {part})"
+    return "unknown"
+
+
 def time_oracle(wl, budget_s: float, max_rows=None):
     """Time the CPU oracle on row samples of the workload for about budget_s seconds."""
     import oracle
@@ -816,6 +836,7 @@ def time_oracle(wl, budget_s: float, max_rows=None):
         reps += 1
     units = wl.oracle_units(rows) * reps
     return {"value": wl.value(units, total), "unit": wl.unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"{reps} run(s) of {rows} of {wl.oracle_full_rows} rows, {total:.1f} s"}
 
 
@@ -847,7 +868,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic", "config": wl.config(),
-            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": cores, "kind": "oracle", "cpu": cpu_model(),
                              "sample": f"{wl.step_rows} of {wl.oracle_full_rows} rows per step"},
             "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
