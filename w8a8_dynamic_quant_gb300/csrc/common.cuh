@@ -96,11 +96,16 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t v, uint32_t& lo, uint32_t
 // rounded binary32 operation, so the result is fully determined by these steps.
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
 
-// Branch-free: the steps run on x clamped to [-104, 89] (unchanged inside that range, so every result there
-// is the same), and the out-of-range and NaN results are selected at the end; without branches the
-// compiler can interleave the steps of neighbouring elements.
+// Branch-free: the steps run on x clamped to [-104, 89] with NaN propagated.  The clamp alone gives the
+// specified results outside that range: the steps at x = 89 overflow to +inf (e^89 > FLT_MAX) and at
+// x = -104 round to +0 (e^-104 < 2^-150), the results for every x > 89 and x < -104; a NaN runs through
+// the steps and comes out NaN.  (Checked against the form that selects those results explicitly, on
+// every binary32 value in [-112, -100] and [84, 96] and at the infinities.)  Without branches or selects
+// the compiler can interleave the steps of neighbouring elements.
 __device__ __forceinline__ float exp_cw(float x_in) {
-  const float x = fminf(fmaxf(x_in, -104.0f), 89.0f);
+  float x;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(x) : "f"(x_in), "f"(-104.0f));
+  asm("min.NaN.f32 %0, %0, %1;" : "+f"(x) : "f"(89.0f));
   const float log2e = __int_as_float(0x3fb8aa3b);
   const float ln2_hi = __int_as_float(0x3f317200);
   const float ln2_lo = __int_as_float(0x35bfbe8e);
@@ -126,10 +131,7 @@ __device__ __forceinline__ float exp_cw(float x_in) {
   p = __fmaf_rn(p, r, 1.0f);
   const int n1 = ni / 2;
   const int n2 = ni - n1;
-  const float y = __fmul_rn(__fmul_rn(p, pow2i(n1)), pow2i(n2));
-  const float hi = x_in > 89.0f ? __int_as_float(0x7f800000) : y;
-  const float lo = x_in < -104.0f ? 0.0f : hi;
-  return x_in != x_in ? x_in : lo;
+  return __fmul_rn(__fmul_rn(p, pow2i(n1)), pow2i(n2));
 }
 
 // h = bf16((g * sigmoid(g)) * u), sigmoid(g) = 1 / (1 + exp(-g)) (the correctly rounded reciprocal, the
