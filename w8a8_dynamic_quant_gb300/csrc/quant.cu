@@ -62,11 +62,11 @@ constexpr float kRoundMagic = 12582912.0f;
 //
 // Fast path, for rows without a NaN whose s is 0 or in [2^-120, FLT_MAX]: the quotient by one
 // correction of the reciprocal product (Markstein's step): y0 = RN(x * rs), r = x - y0 * s (exact, one
-// fma), y = RN(y0 + r * rs).  Over the whole domain the kernel meets -- every positive finite bf16 amax
-// whose s lies in that range and every bf16 x with |x| <= amax, 532 million pairs, negative x by symmetry
-// -- y equals RN(x / s) wherever it decides the code: rint(y) = rint(RN(x / s)) for all of them, checked
-// exhaustively on the GPU against the correctly rounded divide (y0 alone misses 5,959, all at quotients
-// within a few ulps of a half-integer).  |x / s| <= 127 (1 + 2^-23), so no code passes 127 and no clamp
+// fma), y = RN(y0 + r * rs).  Over the whole domain the kernel meets there -- every positive finite bf16
+// amax whose s lies in that range and every bf16 x with |x| <= amax, 531 million pairs, negative x by
+// symmetry -- rint(y) = rint(RN(x / s)) for every pair, checked exhaustively on the GPU against the
+// correctly rounded divide (rint(y0) misses 5,784 of them, all at quotients within a few ulps of a
+// half-integer).  |x / s| <= 127 (1 + 2^-23), so no code passes 127 and no clamp
 // is needed.  s = 0 means every x is +-0: y = 0.
 //
 // Other rows (rare): a row holding a NaN (its absmax passes NaNs over) takes the fast path but sends
